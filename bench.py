@@ -1,0 +1,319 @@
+"""Decode throughput of the 2.3B lane model on GB300 (batch 1, FP16).
+
+Workload (the single-step microbench): full shape (15 layers, d=4096, 32 q /
+16 KV heads of 128, FFN 7168, vocab 32000, 8 lanes, delay 2), FP16 weights
+N(0, 0.02) from seed 1, KV cache slots 0..511 of every layer filled with
+N(0, 1) FP16 values, one decode step of a random token at position 512.  A
+timed "step" is one such decode step (the whole hot path: 15 layers, the
+delayed lane sum, LM head, argmax); the position is set back to 512 before
+every step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank decodes its own replica on its own GPU (the
+path needs no exchange between GPUs); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "batch-1 decode tokens/s (2.3B lane model, FP16) and % of HBM roofline"
+UNIT = "tokens/s"
+POS = 512
+SEED = 1
+PROFILE = os.path.join(ROOT, "profiles", "decode_kernel_full_p512.txt")
+KERNEL_SRC = os.path.join(ROOT, "decode_persistent_sm_gb300", "csrc", "lf_kernel.cu")
+
+
+def algorithmic_bytes(shape, pos: int) -> int:
+    """Bytes one decode step must move at position `pos`: every parameter but
+    the embedding table (one 8 KB row of it), plus the live KV cache
+    sum_l min(pos+1, W_l) keys * n_kv * head_dim * (K, V) * 2 bytes."""
+    d = shape.d_model
+    weights = (shape.n_params - shape.vocab * d) * 2
+    kv = 0
+    for w in shape.swa_window:
+        keys = pos + 1 if w == 0 else min(pos + 1, w)
+        kv += keys * shape.n_kv_heads * shape.head_dim * 2 * 2
+    return weights + kv
+
+
+def workload_config(shape):
+    return {
+        "workload": "single decode step at position 512 (KV pre-filled N(0,1)), full 2.3B lane "
+                    "model: 15 layers, d_model 4096, 32 q / 16 KV heads x 128, FFN 7168, vocab 32000, "
+                    "8 lanes, DTP delay 2, SWA 1024 on 10 layers",
+        "batch": 1, "position": POS, "n_lanes": shape.n_lanes, "dtp_delay": shape.dtp_delay,
+        "l2": "no flush: inputs larger than L2 (4.4 GB streamed per step vs 129 MB L2)",
+        "seed": SEED,
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        if not shutil.which("nvidia-smi"):
+            return
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        self.proc = subprocess.Popen(
+            ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+             "--format=csv,noheader,nounits", "-lms", "50"],
+            stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        time.sleep(0.3)
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
+
+
+def profile_traffic():
+    """DRAM bytes per launch from the committed ncu summary, or None if the
+    kernel source changed since the counters were taken."""
+    if not os.path.exists(PROFILE):
+        return None
+    kv = {}
+    for line in open(PROFILE):
+        if "=" in line and not line.startswith("#"):
+            k, v = line.split("=", 1)
+            kv[k.strip()] = v.strip()
+    src_hash = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+    if kv.get("kernel_source_sha256_16") != src_hash:
+        return None
+    try:
+        return int(float(kv["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+def peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        return float(json.load(open(path))["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def oracle_rate(shape, blob, kv, tokens, budget_s: float, max_steps: int):
+    """Decode steps/s of the CPU oracle at position 512 on a bounded sample."""
+    import oracle
+    orc = oracle.Oracle(shape, blob)
+    orc.load_kv(kv, POS)
+    n, t0 = 0, time.perf_counter()
+    while n < max_steps:
+        orc.set_pos(POS)
+        orc.step(int(tokens[n % len(tokens)]))
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return n / dt, n, dt, oracle.threads()
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    """The oracle, as it stands, timed on the host cores (rank 0 only)."""
+    import synth
+    if rank != 0:
+        return
+    shape = synth.FULL
+    blob = synth.make_weights(shape, SEED)
+    kv = synth.make_kv(shape, SEED, POS)
+    tokens = synth.make_tokens(SEED, args.steps + args.warmup, shape.vocab)
+    import oracle
+    orc = oracle.Oracle(shape, blob)
+    orc.load_kv(kv, POS)
+    for i in range(args.warmup):
+        orc.set_pos(POS)
+        orc.step(int(tokens[i]))
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        orc.set_pos(POS)
+        orc.step(int(tokens[args.warmup + i]))
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(shape),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+                         "sample": f"{args.steps} decode steps at position {POS} (each step a full "
+                                   "pass of the fp64 oracle over the same workload)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import synth
+    from decode_persistent_sm_gb300 import Engine
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    shape = synth.FULL
+    blob = synth.make_weights(shape, SEED)
+    kv = synth.make_kv(shape, SEED, POS)
+    tokens = synth.make_tokens(SEED + rank, args.steps + args.warmup, shape.vocab)
+
+    stream = torch.cuda.current_stream()
+    eng = Engine.from_shape(shape)
+    eng.set_stream(stream.cuda_stream)
+    eng.load_weights(blob)
+    eng.load_kv(kv, POS)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for i in range(max(args.warmup, 3)):
+        eng.set_position(POS)
+        eng.decode_step_async(int(tokens[i % len(tokens)]))
+    eng.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    launches0 = eng.info()["launches"]
+    ev0.record(stream)
+    for i in range(args.steps):
+        eng.set_position(POS)
+        eng.decode_step_async(int(tokens[args.warmup + i]))
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    eng.synchronize()  # raises if any timed step failed
+    launches = eng.info()["launches"] - launches0
+    total_ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / args.steps
+    value = world * args.steps / (total_ms / 1e3)
+
+    # end to end through the C ABI: token in by value, logits + argmax back
+    # into pinned host memory, every step synchronous
+    n_e2e = min(args.steps, 300)
+    host_logits = torch.empty(shape.vocab, dtype=torch.float32, pin_memory=True)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        eng.set_position(POS)
+        eng.decode_step_into(int(tokens[i]), host_logits.data_ptr())
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = {"value": world * n_e2e / e2e_s, "unit": UNIT, "h2d_bytes_per_step": 4,
+           "d2h_bytes_per_step": shape.vocab * 4 + 4 * 8}
+
+    nbytes = algorithmic_bytes(shape, POS)
+    peak, peak_kind = peak_hbm()
+    achieved = nbytes / (ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": profile_traffic(),
+                "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                "algorithmic_bytes_per_launch": nbytes}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, n, dt, cores = oracle_rate(shape, blob, kv, tokens, args.cpu_budget_s, 200)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{n} decode steps at position {POS} of the same workload ({dt:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp16 weights, fp32 accumulate",
+            "data": "synthetic (seeded N(0,0.02) FP16 weights, N(0,1) KV fill)",
+            "config": workload_config(shape), "roofline": roofline, "cpu_baseline": cpu,
+            "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+            "parallelism": "replicas only" if world > 1 else "1 GPU, 8 lanes = SM groups",
+        }
+        print(json.dumps(line), flush=True)
+    eng.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        if args.steps > 50:
+            args.steps = 20  # each oracle step takes a fraction of a second
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

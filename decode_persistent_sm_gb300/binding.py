@@ -1,0 +1,233 @@
+"""ctypes binding of include/laneformer.h (argument marshalling only)."""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "liblaneformer.so")
+MAX_LAYERS = 64
+
+STATUS = {
+    0: "LF_OK", 1: "LF_ERR_INVALID_ARG", 2: "LF_ERR_OOM", 3: "LF_ERR_CUDA",
+    4: "LF_ERR_NOT_LOADED", 5: "LF_ERR_CTX_OVERFLOW", 6: "LF_ERR_TIMEOUT",
+    7: "LF_ERR_UNSUPPORTED",
+}
+
+# Every function declared in include/laneformer.h with its ctypes signature.
+_vp, _ci, _i32, _f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int32, ctypes.c_float
+_SIGS = {
+    "lf_validate_config": (_ci, [_vp]),
+    "lf_create": (_ci, [_vp, ctypes.POINTER(_vp)]),
+    "lf_load_weights": (_ci, [_vp, _vp, ctypes.c_size_t]),
+    "lf_load_kv": (_ci, [_vp, _vp, ctypes.c_size_t, _ci]),
+    "lf_prefill": (_ci, [_vp, _vp, _ci, _vp, _vp]),
+    "lf_decode_step": (_ci, [_vp, _i32, _vp, _vp]),
+    "lf_synchronize": (_ci, [_vp]),
+    "lf_set_position": (_ci, [_vp, _ci]),
+    "lf_get_position": (_ci, [_vp, ctypes.POINTER(_ci)]),
+    "lf_reset": (_ci, [_vp]),
+    "lf_destroy": (None, [_vp]),
+    "lf_status_string": (ctypes.c_char_p, [_ci]),
+    "lf_set_stream": (_ci, [_vp, _vp]),
+    "lf_get_logits_device": (_ci, [_vp, ctypes.POINTER(_vp)]),
+    "lf_get_argmax_device": (_ci, [_vp, ctypes.POINTER(_vp)]),
+    "lf_read_kv": (_ci, [_vp, _ci, _ci, _ci, _vp, _vp]),
+    "lf_set_timeout_ns": (_ci, [_vp, ctypes.c_uint64]),
+    "lf_debug_skip_arrival": (_ci, [_vp, _ci]),
+    "lf_plan_stats": (_ci, [_vp, _ci, _vp]),
+    "lf_engine_info": (_ci, [_vp, _vp]),
+}
+
+
+class LfConfig(ctypes.Structure):
+    _fields_ = [
+        ("n_layers", _ci), ("d_model", _ci), ("n_q_heads", _ci), ("n_kv_heads", _ci),
+        ("head_dim", _ci), ("ffn_dim", _ci), ("vocab", _ci), ("n_lanes", _ci),
+        ("dtp_delay", _ci), ("ctx_cap", _ci), ("rms_eps", _f32), ("rope_theta", _f32),
+        ("swa_window", _ci * MAX_LAYERS), ("own_lane_immediate", _ci),
+    ]
+
+
+class LaneformerError(RuntimeError):
+    def __init__(self, call: str, code: int):
+        self.code = code
+        super().__init__(f"{call}: {STATUS.get(code, code)}")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Loads liblaneformer.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build the CUDA engine first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def config_from_shape(shape, **overrides) -> LfConfig:
+    """LfConfig from any object with the model-shape attributes."""
+    get = lambda k: overrides.get(k, getattr(shape, k))
+    c = LfConfig()
+    for k in ("n_layers", "d_model", "n_q_heads", "n_kv_heads", "head_dim", "ffn_dim", "vocab",
+              "n_lanes", "dtp_delay", "ctx_cap"):
+        setattr(c, k, int(get(k)))
+    c.rms_eps = float(get("rms_eps"))
+    c.rope_theta = float(get("rope_theta"))
+    for i, w in enumerate(get("swa_window")):
+        c.swa_window[i] = int(w)
+    c.own_lane_immediate = int(overrides.get("own_lane_immediate", getattr(shape, "own_lane_immediate", 0)))
+    return c
+
+
+def _check(call: str, code: int):
+    if code != 0:
+        raise LaneformerError(call, code)
+
+
+def validate_config(cfg: LfConfig) -> int:
+    return load_library().lf_validate_config(ctypes.byref(cfg))
+
+
+def plan_stats(cfg: LfConfig, n_sm: int) -> Tuple[int, np.ndarray]:
+    out = np.zeros(8, dtype=np.int64)
+    rc = load_library().lf_plan_stats(ctypes.byref(cfg), n_sm, out.ctypes.data)
+    return rc, out
+
+
+class Engine:
+    """One decode session on the current CUDA device."""
+
+    def __init__(self, cfg: LfConfig):
+        self._lib = load_library()
+        self.cfg = cfg
+        self.vocab = cfg.vocab
+        h = _vp()
+        _check("lf_create", self._lib.lf_create(ctypes.byref(cfg), ctypes.byref(h)))
+        self._h = h
+
+    @classmethod
+    def from_shape(cls, shape, **overrides) -> "Engine":
+        return cls(config_from_shape(shape, **overrides))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.lf_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        self.close()
+
+    # -- calls ------------------------------------------------------------
+    def load_weights(self, blob: np.ndarray):
+        blob = np.ascontiguousarray(blob)
+        _check("lf_load_weights", self._lib.lf_load_weights(self._h, blob.ctypes.data, blob.nbytes))
+
+    def load_kv(self, kv: np.ndarray, n_pos: int):
+        kv = np.ascontiguousarray(kv)
+        _check("lf_load_kv", self._lib.lf_load_kv(self._h, kv.ctypes.data, kv.nbytes, n_pos))
+
+    def decode_step(self, token: int, logits: bool = True) -> Tuple[Optional[np.ndarray], int]:
+        """Returns (logits or None, argmax)."""
+        am = ctypes.c_int32(-1)
+        out = np.empty(self.vocab, dtype=np.float32) if logits else None
+        rc = self._lib.lf_decode_step(self._h, int(token),
+                                      out.ctypes.data if logits else None, ctypes.byref(am))
+        _check("lf_decode_step", rc)
+        return out, am.value
+
+    def decode_step_into(self, token: int, logits_ptr: int) -> int:
+        """One synchronous step writing the logits to host memory at logits_ptr;
+        returns the argmax."""
+        am = ctypes.c_int32(-1)
+        _check("lf_decode_step", self._lib.lf_decode_step(self._h, int(token), logits_ptr,
+                                                          ctypes.byref(am)))
+        return am.value
+
+    def decode_step_async(self, token: int):
+        """Enqueues one step; results stay on the device."""
+        _check("lf_decode_step", self._lib.lf_decode_step(self._h, int(token), None, None))
+
+    def prefill(self, tokens: Sequence[int], logits: bool = True):
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        am = ctypes.c_int32(-1)
+        out = np.empty(self.vocab, dtype=np.float32) if logits else None
+        rc = self._lib.lf_prefill(self._h, t.ctypes.data, t.size,
+                                  out.ctypes.data if logits else None, ctypes.byref(am))
+        _check("lf_prefill", rc)
+        return out, am.value
+
+    def synchronize(self):
+        _check("lf_synchronize", self._lib.lf_synchronize(self._h))
+
+    def set_position(self, pos: int):
+        _check("lf_set_position", self._lib.lf_set_position(self._h, int(pos)))
+
+    @property
+    def position(self) -> int:
+        v = _ci(0)
+        _check("lf_get_position", self._lib.lf_get_position(self._h, ctypes.byref(v)))
+        return v.value
+
+    def reset(self):
+        _check("lf_reset", self._lib.lf_reset(self._h))
+
+    def set_stream(self, stream_ptr: Optional[int]):
+        _check("lf_set_stream", self._lib.lf_set_stream(self._h, stream_ptr))
+
+    def logits_device_ptr(self) -> int:
+        p = _vp()
+        _check("lf_get_logits_device", self._lib.lf_get_logits_device(self._h, ctypes.byref(p)))
+        return p.value
+
+    def argmax_device_ptr(self) -> int:
+        p = _vp()
+        _check("lf_get_argmax_device", self._lib.lf_get_argmax_device(self._h, ctypes.byref(p)))
+        return p.value
+
+    def read_kv(self, layer: int, kv_head: int, pos: int):
+        k = np.empty(self.cfg.head_dim, dtype=np.float32)
+        v = np.empty(self.cfg.head_dim, dtype=np.float32)
+        _check("lf_read_kv", self._lib.lf_read_kv(self._h, layer, kv_head, pos, k.ctypes.data,
+                                                  v.ctypes.data))
+        return k, v
+
+    def set_timeout_ns(self, ns: int):
+        _check("lf_set_timeout_ns", self._lib.lf_set_timeout_ns(self._h, int(ns)))
+
+    def debug_skip_arrival(self, cta: int):
+        _check("lf_debug_skip_arrival", self._lib.lf_debug_skip_arrival(self._h, int(cta)))
+
+    def info(self) -> dict:
+        out = np.zeros(8, dtype=np.int64)
+        _check("lf_engine_info", self._lib.lf_engine_info(self._h, out.ctypes.data))
+        keys = ["n_sm", "wstream_bytes", "device_bytes", "smem_per_cta", "threads_per_cta",
+                "launches"]
+        return {k: int(v) for k, v in zip(keys, out)}
+
+    def raw_call(self, name: str, *args) -> int:
+        """Status code of a raw C-ABI call on this engine (for tests of error paths)."""
+        return getattr(self._lib, name)(self._h, *args)

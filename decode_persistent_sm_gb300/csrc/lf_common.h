@@ -1,0 +1,71 @@
+// Definitions shared by the host planner, the runtime and the decode kernel.
+#pragma once
+
+#include <stdint.h>
+
+#ifdef __CUDACC__
+#define LF_HD __host__ __device__ __forceinline__
+#else
+#define LF_HD inline
+#endif
+
+namespace lf {
+
+// CTA shape: 8 consumer warps do the arithmetic, 1 producer warp streams
+// weight and KV tiles into a ring of shared-memory stages with bulk copies.
+constexpr int kConsWarps = 8;
+constexpr int kConsThreads = kConsWarps * 32;
+constexpr int kThreads = kConsThreads + 32;
+constexpr int kStageBytes = 32768;
+constexpr int kStages = 6;
+constexpr int kRChunk = 32;        // floats per chunk of the delayed lane sum
+constexpr int kMaxUnitsPerCta = 256;
+constexpr int kMaxORowsPerCta = 256;
+constexpr int kMaxGroup = 4;       // q heads per KV head inside one lane
+
+// Op list: every CTA walks the same list; an op's data differs per CTA.
+enum OpType : int {
+    OP_EMBED = 0,   // x = E[token]
+    OP_ADD = 1,     // x += R[arg]         (waits for the delayed sum arg)
+    OP_NORM = 2,    // h = rmsnorm(x) * gain[arg] (arg < L attn, < 2L ffn, 2L final)
+    OP_QKV = 3,     // q,k,v rows of layer arg, RoPE, KV append; arrives lane barrier A
+    OP_GATEUP = 4,  // gate/up rows of layer arg, SwiGLU into shared memory
+    OP_DOWN = 5,    // down_proj^T rows: partial of sub-block 2*arg+1
+    OP_ATTN = 6,    // split-K attention of layer arg (waits A), arrives lane barrier B
+    OP_OPROJ = 7,   // merge + o_proj^T rows (waits B): partial of sub-block 2*arg
+    OP_REDUCE = 8,  // chunk of R[arg] = sum of all partials of sub-block arg
+    OP_LMHEAD = 9,  // final logits rows and argmax
+};
+LF_HD int op_type(int op) { return op & 0xff; }
+LF_HD int op_arg(int op) { return op >> 8; }
+LF_HD int make_op(int type, int arg) { return type | (arg << 8); }
+
+struct CtaPlan {
+    int lane;      // lane of this CTA
+    int k;         // index inside the lane
+    int S;         // CTAs in the lane
+    int cta0;      // first CTA of the lane
+    int lm_begin;  // first LM-head row
+    int lm_count;
+    long long w_row0;  // first row of this CTA in the weight stream
+};
+
+struct LayerPlan {
+    int qkv_begin, qkv_n;  // QKV row pairs (lane-local pair index)
+    int ffn_begin, ffn_n;  // FFN units (lane-local)
+    int o_begin, o_n;      // o_proj input columns (lane-local)
+};
+
+// Previous keys [lo, p) of a step are split evenly over the lane's S CTAs;
+// the current key p is handled by the last CTA of the lane.
+LF_HD int attn_lo(int p, int window) {
+    return (window > 0 && p - window + 1 > 0) ? p - window + 1 : 0;
+}
+LF_HD void attn_range(int p, int window, int k, int S, int *a, int *b) {
+    const int lo = attn_lo(p, window);
+    const long long n = p - lo;
+    *a = lo + (int)(n * k / S);
+    *b = lo + (int)(n * (k + 1) / S);
+}
+
+}  // namespace lf

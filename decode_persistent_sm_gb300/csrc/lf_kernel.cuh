@@ -1,0 +1,52 @@
+// Parameters of the persistent decode kernel and its launcher.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "laneformer.h"
+#include "lf_common.h"
+
+namespace lf {
+
+struct KParams {
+    // shape
+    int L, D, DH, HQ_L, HKV_L, GL, F_L, V, NL, n_cta, ctx, n_ops, nch, qkv_l;
+    float eps, attn_scale;
+    // this step
+    int pos, token;
+    uint32_t epoch;  // launches since the last reset; counters target epoch * n
+    unsigned long long timeout_ns;
+    int skip_arrive_cta;
+    int window[LF_MAX_LAYERS];
+    // plan
+    const int *ops;
+    const CtaPlan *cta;
+    const LayerPlan *lp;  // [cta][L]
+    // weights
+    const __half *wstream;  // per-CTA row streams, rows of D values
+    const __half *emb;      // [V][D]
+    const __half *gains;    // [2L+1][D]: attn gains, ffn gains, final gain
+    const float2 *rope;     // [ctx][DH/2] (cos, sin)
+    // state
+    __half *kc, *vc;        // [lane][L][HKV_L][ctx][DH]
+    float *qkv;             // [L][NL][qkv_l]
+    float *apart;           // [L][n_cta][HQ_L][DH+2]: acc[DH], m, l
+    float *part;            // [2L][n_cta][D]
+    float *R;               // [2L][D]
+    uint32_t *barA, *barB;  // [L][NL]
+    uint32_t *cnt, *ready;  // [2L]
+    uint32_t *fin;          // [1]
+    float *cand_v;          // [n_cta]
+    int *cand_i;            // [n_cta]
+    float *logits;          // [V]
+    int *argmax;            // [1]
+    uint32_t *err;          // [4]: code, op index, cta, lane
+};
+
+// Dynamic shared memory needed by the kernel for (D, DH); 0 if unsupported.
+size_t decode_smem_bytes(int D, int DH);
+// One decode step; grid = n_cta CTAs (one per SM), cooperative launch.
+cudaError_t launch_decode(const KParams &p, cudaStream_t stream);
+
+}  // namespace lf

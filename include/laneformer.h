@@ -1,0 +1,162 @@
+/*
+ * laneformer.h — C ABI of the GB300 (sm_103a) batch-1 decode engine for the
+ * lane-structured decoder with Delayed Tensor Parallelism.
+ *
+ * The problem these calls serve is the one the pages describe: a single
+ * request decoded one token at a time at batch 1, greedy, in FP16, within a
+ * 4096-token context ("Kog Laneformer 2B generates 3000 tokens per second
+ * thanks to delayed tensor parallelism", section "Performance and
+ * infrastructure"; "Kog Laneformer 2B: the latency-first model behind Kog
+ * Inference Engine", sections "TL;DR" and "Designing the architecture").
+ *
+ * Conventions for every call:
+ *  - Plain C types only; pointers are HOST pointers unless a name says
+ *    "device".  The engine owns all device memory it allocates; the caller
+ *    keeps ownership of every buffer it passes.
+ *  - Every call returns an lf_status.  After LF_ERR_CUDA or LF_ERR_TIMEOUT the
+ *    engine is poisoned: every call but lf_reset and lf_destroy returns that
+ *    status again until lf_reset succeeds.
+ *  - Calls run on the engine stream (default: the legacy stream, or the one
+ *    given to lf_set_stream) and are synchronous unless stated otherwise.
+ *  - One engine per thread; there is no internal locking.
+ */
+#ifndef LANEFORMER_H
+#define LANEFORMER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LF_MAX_LAYERS 64
+
+typedef enum {
+    LF_OK = 0,
+    LF_ERR_INVALID_ARG = 1,   /* bad pointer, size, token id or config value */
+    LF_ERR_OOM = 2,           /* device or host allocation failed */
+    LF_ERR_CUDA = 3,          /* a CUDA call failed (no device, launch error, ...) */
+    LF_ERR_NOT_LOADED = 4,    /* decode or prefill before lf_load_weights */
+    LF_ERR_CTX_OVERFLOW = 5,  /* the position would reach ctx_cap */
+    LF_ERR_TIMEOUT = 6,       /* a bounded device-side wait ran out */
+    LF_ERR_UNSUPPORTED = 7    /* a valid config this build has no kernel for */
+} lf_status;
+
+/*
+ * Model shape and run options.  The lane structure follows "Kog Laneformer
+ * 2B: the latency-first model behind Kog Inference Engine", section
+ * "Designing the architecture": n_lanes lanes, each owning an equal, contiguous
+ * block of query heads (and the KV heads those read, q head h reading KV head
+ * h / (n_q_heads / n_kv_heads)) and an equal block of FFN units.
+ *
+ * Delayed lane sum: sub-block s (2l = attention, 2l+1 = FFN of layer l) reads
+ * the residual e + sum_{u <= s-1-2*dtp_delay} sum_lanes P[u], where P[u] is the
+ * row-parallel o_proj / down_proj output of sub-block u; every pending partial
+ * is added before the final norm.  dtp_delay = 0 is ordinary per-layer
+ * tensor-parallel synchronisation.  (Sections "Hiding overhead" of the blog
+ * and "Architectural decisions" of the news page fix only that the
+ * synchronisation is delayed by 2 layers; this exact form is the reading this
+ * library implements.)
+ */
+typedef struct {
+    int n_layers, d_model, n_q_heads, n_kv_heads, head_dim, ffn_dim, vocab;
+    int n_lanes;             /* lanes = SM groups of one GPU; divides n_q_heads and ffn_dim */
+    int dtp_delay;           /* >= 0, in layers */
+    int ctx_cap;             /* maximum context (positions 0 .. ctx_cap-1) */
+    float rms_eps, rope_theta;
+    int swa_window[LF_MAX_LAYERS]; /* per layer: keys j > p - W; 0 = full causal */
+    int own_lane_immediate;  /* must be 0 (lane adds own partial at once: not built) */
+} lf_config;
+
+typedef struct lf_engine lf_engine;
+
+/* Host-only check of a config (no GPU needed).  LF_ERR_INVALID_ARG for values
+ * that define no model, LF_ERR_UNSUPPORTED for shapes without a kernel
+ * (built: d_model 4096 with head_dim 128, d_model 256 with head_dim 32). */
+lf_status lf_validate_config(const lf_config *cfg);
+
+/* Creates an engine on the current CUDA device: validates the config, plans
+ * the lane -> SM mapping for the device's SM count and allocates the KV cache,
+ * the delayed-sum buffers, the logits and the weight stream.  *out is NULL on
+ * failure. */
+lf_status lf_create(const lf_config *cfg, lf_engine **out);
+
+/* Copies an FP16 weight blob (nbytes = 2 * number of parameters; tensor order
+ * E, per layer [g_attn, Wq, Wk, Wv, Wo, g_ffn, Wg, Wu, Wd], g_f, W_lm; each
+ * matrix row-major [out][in]) to the device and repacks it into the per-SM
+ * streaming layout.  The caller keeps the blob.  Resets the position to 0. */
+lf_status lf_load_weights(lf_engine *e, const void *host_blob, size_t nbytes);
+
+/* Fills KV-cache slots [0, n_pos) of every layer from a host FP16 array in
+ * layout [layer][K|V][pos][kv_head][head_dim] (nbytes must match) and sets the
+ * position to n_pos.  Used to start decoding from a given cache. */
+lf_status lf_load_kv(lf_engine *e, const void *host_kv, size_t nbytes, int n_pos);
+
+/* Decodes n tokens one after another from the current position (prefill by
+ * sequential decode steps, which equals a causal prefill exactly).  logits
+ * (vocab floats, nullable) and argmax (nullable) receive the result of the
+ * last token.  LF_ERR_CTX_OVERFLOW if position + n > ctx_cap (nothing run). */
+lf_status lf_prefill(lf_engine *e, const int32_t *tokens, int n, float *logits, int32_t *argmax);
+
+/* One decode step of `token` at the current position; advances the position.
+ * logits: host array of vocab floats or NULL; argmax: host int32 or NULL
+ * (lowest index among equal maxima).  When both are NULL the step is only
+ * enqueued on the engine stream and the call returns without waiting; its
+ * results stay on the device (lf_get_logits_device, lf_get_argmax_device) and
+ * a device-side error surfaces at the next synchronising call. */
+lf_status lf_decode_step(lf_engine *e, int32_t token, float *logits, int32_t *argmax);
+
+/* Waits for the engine stream and reports a device-side error, if any. */
+lf_status lf_synchronize(lf_engine *e);
+
+/* Position control.  lf_set_position accepts 0 <= pos <= ctx_cap; cache slots
+ * below pos keep whatever they hold. */
+lf_status lf_set_position(lf_engine *e, int pos);
+lf_status lf_get_position(const lf_engine *e, int *pos);
+
+/* Sets the position to 0 and clears the device synchronisation state; also
+ * the way out of a poisoned engine. */
+lf_status lf_reset(lf_engine *e);
+
+void lf_destroy(lf_engine *e);
+const char *lf_status_string(lf_status s);
+
+/* Uses `cuda_stream` (a cudaStream_t owned by the caller, e.g. PyTorch's) for
+ * every later call; NULL selects the legacy default stream. */
+lf_status lf_set_stream(lf_engine *e, void *cuda_stream);
+
+/* Device pointers to the last step's logits (vocab fp32) and argmax (int32);
+ * valid until lf_destroy. */
+lf_status lf_get_logits_device(lf_engine *e, const float **dptr);
+lf_status lf_get_argmax_device(lf_engine *e, const int32_t **dptr);
+
+/* Reads the cached K and V (head_dim values each, as fp32) of `layer`,
+ * global KV head `kv_head` and position `pos` (copy held by the first lane
+ * that reads that head). */
+lf_status lf_read_kv(lf_engine *e, int layer, int kv_head, int pos, float *k, float *v);
+
+/* Limit of every device-side wait, in nanoseconds (default 2e9).  A wait that
+ * runs out makes the step fail with LF_ERR_TIMEOUT instead of hanging. */
+lf_status lf_set_timeout_ns(lf_engine *e, uint64_t ns);
+
+/* Test hook: in the next decode step, CTA `cta` skips its first lane-barrier
+ * arrival (-1 = off), so that the lane's other CTAs time out.  Proves that the
+ * step ends with LF_ERR_TIMEOUT rather than a hang. */
+lf_status lf_debug_skip_arrival(lf_engine *e, int cta);
+
+/* Host-only plan statistics for `n_sm` SMs (no GPU needed): stats[0] = weight
+ * rows in the stream, [1] = min rows per SM, [2] = max rows per SM, [3] = ops
+ * per step, [4] = 1 if every weight row of every lane appears exactly once,
+ * [5] = SMs per lane (smallest), [6] = SMs per lane (largest). */
+lf_status lf_plan_stats(const lf_config *cfg, int n_sm, int64_t stats[8]);
+
+/* Engine facts: [0] SMs used, [1] weight-stream bytes, [2] device bytes
+ * allocated, [3] smem bytes per CTA, [4] threads per CTA, [5] kernel launches
+ * made since creation. */
+lf_status lf_engine_info(const lf_engine *e, int64_t info[8]);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LANEFORMER_H */
