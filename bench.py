@@ -204,6 +204,8 @@ def run_ours(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     shape = synth.FULL
+    if args.layers:  # a smaller model of the same width, for profiler captures only
+        shape = shape.replace(n_layers=args.layers, swa_window=shape.swa_window[:args.layers])
     blob = synth.make_weights(shape, SEED)
     kv = synth.make_kv(shape, SEED, POS)
     tokens = synth.make_tokens(SEED + rank, args.steps + args.warmup, shape.vocab)
@@ -285,7 +287,9 @@ def run_ours(args, world, rank, local):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp16 weights, fp32 accumulate",
             "data": "synthetic (seeded N(0,0.02) FP16 weights, N(0,1) KV fill)",
-            "config": workload_config(shape), "roofline": roofline, "cpu_baseline": cpu,
+            "config": workload_config(shape) if not args.layers else
+            {"workload": f"profiling case: {args.layers} layers of the full width"},
+            "roofline": roofline, "cpu_baseline": cpu,
             "e2e": e2e, "gpu_launches": launches, "clocks": clk,
             "parallelism": "replicas only" if world > 1 else "1 GPU, 8 lanes = SM groups",
         }
@@ -303,6 +307,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: same width with fewer layers (not a bench number)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
