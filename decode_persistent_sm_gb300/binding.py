@@ -40,6 +40,7 @@ _SIGS = {
     "lf_debug_skip_arrival": (_ci, [_vp, _ci]),
     "lf_plan_stats": (_ci, [_vp, _ci, _vp]),
     "lf_engine_info": (_ci, [_vp, _vp]),
+    "lf_decode_step_static_scratch": (_ci, [_vp, _i32, _vp, _vp]),
 }
 
 

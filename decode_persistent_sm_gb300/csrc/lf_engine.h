@@ -1,0 +1,40 @@
+// Engine state shared by the runtime translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <vector>
+
+#include "laneformer.h"
+#include "lf_common.h"
+#include "lf_plan.h"
+
+struct lf_engine {
+    lf_config cfg;
+    lf::Plan plan;
+    int device = 0;
+    cudaStream_t stream = nullptr;
+    // device memory
+    __half *wstream = nullptr, *emb = nullptr, *gains = nullptr, *kc = nullptr, *vc = nullptr;
+    float2 *rope = nullptr;
+    float *qkv = nullptr, *apart = nullptr, *part = nullptr, *R = nullptr, *cand_v = nullptr,
+          *logits = nullptr;
+    int *cand_i = nullptr, *d_ops = nullptr, *d_kvfirst = nullptr;
+    uint32_t *ctr = nullptr;     // barA | barB | cnt | ready | fin
+    uint32_t *status = nullptr;  // [0] argmax, [4..7] error word
+    lf::CtaPlan *d_cta = nullptr;
+    lf::LayerPlan *d_lp = nullptr;
+    size_t n_ctr = 0;
+    // host
+    uint32_t *h_status = nullptr;  // pinned, 8 words
+    int pos = 0;
+    uint32_t epoch = 0;
+    bool loaded = false;
+    lf_status poisoned = LF_OK;
+    unsigned long long timeout_ns = 2000000000ull;
+    int skip_cta = -1;
+    size_t dev_bytes = 0;
+    long long launches = 0;
+    std::vector<void *> allocs;
+};

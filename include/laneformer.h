@@ -145,6 +145,40 @@ lf_status lf_set_timeout_ns(lf_engine *e, uint64_t ns);
  * step ends with LF_ERR_TIMEOUT rather than a hang. */
 lf_status lf_debug_skip_arrival(lf_engine *e, int cta);
 
+/*
+ * Decode step that allocates nothing.  The pages have no counterpart to this
+ * call: it exists for callers that may not call the CUDA allocator while they
+ * decode, e.g. a host that gives the library a fixed device-memory budget up
+ * front and accounts for every byte itself, or a latency-bound serving loop
+ * for which a cudaMalloc (which may synchronise the whole device and stall
+ * its other streams) is not acceptable.  Such a caller creates and loads the
+ * engine beforehand and passes its own output buffers here.
+ *
+ * Same step as lf_decode_step (same kernel, same results, advances the
+ * position, appends to the engine's KV cache), but the step's working memory
+ * (lane-sum partials and sums, q/k/v and attention partials, counters, argmax
+ * candidates, error word) comes from one fixed device array inside the
+ * library, LF_STATIC_SCRATCH_BYTES long, that every GPU which loads this part
+ * of the library keeps until the process exits.  The call makes no
+ * cudaMalloc, cudaFree or other allocating call.
+ *   logits_device: DEVICE array of vocab floats, written by the step.
+ *   argmax_device: DEVICE int32, written by the step.
+ * The engine's device must be the current device.  The first call on a
+ * device looks up the array's device address (once per device); make that
+ * first call before any stream capture.  Every call uses the same array and
+ * finds in it what the previous call left; the call clears the parts that
+ * must start at zero itself.  Calls whose work overlaps on the GPU (on other
+ * streams, or from other engines on the same device) race on the array: issue
+ * them one after another.  Synchronous: waits for the step and reports a
+ * device-side timeout.  Returns LF_ERR_UNSUPPORTED when the engine's working
+ * set does not fit the array (the full 2.3B lane model needs about 80 MB on
+ * 152 SMs), LF_ERR_INVALID_ARG for null outputs or another current device,
+ * and the same statuses as lf_decode_step otherwise.
+ */
+#define LF_STATIC_SCRATCH_BYTES (96u * 1024u * 1024u)
+lf_status lf_decode_step_static_scratch(lf_engine *e, int32_t token, float *logits_device,
+                                        int32_t *argmax_device);
+
 /* Host-only plan statistics for `n_sm` SMs (no GPU needed): stats[0] = weight
  * rows in the stream, [1] = min rows per SM, [2] = max rows per SM, [3] = ops
  * per step, [4] = 1 if every weight row of every lane appears exactly once,
