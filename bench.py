@@ -150,6 +150,52 @@ def oracle_rate(shape, blob, kv, tokens, budget_s: float, max_steps: int):
     return n / dt, n, dt, oracle.threads()
 
 
+OP_NAMES = {0: "embed", 1: "add", 2: "norm", 3: "qkv", 4: "gateup", 5: "down", 6: "attn",
+            7: "oproj", 8: "reduce", 9: "lmhead"}
+
+
+def write_trace(eng, path, tokens, shape):
+    """One traced step at position 512: per op type, the mean over CTAs of the
+    time spent in the op, blocked on cross-CTA counters and blocked on tiles."""
+    eng.trace(True)
+    for i in range(3):
+        eng.set_position(POS)
+        eng.decode_step_async(int(tokens[i]))
+    eng.synchronize()
+    tr, ops = eng.read_trace()
+    eng.trace(False)
+    tr = tr.astype(np.int64)
+    t0 = tr[:, 0, 0].min()
+    step_ns = int(tr[:, -1, 1].max() - t0)
+    dur = tr[:, :, 1] - tr[:, :, 0]
+    by = {}
+    for j, op in enumerate(ops):
+        name = OP_NAMES[int(op) & 0xFF]
+        b = by.setdefault(name, [0.0, 0.0, 0.0, 0])
+        b[0] += dur[:, j].mean()
+        b[1] += tr[:, j, 2].mean()
+        b[2] += tr[:, j, 3].mean()
+        b[3] += 1
+    start_skew = int(tr[:, 0, 0].max() - t0)
+    end_spread = int(tr[:, -1, 1].max() - tr[:, -1, 1].min())
+    lm = [j for j, op in enumerate(ops) if int(op) & 0xFF == 9][0]
+    out = {"step_ns": step_ns, "cta_start_skew_ns": start_skew, "cta_end_spread_ns": end_spread,
+           "lmhead_start_ns_mean": float((tr[:, lm, 0] - t0).mean()),
+           "by_op": {k: {"count": v[3], "mean_ns": v[0], "sync_wait_ns": v[1], "tile_wait_ns": v[2]}
+                     for k, v in by.items()},
+           "per_op": [{"op": OP_NAMES[int(op) & 0xFF], "arg": int(op) >> 8,
+                       "start_ns_mean": float((tr[:, j, 0] - t0).mean()),
+                       "dur_ns_mean": float(dur[:, j].mean()), "dur_ns_max": int(dur[:, j].max()),
+                       "sync_ns_mean": float(tr[:, j, 2].mean()),
+                       "tile_ns_mean": float(tr[:, j, 3].mean())} for j, op in enumerate(ops)]}
+    with open(path, "w") as f:
+        json.dump(out, f, indent=1)
+    print(f"traced step: {step_ns / 1e3:.1f} us; CTA start skew {start_skew / 1e3:.1f} us", file=sys.stderr)
+    for k, v in out["by_op"].items():
+        print(f"  {k:7s} x{v['count']:3d}  {v['mean_ns'] / 1e3:8.1f} us  sync {v['sync_wait_ns'] / 1e3:7.1f}"
+              f"  tiles {v['tile_wait_ns'] / 1e3:7.1f}", file=sys.stderr)
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -215,6 +261,8 @@ def run_ours(args, world, rank, local):
     eng.set_stream(stream.cuda_stream)
     eng.load_weights(blob)
     eng.load_kv(kv, POS)
+    if args.l2_prefetch_kb >= 0:
+        eng.set_l2_prefetch(args.l2_prefetch_kb * 1024)
 
     def barrier():
         if world > 1:
@@ -267,6 +315,9 @@ def run_ours(args, world, rank, local):
     e2e = {"value": world * n_e2e / e2e_s, "unit": UNIT, "h2d_bytes_per_step": 4,
            "d2h_bytes_per_step": shape.vocab * 4 + 4 * 8}
 
+    if args.trace:
+        write_trace(eng, args.trace, tokens, shape)
+
     nbytes = algorithmic_bytes(shape, POS)
     peak, peak_kind = peak_hbm()
     achieved = nbytes / (ms / 1e3) / 1e9
@@ -307,6 +358,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--l2-prefetch-kb", type=int, default=-1,
+                    help="weight-stream L2 prefetch distance per SM (default: the engine's)")
+    ap.add_argument("--trace", default="", help="write a one-step op trace (JSON) to this path")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: same width with fewer layers (not a bench number)")
     args = ap.parse_args()

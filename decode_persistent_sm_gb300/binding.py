@@ -41,6 +41,9 @@ _SIGS = {
     "lf_plan_stats": (_ci, [_vp, _ci, _vp]),
     "lf_engine_info": (_ci, [_vp, _vp]),
     "lf_decode_step_static_scratch": (_ci, [_vp, _i32, _vp, _vp]),
+    "lf_debug_trace": (_ci, [_vp, _ci]),
+    "lf_set_l2_prefetch": (_ci, [_vp, ctypes.c_uint32]),
+    "lf_debug_read_trace": (_ci, [_vp, _vp, ctypes.c_size_t, _vp]),
 }
 
 
@@ -219,6 +222,9 @@ class Engine:
     def set_timeout_ns(self, ns: int):
         _check("lf_set_timeout_ns", self._lib.lf_set_timeout_ns(self._h, int(ns)))
 
+    def set_l2_prefetch(self, bytes_per_sm: int):
+        _check("lf_set_l2_prefetch", self._lib.lf_set_l2_prefetch(self._h, int(bytes_per_sm)))
+
     def debug_skip_arrival(self, cta: int):
         _check("lf_debug_skip_arrival", self._lib.lf_debug_skip_arrival(self._h, int(cta)))
 
@@ -226,8 +232,21 @@ class Engine:
         out = np.zeros(8, dtype=np.int64)
         _check("lf_engine_info", self._lib.lf_engine_info(self._h, out.ctypes.data))
         keys = ["n_sm", "wstream_bytes", "device_bytes", "smem_per_cta", "threads_per_cta",
-                "launches"]
+                "launches", "n_ops"]
         return {k: int(v) for k, v in zip(keys, out)}
+
+    def trace(self, enable: bool = True):
+        _check("lf_debug_trace", self._lib.lf_debug_trace(self._h, 1 if enable else 0))
+
+    def read_trace(self):
+        """(trace [n_sm, n_ops, 4] uint64, ops [n_ops] int32) of the last traced step."""
+        inf = self.info()
+        n_sm, n_ops = inf["n_sm"], inf["n_ops"]
+        out = np.zeros((n_sm, n_ops, 4), dtype=np.uint64)
+        ops = np.zeros(n_ops, dtype=np.int32)
+        _check("lf_debug_read_trace", self._lib.lf_debug_read_trace(
+            self._h, out.ctypes.data, out.size, ops.ctypes.data))
+        return out, ops
 
     def raw_call(self, name: str, *args) -> int:
         """Status code of a raw C-ABI call on this engine (for tests of error paths)."""

@@ -11,17 +11,27 @@
 
 namespace lf {
 
-// CTA shape: 8 consumer warps do the arithmetic, 1 producer warp streams
-// weight and KV tiles into a ring of shared-memory stages with bulk copies.
-constexpr int kConsWarps = 8;
+// CTA shape: 16 streaming warps run the GEMVs over weight tiles that 1
+// producer warp streams into a ring of shared-memory stages with bulk copies;
+// 2 attention warps run split-K attention and the o_proj merge on the side
+// (with their own KV tile buffer); 1 helper warp sums the lane partials.
+constexpr int kConsWarps = 16;
 constexpr int kConsThreads = kConsWarps * 32;
-constexpr int kThreads = kConsThreads + 32;
+constexpr int kAttnWarps = 2;
+constexpr int kAttnThreads = kAttnWarps * 32;
+constexpr int kThreads = kConsThreads + kAttnThreads + 64;
 constexpr int kStageBytes = 32768;
-constexpr int kStages = 6;
+constexpr int kStages = 4;
+constexpr int kAttnBuf = 32768;    // attention group's KV tile buffer
+constexpr int kMaxCtas = 160;      // helper buffer rows (one 128-byte piece per CTA)
 constexpr int kRChunk = 32;        // floats per chunk of the delayed lane sum
 constexpr int kMaxUnitsPerCta = 256;
 constexpr int kMaxORowsPerCta = 256;
 constexpr int kMaxGroup = 4;       // q heads per KV head inside one lane
+constexpr int kMaxLaneCtas = 160;  // CTAs per lane (attention merge weights)
+constexpr int kRedRows = 128;      // GEMV rows reduced per epilogue block
+constexpr int kAttnScores = 528;   // scores per attention tile (q heads x keys)
+constexpr int kMaxChunkHeads = 16; // q heads per attention chunk
 
 // Op list: every CTA walks the same list; an op's data differs per CTA.
 enum OpType : int {
@@ -48,6 +58,7 @@ struct CtaPlan {
     int lm_begin;  // first LM-head row
     int lm_count;
     long long w_row0;  // first row of this CTA in the weight stream
+    long long w_rows;  // rows of this CTA's stream
 };
 
 struct LayerPlan {

@@ -34,7 +34,9 @@ struct lf_engine {
     lf_status poisoned = LF_OK;
     unsigned long long timeout_ns = 2000000000ull;
     int skip_cta = -1;
+    unsigned l2_prefetch_bytes = 128u * 1024u;
     size_t dev_bytes = 0;
     long long launches = 0;
     std::vector<void *> allocs;
+    unsigned long long *trace = nullptr;  // lf_debug_trace buffer (owned separately)
 };

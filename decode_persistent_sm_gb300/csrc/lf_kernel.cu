@@ -4,23 +4,25 @@
 // final norm, the LM head and the argmax.  One CTA runs on every SM; the CTAs
 // of a lane form an SM group ("Kog Laneformer 2B: the latency-first model
 // behind Kog Inference Engine", section "Designing the architecture": 8 lanes,
-// heads spread evenly over them).  Each CTA has
-//   - one producer warp that streams, with bulk asynchronous copies, the
-//     weight rows of its work (in one contiguous per-CTA region) and the KV
-//     tiles it attends over into a ring of shared-memory stages.  Weights do
-//     not depend on activations, so the producer runs ahead of every data
-//     dependency and HBM stays busy while the consumers wait;
-//   - eight consumer warps that walk the same op list: fused RMSNorm + GEMV
-//     with RoPE / KV append (QKV) or SwiGLU (gate/up) in the epilogue, split-K
-//     decode attention with a per-layer window, o_proj / down_proj as
-//     column-slice GEMVs that produce full-width partials, the delayed lane
-//     sum (chunked, fixed summation order) and the vocab GEMV with argmax.
+// heads spread evenly over them).  Each CTA has four roles:
+//   - producer warp: streams the weight rows of its work (one contiguous
+//     per-CTA region) into a ring of shared-memory stages with bulk copies.
+//     Weights do not depend on activations, so it runs ahead of every data
+//     dependency and keeps this SM's share of HBM busy;
+//   - 16 streaming warps: fused RMSNorm + GEMV with RoPE / KV append (QKV) or
+//     SwiGLU (gate/up) in the epilogue, o_proj / down_proj as column-slice
+//     GEMVs that produce full-width partials, the vocab GEMV with argmax;
+//   - 2 attention warps: split-K decode attention with a per-layer window over
+//     their own KV tiles, then the merge of all lane CTAs' attention partials
+//     into this CTA's o_proj inputs; they run beside the streaming warps (the
+//     FFN of a layer does not wait for its attention when the delay is >= 1);
+//   - helper warp: the delayed lane sum, chunk by chunk, in a fixed order.
 // Cross-CTA dependencies are release/acquire counters in global memory.  Lane
 // barriers (QKV -> attention -> o_proj) involve only the CTAs of one lane; the
 // lane sum of sub-block u is waited for only at sub-block u + 1 + 2*delay
 // ("Hiding overhead": communication delayed by two layers).
 // Every wait is bounded by a deadline: when one runs out the CTA records an
-// error, keeps executing the op list without waiting (so its barrier sequence
+// error, keeps executing its op list without waiting (so its barrier sequence
 // stays intact), lets its copies in flight land and exits.
 #include <float.h>
 
@@ -31,40 +33,52 @@ namespace lf {
 
 template <int D, int DH>
 struct Cfg {
-    static constexpr bool kBlockRow = D >= 2048;  // one row spread over all consumer threads
-    static_assert(kBlockRow ? (D % 2048 == 0) : (D == 256), "d_model layout");
-    static constexpr int NCHT = kBlockRow ? D / 2048 : 1;  // 16-byte chunks per thread
-    static constexpr int NX = 8 * NCHT;                     // residual values per thread
-    static constexpr int RPT = kStageBytes / (2 * D);       // weight rows per tile
+    static constexpr int CPR = D / 8;                       // 16-byte chunks per weight row
+    static constexpr bool kBlockRow = CPR >= kConsThreads;  // one row spread over all streamers
+    static_assert(kBlockRow ? (CPR % kConsThreads == 0) : (CPR == 32), "d_model layout");
+    static constexpr int NCHT = kBlockRow ? CPR / kConsThreads : 1;  // chunks per thread
+    static constexpr int NX = 8 * NCHT;                               // residual values per thread
+    static constexpr int STAGES = kBlockRow ? kStages : 4;
+    static constexpr int RPT = kStageBytes / (2 * D);                 // weight rows per tile
     static_assert(!kBlockRow || RPT == 4, "block-row GEMV assumes 4 rows per tile");
-    static_assert(RPT <= 64, "reduction buffer");
-    static constexpr int KPT = (kStageBytes / 2) / (2 * DH);  // keys per attention tile
-    static constexpr int TPK = DH / 16;                       // threads per key (scores)
-    static constexpr int KPP = kConsThreads / TPK;            // keys per score pass
-    static constexpr int GLMAX = (256 / DH) < kMaxGroup ? (256 / DH) : kMaxGroup;
+    static_assert(kRedRows % RPT == 0, "reduction block");
+    static constexpr int TPK = DH / 16;                  // attention threads per (head, key)
+    static constexpr int PPP = kAttnThreads / TPK;       // (head, key) pairs per score pass
+    static constexpr int GLMAX = 256 / DH < kMaxGroup ? 256 / DH : kMaxGroup;
+    static constexpr int IPT = kConsThreads / kAttnThreads;  // P.V outputs per attention thread
     static_assert(DH % 16 == 0 && 32 % TPK == 0, "head_dim layout");
 };
 
 template <int D, int DH>
 struct Smem {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    float red[2][kConsWarps][64];
+    using C = Cfg<D, DH>;
+    uint64_t full[C::STAGES];
+    uint64_t empty[C::STAGES];
+    uint64_t abar;                    // attention KV tile arrival
+    uint64_t hbar;                    // helper: partial pieces arrival
+    // streaming warps
+    float red[kConsWarps][kRedRows];  // GEMV row partials per warp (row sums in red[0] if warp-per-row)
     float nred[2][kConsWarps];
     float ubuf[kMaxUnitsPerCta];
-    float obuf[kMaxORowsPerCta];
-    float qs[kMaxGroup][DH];
-    float sc[2][kMaxGroup][Cfg<D, DH>::KPT];
-    float am[kMaxGroup], al[kMaxGroup], alpha[2][kMaxGroup];
-    float accred[kConsThreads];
-    float4 rbuf[32][8];
-    float axbuf[kConsWarps][Cfg<D, DH>::kBlockRow ? 1 : D];
-    __align__(16) __half curk[DH];
-    __align__(16) __half curv[DH];
-    float mw[4][256];
+    float obuf[2][kMaxORowsPerCta];   // merged attention output (o_proj inputs), by layer parity
+    __align__(16) __half gsm[C::kBlockRow ? D : 8];  // prefetched RMSNorm gains
+    float axbuf[kConsWarps][C::kBlockRow ? 1 : D];
     float amv[kConsWarps];
     int ami[kConsWarps];
+    // attention warps
+    __align__(16) float qs[kConsThreads];      // q of the current head chunk
+    float sc[kAttnScores];                     // scores / probabilities, [q head][key]
+    float am[kMaxChunkHeads], al[kMaxChunkHeads], alpha[kMaxChunkHeads];
+    __align__(16) __half curk[kConsThreads];   // this step's key / value, per chunk head
+    __align__(16) __half curv[kConsThreads];
+    float2 ml[4][kMaxLaneCtas];                // merge: (m, l) per lane CTA, then (weight, l)
+    // helper warp: one 32-float piece of every CTA's partial
+    __align__(16) float hbuf[kMaxCtas][kRChunk];
+    // control
     int last;
+    volatile int cur_op;
+    unsigned long long t_sync, t_tile;  // trace: blocked time in the current op (thread 0)
+    volatile int oflag;                 // layers whose o_proj inputs are merged
     volatile int abort_;
     volatile int prod_done;
     volatile int issued;
@@ -72,7 +86,7 @@ struct Smem {
 
 template <int D, int DH>
 constexpr size_t smem_total() {
-    return (size_t)kStages * kStageBytes + sizeof(Smem<D, DH>) + 128;
+    return (size_t)Cfg<D, DH>::STAGES * kStageBytes + kAttnBuf + sizeof(Smem<D, DH>) + 128;
 }
 static_assert(smem_total<4096, 128>() <= 232448, "shared memory per CTA");
 static_assert(smem_total<256, 32>() <= 232448, "shared memory per CTA");
@@ -90,54 +104,63 @@ __device__ __forceinline__ float warp_max(float v) {
 __device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
     return v1 > v2 || (v1 == v2 && i1 < i2);
 }
+__device__ __forceinline__ void attn_sync() {
+    asm volatile("bar.sync 2, %0;" ::"n"(kAttnThreads) : "memory");
+}
 
+// Records the first error (code, op, cta) and switches the CTA to abort mode.
+__device__ __forceinline__ void record_error(const KParams &p, volatile int *abort_flag, uint32_t code,
+                                             int op) {
+    if (atomicCAS(&p.err[0], 0u, code) == 0u) {
+        p.err[1] = (uint32_t)op;
+        p.err[2] = (uint32_t)blockIdx.x;
+    }
+    *abort_flag = 1;
+}
+
+// ============================================================ streaming warps
 template <int D, int DH>
-struct Consumer {
+struct Streamer {
     using C = Cfg<D, DH>;
     const KParams &p;
     Smem<D, DH> &S;
     uint8_t *stages;
-    int tid, warp, lane, cta, cur_op;
-    CtaPlan cp;
+    int tid, warp, lane, cta;
     uint64_t deadline;
     uint32_t it;
-    int rpar, npar, spar;
-    float x[C::NX], h[C::NX];
+    int npar;
+    int pre_u, pre_g;  // lane sum prefetched into rpre / gains prefetched into S.gsm
+    float x[C::NX], h[C::NX], rpre[C::NX];
 
-    __device__ Consumer(const KParams &p_, Smem<D, DH> &S_, uint8_t *st, uint64_t dl)
-        : p(p_), S(S_), stages(st), deadline(dl), it(0), rpar(0), npar(0), spar(0) {
+    __device__ Streamer(const KParams &p_, Smem<D, DH> &S_, uint8_t *st, uint64_t dl)
+        : p(p_), S(S_), stages(st), deadline(dl), it(0), npar(0), pre_u(-1), pre_g(-1) {
         tid = threadIdx.x;
         warp = tid >> 5;
         lane = tid & 31;
         cta = blockIdx.x;
-        cp = p.cta[cta];
-        cur_op = 0;
     }
 
-    __device__ int col(int i) const { return C::kBlockRow ? 8 * (tid + 256 * i) : 8 * lane; }
-
-    __device__ void fail(uint32_t code) {
-        if (atomicCAS(&p.err[0], 0u, code) == 0u) {
-            p.err[1] = (uint32_t)cur_op;
-            p.err[2] = (uint32_t)cta;
-        }
-        S.abort_ = 1;
-    }
+    __device__ CtaPlan plan() const { return p.cta[cta]; }
+    __device__ int col(int i) const { return C::kBlockRow ? 8 * (tid + kConsThreads * i) : 8 * lane; }
+    __device__ void fail(uint32_t code) { record_error(p, &S.abort_, code, S.cur_op); }
 
     // Thread 0 polls `ptr` until it reaches `target` (wrap-safe), the global
-    // error word is set, or the deadline passes.  All consumers leave together.
+    // error word is set, or the deadline passes.  All streamers leave together.
     __device__ void wait_geq(const uint32_t *ptr, uint32_t target) {
         if (tid == 0 && !S.abort_) {
+            const uint64_t t0 = p.trace ? global_timer_ns() : 0;
             while (true) {
                 if ((int)(ld_acquire(ptr) - target) >= 0) break;
                 if (ld_relaxed(p.err) != 0u) { S.abort_ = 1; break; }
                 if (global_timer_ns() > deadline) { fail(1); break; }
             }
+            if (p.trace) S.t_sync += global_timer_ns() - t0;
         }
         cons_sync();
     }
 
     __device__ void arrive(uint32_t *ctr) {
+        fence_proxy_async_global();  // these writes are read by other SMs' bulk copies
         cons_sync();
         if (tid == 0 && !S.abort_) {
             __threadfence();
@@ -146,10 +169,16 @@ struct Consumer {
     }
 
     __device__ const uint8_t *wait_tile() {
-        const int stage = it % kStages;
-        const uint32_t par = (it / kStages) & 1u;
+        const int stage = it % C::STAGES;
+        const uint32_t par = (it / C::STAGES) & 1u;
         ++it;
-        if (!mbar_try_wait(&S.full[stage], par)) {
+        if (p.trace && tid == 0 && !mbar_test_wait(&S.full[stage], par)) {
+            const uint64_t t0 = global_timer_ns();
+            while (!S.abort_ && !mbar_try_wait(&S.full[stage], par)) {
+                if (global_timer_ns() > deadline) fail(2);
+            }
+            S.t_tile += global_timer_ns() - t0;
+        } else if (!mbar_try_wait(&S.full[stage], par)) {
             while (!S.abort_ && !mbar_try_wait(&S.full[stage], par)) {
                 if (global_timer_ns() > deadline) fail(2);
             }
@@ -158,7 +187,7 @@ struct Consumer {
     }
 
     __device__ void release_tile() {
-        const int stage = (it - 1) % kStages;
+        const int stage = (it - 1) % C::STAGES;
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[stage]);
     }
@@ -173,19 +202,91 @@ struct Consumer {
         }
     }
 
-    __device__ void add(int u) {
-        wait_geq(&p.ready[u], p.epoch * (uint32_t)p.nch);
+    __device__ void load_r(int u, float *dst, bool accumulate) {
         const float *r = p.R + (size_t)u * D;
 #pragma unroll
         for (int i = 0; i < C::NCHT; ++i) {
-            float4 a = __ldcg(reinterpret_cast<const float4 *>(r + col(i)));
-            float4 b = __ldcg(reinterpret_cast<const float4 *>(r + col(i) + 4));
-            x[8 * i + 0] += a.x; x[8 * i + 1] += a.y; x[8 * i + 2] += a.z; x[8 * i + 3] += a.w;
-            x[8 * i + 4] += b.x; x[8 * i + 5] += b.y; x[8 * i + 6] += b.z; x[8 * i + 7] += b.w;
+            const float4 a = __ldcg(reinterpret_cast<const float4 *>(r + col(i)));
+            const float4 b = __ldcg(reinterpret_cast<const float4 *>(r + col(i) + 4));
+            const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dst[8 * i + e] = accumulate ? dst[8 * i + e] + v[e] : v[e];
         }
     }
 
-    __device__ void norm(int gi) {
+    // x += R[u].  Warp-local: each warp owns its residual columns, so no CTA
+    // barrier; uses the copy prefetched into registers when there is one.
+    __device__ void add(int u) {
+        if (pre_u == u) {
+#pragma unroll
+            for (int i = 0; i < C::NX; ++i) x[i] += rpre[i];
+            pre_u = -1;
+            return;
+        }
+        const uint32_t target = p.epoch * (uint32_t)p.nch;
+        if (lane == 0 && !S.abort_) {
+            const uint64_t t0 = (p.trace && tid == 0) ? global_timer_ns() : 0;
+            while (true) {
+                if ((int)(ld_acquire(&p.ready[u]) - target) >= 0) break;
+                if (ld_relaxed(p.err) != 0u) { S.abort_ = 1; break; }
+                if (global_timer_ns() > deadline) { fail(1); break; }
+            }
+            if (p.trace && tid == 0) S.t_sync += global_timer_ns() - t0;
+        }
+        __syncwarp();
+        (void)ld_acquire(&p.ready[u]);
+        load_r(u, x, true);
+    }
+
+    // At the start of a streaming op: if the lane sum of the next ADD (within
+    // the next few ops) is already complete, fetch it now; its L2 latency then
+    // hides behind the weight stream.
+    __device__ void prefetch_add(int oi) {
+        int u = -1;
+        for (int j = oi + 1; j < p.n_ops && j <= oi + 4; ++j) {
+            const int op = __ldg(p.ops + j);
+            if (op_type(op) == OP_ADD) { u = op_arg(op); break; }
+        }
+        if (u < 0 || u == pre_u) return;
+        const uint32_t v = ld_acquire(&p.ready[u]);
+        if (!__all_sync(0xffffffffu, (int)(v - p.epoch * (uint32_t)p.nch) >= 0)) return;
+        load_r(u, rpre, false);
+        pre_u = u;
+    }
+
+    // Gains of the next NORM after op oi into S.gsm (each thread its own chunks).
+    __device__ void prefetch_gains(int oi) {
+        if constexpr (C::kBlockRow) {
+            for (int j = oi + 1; j < p.n_ops; ++j) {
+                const int op = __ldg(p.ops + j);
+                if (op_type(op) == OP_NORM) {
+                    const __half *g = p.gains + (size_t)op_arg(op) * D;
+#pragma unroll
+                    for (int i = 0; i < C::NCHT; ++i) cp_async16(&S.gsm[col(i)], g + col(i));
+                    cp_async_commit();
+                    pre_g = op_arg(op);
+                    return;
+                }
+            }
+        }
+    }
+
+    __device__ void norm(int gi, int oi) {
+        float gf[C::NX];
+        if constexpr (C::kBlockRow) {
+            if (pre_g != gi) {
+#pragma unroll
+                for (int i = 0; i < C::NCHT; ++i)
+                    cp_async16(&S.gsm[col(i)], p.gains + (size_t)gi * D + col(i));
+                cp_async_commit();
+            }
+            cp_async_wait_all();
+#pragma unroll
+            for (int i = 0; i < C::NCHT; ++i)
+                h8_to_f(*reinterpret_cast<const uint4 *>(&S.gsm[col(i)]), &gf[8 * i]);
+        } else {
+            h8_to_f(__ldg(reinterpret_cast<const uint4 *>(p.gains + (size_t)gi * D + col(0))), gf);
+        }
         float ss = 0.f;
 #pragma unroll
         for (int i = 0; i < C::NX; ++i) ss += x[i] * x[i];
@@ -200,21 +301,16 @@ struct Consumer {
             for (int w = 0; w < kConsWarps; ++w) ss += nr[w];
         }
         const float inv = rsqrtf(ss / (float)D + p.eps);
-        const __half *g = p.gains + (size_t)gi * D;
 #pragma unroll
-        for (int i = 0; i < C::NCHT; ++i) {
-            float gf[8];
-            h8_to_f(__ldg(reinterpret_cast<const uint4 *>(g + col(i))), gf);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) h[8 * i + e] = x[8 * i + e] * inv * gf[e];
-        }
+        for (int i = 0; i < C::NX; ++i) h[i] = x[i] * inv * gf[i];
+        prefetch_gains(oi);
     }
 
     // ----------------------------------------------------------------- GEMV
-    // Row sums of one tile of `n` rows against h, left in S.red[parity].
-    __device__ float (*dot_tile(const uint8_t *tile, int n))[64] {
-        float(*red)[64] = S.red[rpar & 1];
-        ++rpar;
+    // Row partials of one tile of `n` rows against h into S.red, rows t0..t0+n-1
+    // of the current reduction block.  No CTA-wide barrier per tile: each warp
+    // runs through the tiles at its own pace.
+    __device__ void dot_tile(const uint8_t *tile, int n, int t0) {
         if constexpr (C::kBlockRow) {
             float acc[4];
 #pragma unroll
@@ -225,10 +321,15 @@ struct Consumer {
                     for (int i = 0; i < C::NCHT; ++i) {
                         float w[8];
                         h8_to_f(*reinterpret_cast<const uint4 *>(tile + (size_t)r * 2 * D +
-                                                                 16 * (tid + 256 * i)),
+                                                                 16 * (tid + kConsThreads * i)),
                                 w);
+                        float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[r] = fmaf(w[e], h[8 * i + e], acc[r]);
+                        for (int e = 0; e < 8; e += 2) {
+                            a0 = fmaf(w[e], h[8 * i + e], a0);
+                            a1 = fmaf(w[e + 1], h[8 * i + e + 1], a1);
+                        }
+                        acc[r] += a0 + a1;
                     }
                 }
             }
@@ -243,7 +344,7 @@ struct Consumer {
             k += __shfl_xor_sync(0xffffffffu, k, 4);
             k += __shfl_xor_sync(0xffffffffu, k, 2);
             k += __shfl_xor_sync(0xffffffffu, k, 1);
-            if ((lane & 7) == 0) red[warp][(hi ? 2 : 0) + (b8 ? 1 : 0)] = k;
+            if ((lane & 7) == 0) S.red[warp][t0 + (hi ? 2 : 0) + (b8 ? 1 : 0)] = k;
         } else {
 #pragma unroll 1
             for (int r = warp; r < n; r += kConsWarps) {
@@ -253,33 +354,37 @@ struct Consumer {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) a = fmaf(w[e], h[e], a);
                 a = warp_sum(a);
-                if (lane == 0) red[0][r] = a;
+                if (lane == 0) S.red[0][t0 + r] = a;
             }
         }
-        return red;
     }
 
-    __device__ float row_sum(float (*red)[64], int r) const {
+    __device__ float row_sum(int r) const {
         if constexpr (C::kBlockRow) {
             float s = 0.f;
 #pragma unroll
-            for (int w = 0; w < kConsWarps; ++w) s += red[w][r];
+            for (int w = 0; w < kConsWarps; ++w) s += S.red[w][r];
             return s;
         } else {
-            return red[0][r];
+            return S.red[0][r];
         }
     }
 
-    // Streams n_rows rows; epi(r0, n, red) runs after each tile's reduction.
+    // Streams n_rows rows in blocks of up to kRedRows; after each block the
+    // warps' partials are summed and epi(b0, nb) runs (row sums: row_sum(r)).
     template <class Epi>
     __device__ void dot_op(int n_rows, Epi epi) {
-        for (int r0 = 0; r0 < n_rows; r0 += C::RPT) {
-            const int n = min(C::RPT, n_rows - r0);
-            const uint8_t *tile = wait_tile();
-            float(*red)[64] = dot_tile(tile, n);
-            release_tile();
+        for (int b0 = 0; b0 < n_rows; b0 += kRedRows) {
+            const int nb = min(kRedRows, n_rows - b0);
+            for (int t0 = 0; t0 < nb; t0 += C::RPT) {
+                const int n = min(C::RPT, nb - t0);
+                const uint8_t *tile = wait_tile();
+                dot_tile(tile, n, t0);
+                release_tile();
+            }
             cons_sync();
-            epi(r0, n, red);
+            epi(b0, nb);
+            cons_sync();
         }
     }
 
@@ -301,7 +406,7 @@ struct Consumer {
                         for (int i = 0; i < C::NCHT; ++i) {
                             float w[8];
                             h8_to_f(*reinterpret_cast<const uint4 *>(tile + (size_t)r * 2 * D +
-                                                                     16 * (tid + 256 * i)),
+                                                                     16 * (tid + kConsThreads * i)),
                                     w);
 #pragma unroll
                             for (int e = 0; e < 8; ++e) acc[8 * i + e] = fmaf(c, w[e], acc[8 * i + e]);
@@ -331,26 +436,34 @@ struct Consumer {
 #pragma unroll
             for (int e = 0; e < 8; ++e) S.axbuf[warp][8 * lane + e] = acc[e];
             cons_sync();
-            float s = 0.f;
+            if (tid < D) {
+                float s = 0.f;
 #pragma unroll
-            for (int w = 0; w < kConsWarps; ++w) s += S.axbuf[w][tid];
-            out[tid] = s;
+                for (int w = 0; w < kConsWarps; ++w) s += S.axbuf[w][tid];
+                out[tid] = s;
+            }
         }
     }
 
     // ------------------------------------------------------------ QKV / FFN
     __device__ void qkv(int l) {
         const LayerPlan lp = p.lp[(size_t)cta * p.L + l];
+        const int lane_id = plan().lane;
         const int half = DH / 2;
-        float *qkvb = p.qkv + ((size_t)l * p.NL + cp.lane) * p.qkv_l;
-        dot_op(2 * lp.qkv_n, [&](int r0, int n, float(*red)[64]) {
+        float *qkvb = p.qkv + ((size_t)l * p.NL + lane_id) * p.qkv_l;
+        // RoPE factors of this thread's pair in the first block, fetched now so
+        // that the load is long done when the epilogue runs.
+        float2 cs0 = make_float2(1.f, 0.f);
+        if (tid < min(lp.qkv_n, kRedRows / 2))
+            cs0 = __ldg(p.rope + (size_t)p.pos * half + (lp.qkv_begin + tid) % half);
+        dot_op(2 * lp.qkv_n, [&](int b0, int nb) {
             const int t = tid;
-            if (t < n / 2) {
-                const int j = lp.qkv_begin + r0 / 2 + t;
+            if (t < nb / 2) {
+                const int j = lp.qkv_begin + b0 / 2 + t;
                 const int hs = j / half, c = j % half;
-                float a = row_sum(red, 2 * t), b = row_sum(red, 2 * t + 1);
+                float a = row_sum(2 * t), b = row_sum(2 * t + 1);
                 if (hs < p.HQ_L + p.HKV_L) {  // RoPE on q and k
-                    const float2 cs = p.rope[(size_t)p.pos * half + c];
+                    const float2 cs = b0 == 0 ? cs0 : __ldg(p.rope + (size_t)p.pos * half + c);
                     const float a2 = a * cs.x - b * cs.y;
                     const float b2 = a * cs.y + b * cs.x;
                     a = a2;
@@ -364,7 +477,7 @@ struct Consumer {
                     b = __half2float(hb);
                     __half *cache = isk ? p.kc : p.vc;
                     const size_t at =
-                        ((((size_t)cp.lane * p.L + l) * p.HKV_L + g) * p.ctx + p.pos) * DH;
+                        ((((size_t)lane_id * p.L + l) * p.HKV_L + g) * p.ctx + p.pos) * DH;
                     cache[at + c] = ha;
                     cache[at + c + half] = hb;
                 }
@@ -372,25 +485,23 @@ struct Consumer {
                 qkvb[hs * DH + c + half] = b;
             }
         });
-        cons_sync();
         if (!(p.skip_arrive_cta == cta && l == 0)) {
             if (tid == 0 && !S.abort_) {
                 __threadfence();
-                atomicAdd(&p.barA[l * p.NL + cp.lane], 1u);
+                atomicAdd(&p.barA[l * p.NL + lane_id], 1u);
             }
         }
     }
 
     __device__ void gateup(int l) {
         const LayerPlan lp = p.lp[(size_t)cta * p.L + l];
-        dot_op(2 * lp.ffn_n, [&](int r0, int n, float(*red)[64]) {
+        dot_op(2 * lp.ffn_n, [&](int b0, int nb) {
             const int t = tid;
-            if (t < n / 2) {
-                const float a = row_sum(red, 2 * t), b = row_sum(red, 2 * t + 1);
-                S.ubuf[r0 / 2 + t] = a / (1.f + expf(-a)) * b;
+            if (t < nb / 2) {
+                const float a = row_sum(2 * t), b = row_sum(2 * t + 1);
+                S.ubuf[b0 / 2 + t] = a / (1.f + expf(-a)) * b;
             }
         });
-        cons_sync();
     }
 
     __device__ void down(int l) {
@@ -400,215 +511,23 @@ struct Consumer {
         arrive(&p.cnt[u]);
     }
 
-    // ------------------------------------------------------------ attention
-    __device__ void attn_tile(const __half *kp, const __half *vp, int n, const float (*qr)[16],
-                              float &acc) {
-        float(*sc)[C::KPT] = S.sc[spar & 1];
-        float *alph = S.alpha[spar & 1];
-        ++spar;
-        const int GL = p.GL;
-        // scores: TPK threads per key, each 16 of the head dims
-        {
-            const int c = tid % C::TPK;
-            for (int j0 = 0; j0 < n; j0 += C::KPP) {
-                const int j = j0 + tid / C::TPK;
-                float d[C::GLMAX];
-#pragma unroll
-                for (int g = 0; g < C::GLMAX; ++g) d[g] = 0.f;
-                if (j < n) {
-                    float kf[16];
-                    h8_to_f(*reinterpret_cast<const uint4 *>(kp + (size_t)j * DH + 8 * c), kf);
-                    h8_to_f(*reinterpret_cast<const uint4 *>(kp + (size_t)j * DH + 8 * (c + C::TPK)),
-                            kf + 8);
-#pragma unroll
-                    for (int g = 0; g < C::GLMAX; ++g)
-                        if (g < GL) {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) d[g] = fmaf(qr[g][e], kf[e], d[g]);
-                        }
-                }
-#pragma unroll
-                for (int g = 0; g < C::GLMAX; ++g) {
-#pragma unroll
-                    for (int o = C::TPK / 2; o > 0; o >>= 1)
-                        d[g] += __shfl_xor_sync(0xffffffffu, d[g], o);
-                }
-                if (c == 0 && j < n) {
-#pragma unroll
-                    for (int g = 0; g < C::GLMAX; ++g)
-                        if (g < GL) sc[g][j] = d[g] * p.attn_scale;
-                }
-            }
-        }
-        cons_sync();
-        // online softmax update, one warp per q head
-        if (warp < GL) {
-            const float mo = S.am[warp];
-            float mt = -FLT_MAX;
-            for (int j = lane; j < n; j += 32) mt = fmaxf(mt, sc[warp][j]);
-            mt = warp_max(mt);
-            const float mn = fmaxf(mo, mt);
-            const float a = (mo == -INFINITY) ? 0.f : expf(mo - mn);
-            float s = 0.f;
-            for (int j = lane; j < n; j += 32) {
-                const float pj = expf(sc[warp][j] - mn);
-                sc[warp][j] = pj;
-                s += pj;
-            }
-            s = warp_sum(s);
-            if (lane == 0) {
-                S.am[warp] = mn;
-                S.al[warp] = S.al[warp] * a + s;
-                alph[warp] = a;
-            }
-        }
-        cons_sync();
-        // acc = alpha * acc + sum_j p_j V_j; thread = (key group, q head, dim)
-        {
-            const int GD = GL * DH, KG = kConsThreads / GD;
-            const int o = tid % GD, kg = tid / GD, g = o / DH, dd = o % DH;
-            acc *= alph[g];
-            for (int j = kg; j < n; j += KG) acc = fmaf(sc[g][j], __half2float(vp[(size_t)j * DH + dd]), acc);
-        }
-    }
-
-    __device__ void attn(int l) {
-        const int S_ = cp.S, k = cp.k, GL = p.GL, GD = GL * DH, KG = kConsThreads / GD;
-        wait_geq(&p.barA[l * p.NL + cp.lane], p.epoch * (uint32_t)S_);
-        int a, b;
-        attn_range(p.pos, p.window[l], k, S_, &a, &b);
-        const bool last = (k == S_ - 1);
-        const float *qkvb = p.qkv + ((size_t)l * p.NL + cp.lane) * p.qkv_l;
-        for (int g = 0; g < p.HKV_L; ++g) {
-            if (tid < GL) {
-                S.am[tid] = -INFINITY;
-                S.al[tid] = 0.f;
-            }
-            for (int e = tid; e < GD; e += kConsThreads) S.qs[e / DH][e % DH] = __ldcg(qkvb + (size_t)g * GD + e);
-            cons_sync();
-            float qr[C::GLMAX][16];
-            {
-                const int c = tid % C::TPK;
-#pragma unroll
-                for (int gq = 0; gq < C::GLMAX; ++gq)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        qr[gq][e] = gq < GL ? S.qs[gq][8 * c + e] : 0.f;
-                        qr[gq][8 + e] = gq < GL ? S.qs[gq][8 * (c + C::TPK) + e] : 0.f;
-                    }
-            }
-            float acc = 0.f;
-            for (int j0 = a; j0 < b; j0 += C::KPT) {
-                const int n = min(C::KPT, b - j0);
-                const uint8_t *tile = wait_tile();
-                attn_tile(reinterpret_cast<const __half *>(tile),
-                          reinterpret_cast<const __half *>(tile + kStageBytes / 2), n, qr, acc);
-                release_tile();
-            }
-            if (last) {  // the current key, from this step's QKV rows
-                const float *kcur = qkvb + (size_t)(p.HQ_L + g) * DH;
-                const float *vcur = qkvb + (size_t)(p.HQ_L + p.HKV_L + g) * DH;
-                for (int e = tid; e < DH; e += kConsThreads) {
-                    S.curk[e] = __float2half_rn(__ldcg(kcur + e));
-                    S.curv[e] = __float2half_rn(__ldcg(vcur + e));
-                }
-                cons_sync();
-                attn_tile(S.curk, S.curv, 1, qr, acc);
-            }
-            cons_sync();
-            float *dst = p.apart + (((size_t)l * p.n_cta + cta) * p.HQ_L + (size_t)g * GL) * (DH + 2);
-            if (KG > 1) {
-                S.accred[tid] = acc;
-                cons_sync();
-                if (tid < GD) {
-                    float s = 0.f;
-                    for (int q = 0; q < KG; ++q) s += S.accred[q * GD + tid];
-                    dst[(tid / DH) * (DH + 2) + tid % DH] = s;
-                }
-            } else {
-                dst[(tid / DH) * (DH + 2) + tid % DH] = acc;
-            }
-            if (tid < GL) {
-                dst[tid * (DH + 2) + DH] = S.am[tid];
-                dst[tid * (DH + 2) + DH + 1] = S.al[tid];
-            }
-            cons_sync();
-        }
-        arrive(&p.barB[l * p.NL + cp.lane]);
-    }
-
+    // o_proj of layer l: waits for the attention warps to merge this CTA's
+    // o_proj inputs into S.obuf[l & 1].
     __device__ void oproj(int l) {
         const LayerPlan lp = p.lp[(size_t)cta * p.L + l];
-        const int S_ = cp.S;
-        wait_geq(&p.barB[l * p.NL + cp.lane], p.epoch * (uint32_t)S_);
-        const int u = 2 * l;
-        if (lp.o_n > 0) {
-            const int a0 = lp.o_begin / DH, a1 = (lp.o_begin + lp.o_n - 1) / DH;
-            const size_t stride = (size_t)p.HQ_L * (DH + 2);
-            const float *base = p.apart + ((size_t)l * p.n_cta + cp.cta0) * stride;
-            // merge weights per touched head: w_k = exp(m_k - M) / sum_k exp(m_k - M) l_k
-            for (int hh = 0; hh <= a1 - a0; ++hh) {
-                const int a = a0 + hh;
-                float m = -INFINITY, lsum = 0.f;
-                if (tid < S_) {
-                    m = __ldcg(base + tid * stride + (size_t)a * (DH + 2) + DH);
-                    lsum = __ldcg(base + tid * stride + (size_t)a * (DH + 2) + DH + 1);
-                }
-                float M = warp_max(m);
-                float *nr = S.nred[npar & 1];
-                ++npar;
-                if (lane == 0) nr[warp] = M;
-                cons_sync();
-                M = nr[0];
-#pragma unroll
-                for (int w = 1; w < kConsWarps; ++w) M = fmaxf(M, nr[w]);
-                const float wk = (tid < S_ && m != -INFINITY) ? expf(m - M) : 0.f;
-                float den = warp_sum(wk * lsum);
-                nr = S.nred[npar & 1];
-                ++npar;
-                if (lane == 0) nr[warp] = den;
-                cons_sync();
-                den = 0.f;
-#pragma unroll
-                for (int w = 0; w < kConsWarps; ++w) den += nr[w];
-                if (tid < S_) S.mw[hh][tid] = wk / den;
+        if (tid == 0 && !S.abort_) {
+            const uint64_t t0 = p.trace ? global_timer_ns() : 0;
+            while (S.oflag < l + 1) {
+                if (S.abort_) break;
+                if (global_timer_ns() > deadline) { fail(5); break; }
             }
-            cons_sync();
-            for (int r = tid; r < lp.o_n; r += kConsThreads) {
-                const int c = lp.o_begin + r, a = c / DH, e = c % DH, hh = a - a0;
-                float s = 0.f;
-                for (int kk = 0; kk < S_; ++kk)
-                    s = fmaf(S.mw[hh][kk], __ldcg(base + kk * stride + (size_t)a * (DH + 2) + e), s);
-                S.obuf[r] = s;
-            }
-            cons_sync();
+            __threadfence_block();
+            if (p.trace) S.t_sync += global_timer_ns() - t0;
         }
-        axpy_op(lp.o_n, S.obuf, p.part + ((size_t)u * p.n_cta + cta) * D);
-        arrive(&p.cnt[u]);
-    }
-
-    // ------------------------------------------------------ delayed lane sum
-    __device__ void reduce(int u) {
-        if (cta >= p.nch) return;
-        wait_geq(&p.cnt[u], p.epoch * (uint32_t)p.n_cta);
-        const int f4 = tid & 7, g = tid >> 3;
-        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float *src = p.part + (size_t)u * p.n_cta * D + kRChunk * cta + 4 * f4;
-        for (int k = g; k < p.n_cta; k += 32) {
-            const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + (size_t)k * D));
-            s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
-        }
-        S.rbuf[g][f4] = s;
         cons_sync();
-        if (tid < 8) {
-            float4 t = S.rbuf[0][tid];
-            for (int q = 1; q < 32; ++q) {
-                const float4 v = S.rbuf[q][tid];
-                t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
-            }
-            *reinterpret_cast<float4 *>(p.R + (size_t)u * D + kRChunk * cta + 4 * tid) = t;
-        }
-        arrive(&p.ready[u]);
+        const int u = 2 * l;
+        axpy_op(lp.o_n, S.obuf[l & 1], p.part + ((size_t)u * p.n_cta + cta) * D);
+        arrive(&p.cnt[u]);
     }
 
     // ---------------------------------------------------------- LM + argmax
@@ -632,10 +551,11 @@ struct Consumer {
     __device__ void lmhead() {
         float bv = -INFINITY;
         int bi = 0x7fffffff;
-        dot_op(cp.lm_count, [&](int r0, int n, float(*red)[64]) {
-            if (tid < n) {
-                const int v = cp.lm_begin + r0 + tid;
-                const float z = row_sum(red, tid);
+        const CtaPlan cp = plan();
+        dot_op(cp.lm_count, [&](int b0, int nb) {
+            if (tid < nb) {
+                const int v = cp.lm_begin + b0 + tid;
+                const float z = row_sum(tid);
                 p.logits[v] = z;
                 if (better(z, v, bv, bi)) { bv = z; bi = v; }
             }
@@ -666,21 +586,33 @@ struct Consumer {
     // ------------------------------------------------------------------ run
     __device__ void run() {
         for (int oi = 0; oi < p.n_ops; ++oi) {
-            cur_op = oi;
+            if (tid == 0) S.cur_op = oi;
             const int op = __ldg(p.ops + oi);
             const int a = op_arg(op);
-            switch (op_type(op)) {
-                case OP_EMBED: embed(); break;
+            uint64_t t_start = 0;
+            if (p.trace && tid == 0) {
+                t_start = global_timer_ns();
+                S.t_sync = S.t_tile = 0;
+            }
+            const int t = op_type(op);
+            if (t == OP_QKV || t == OP_GATEUP || t == OP_DOWN || t == OP_OPROJ) prefetch_add(oi);
+            switch (t) {
+                case OP_EMBED: embed(); prefetch_gains(oi); break;
                 case OP_ADD: add(a); break;
-                case OP_NORM: norm(a); break;
+                case OP_NORM: norm(a, oi); break;
                 case OP_QKV: qkv(a); break;
                 case OP_GATEUP: gateup(a); break;
                 case OP_DOWN: down(a); break;
-                case OP_ATTN: attn(a); break;
                 case OP_OPROJ: oproj(a); break;
-                case OP_REDUCE: reduce(a); break;
                 case OP_LMHEAD: lmhead(); break;
-                default: break;
+                default: break;  // ATTN: attention warps; REDUCE: helper warp
+            }
+            if (p.trace && tid == 0) {
+                unsigned long long *tr = p.trace + ((size_t)cta * p.n_ops + oi) * 4;
+                tr[0] = t_start;
+                tr[1] = global_timer_ns();
+                tr[2] = S.t_sync;
+                tr[3] = S.t_tile;
             }
         }
         // After an error: wait (bounded) for the producer to stop and for the
@@ -691,10 +623,10 @@ struct Consumer {
             while (!S.prod_done && global_timer_ns() < dl) {
             }
             const uint32_t issued = (uint32_t)S.issued;
-            for (int st = 0; st < kStages; ++st) {
+            for (int st = 0; st < C::STAGES; ++st) {
                 if ((uint32_t)st >= issued) break;
-                const uint32_t t = st + ((issued - 1 - st) / kStages) * kStages;
-                const uint32_t par = (t / kStages) & 1u;
+                const uint32_t t = st + ((issued - 1 - st) / C::STAGES) * C::STAGES;
+                const uint32_t par = (t / C::STAGES) & 1u;
                 while (!mbar_try_wait(&S.full[st], par) && global_timer_ns() < dl) {
                 }
             }
@@ -702,8 +634,279 @@ struct Consumer {
     }
 };
 
-// ---------------------------------------------------------------- producer
+// ============================================================ attention warps
+template <int D, int DH>
+struct Attention {
+    using C = Cfg<D, DH>;
+    const KParams &p;
+    Smem<D, DH> &S;
+    uint8_t *abuf;
+    int at, awarp, lane, cta, cur_op;
+    uint64_t deadline;
+    uint32_t ntile;   // attention tiles waited for (every attention thread keeps the count)
+    uint32_t issued;  // tiles whose copies thread 0 issued
 
+    __device__ Attention(const KParams &p_, Smem<D, DH> &S_, uint8_t *ab, uint64_t dl)
+        : p(p_), S(S_), abuf(ab), deadline(dl), cur_op(0), ntile(0), issued(0) {
+        at = threadIdx.x - kConsThreads;
+        awarp = at >> 5;
+        lane = at & 31;
+        cta = blockIdx.x;
+    }
+
+    __device__ void fail(uint32_t code) { record_error(p, &S.abort_, code, cur_op); }
+
+    __device__ void wait_geq(const uint32_t *ptr, uint32_t target) {
+        if (at == 0 && !S.abort_) {
+            while (true) {
+                if ((int)(ld_acquire(ptr) - target) >= 0) break;
+                if (ld_relaxed(p.err) != 0u) { S.abort_ = 1; break; }
+                if (global_timer_ns() > deadline) { fail(1); break; }
+            }
+        }
+        attn_sync();
+    }
+
+    // Bulk-loads keys [j0, j0 + n) of the chunk's HC KV heads (K of head g at
+    // g*kt keys, V likewise in the second half) and waits for them.
+    __device__ void load_tile(int l, int lane_id, int g0, int j0, int n) {
+        const int kt = p.kt, HC = p.hc;
+        const uint32_t par = ntile & 1u;  // tile i completes phase i of S.abar
+        if (at == 0 && !S.abort_ && issued == ntile) {
+            const uint32_t bytes = (uint32_t)n * DH * 2;
+            mbar_arrive_expect_tx(&S.abar, 2u * HC * bytes);
+            for (int g = 0; g < HC; ++g) {
+                const size_t head = (((size_t)lane_id * p.L + l) * p.HKV_L + g0 + g) * p.ctx;
+                const size_t off = (size_t)g * kt * DH * 2;
+                bulk_g2s(abuf + off, p.kc + (head + j0) * DH, bytes, &S.abar);
+                bulk_g2s(abuf + kAttnBuf / 2 + off, p.vc + (head + j0) * DH, bytes, &S.abar);
+            }
+            ++issued;
+        }
+        attn_sync();
+        // (in abort mode nothing may have been issued: the loop then stops at once)
+        while (!S.abort_ && !mbar_try_wait(&S.abar, par)) {
+            if (global_timer_ns() > deadline) fail(2);
+        }
+        ++ntile;
+    }
+
+    // Keys [0, n) from the tile buffer plus (has_cur) the current key from
+    // S.curk / S.curv at index n; all q heads of the chunk together.
+    __device__ void tile_update(int n, bool has_cur, float *acc) {
+        const int GL = p.GL, HC = p.hc, kt = p.kt, NQ = HC * GL, ldk = kt + 1;
+        const int nt = n + (has_cur ? 1 : 0);
+        const __half *kbase = reinterpret_cast<const __half *>(abuf);
+        const __half *vbase = reinterpret_cast<const __half *>(abuf + kAttnBuf / 2);
+        float *sc = S.sc;
+        {
+            const int c = at % C::TPK;
+            for (int q0 = 0; q0 < HC * nt; q0 += C::PPP) {
+                const int q = q0 + at / C::TPK;
+                float d[C::GLMAX];
+#pragma unroll
+                for (int gq = 0; gq < C::GLMAX; ++gq) d[gq] = 0.f;
+                const int g = q / max(nt, 1), j = q - g * nt;
+                if (q < HC * nt) {
+                    const __half *kp = j < n ? kbase + ((size_t)g * kt + j) * DH : S.curk + g * DH;
+                    float kf[16];
+                    h8_to_f(*reinterpret_cast<const uint4 *>(kp + 8 * c), kf);
+                    h8_to_f(*reinterpret_cast<const uint4 *>(kp + 8 * (c + C::TPK)), kf + 8);
+#pragma unroll
+                    for (int gq = 0; gq < C::GLMAX; ++gq)
+                        if (gq < GL) {
+                            const float *qv = S.qs + (g * GL + gq) * DH;
+                            const float4 qa = *reinterpret_cast<const float4 *>(qv + 8 * c);
+                            const float4 qb = *reinterpret_cast<const float4 *>(qv + 8 * c + 4);
+                            const float4 qc = *reinterpret_cast<const float4 *>(qv + 8 * (c + C::TPK));
+                            const float4 qd = *reinterpret_cast<const float4 *>(qv + 8 * (c + C::TPK) + 4);
+                            const float qq[16] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w,
+                                                  qc.x, qc.y, qc.z, qc.w, qd.x, qd.y, qd.z, qd.w};
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) d[gq] = fmaf(qq[e], kf[e], d[gq]);
+                        }
+                }
+#pragma unroll
+                for (int gq = 0; gq < C::GLMAX; ++gq) {
+#pragma unroll
+                    for (int o = C::TPK / 2; o > 0; o >>= 1) d[gq] += __shfl_xor_sync(0xffffffffu, d[gq], o);
+                }
+                if (c == 0 && q < HC * nt) {
+#pragma unroll
+                    for (int gq = 0; gq < C::GLMAX; ++gq)
+                        if (gq < GL) sc[(g * GL + gq) * ldk + j] = d[gq] * p.attn_scale;
+                }
+            }
+        }
+        attn_sync();
+        // online softmax update, one warp per q head
+        for (int a = awarp; a < NQ; a += kAttnWarps) {
+            float *sa = sc + a * ldk;
+            const float mo = S.am[a];
+            float mt = -FLT_MAX;
+            for (int j = lane; j < nt; j += 32) mt = fmaxf(mt, sa[j]);
+            mt = warp_max(mt);
+            const float mn = fmaxf(mo, mt);
+            const float al = (mo == -INFINITY) ? 0.f : expf(mo - mn);
+            float sum = 0.f;
+            for (int j = lane; j < nt; j += 32) {
+                const float pj = expf(sa[j] - mn);
+                sa[j] = pj;
+                sum += pj;
+            }
+            sum = warp_sum(sum);
+            if (lane == 0) {
+                S.am[a] = mn;
+                S.al[a] = S.al[a] * al + sum;
+                S.alpha[a] = al;
+            }
+        }
+        attn_sync();
+        // acc = alpha * acc + sum_j p_j V_j for this thread's (q head, dim) outputs
+        const int items = NQ * DH;
+#pragma unroll
+        for (int i = 0; i < C::IPT; ++i) {
+            const int o = at + kAttnThreads * i;
+            if (o < items) {
+                const int a = o / DH, dd = o % DH, g = a / GL;
+                const float *pa = sc + a * ldk;
+                float s = acc[i] * S.alpha[a];
+                for (int j = 0; j < nt; ++j) {
+                    const __half *vp = j < n ? vbase + ((size_t)g * kt + j) * DH : S.curv + g * DH;
+                    s = fmaf(pa[j], __half2float(vp[dd]), s);
+                }
+                acc[i] = s;
+            }
+        }
+        attn_sync();  // the tile buffer and the scores are free again
+    }
+
+    __device__ void attention(int l) {
+        const CtaPlan cp = p.cta[cta];
+        const int S_ = cp.S, GL = p.GL, HC = p.hc, kt = p.kt, NQ = HC * GL, items = NQ * DH;
+        wait_geq(&p.barA[l * p.NL + cp.lane], p.epoch * (uint32_t)S_);
+        int a, b;
+        attn_range(p.pos, p.window[l], cp.k, S_, &a, &b);
+        const bool last = (cp.k == S_ - 1);
+        const int n_prev = b - a, T = (n_prev + kt - 1) / kt, T_eff = (last && T == 0) ? 1 : T;
+        const float *qkvb = p.qkv + ((size_t)l * p.NL + cp.lane) * p.qkv_l;
+        for (int g0 = 0; g0 < p.HKV_L; g0 += HC) {
+            // one round trip: q of the chunk's heads and (last CTA) this step's k, v
+            if (at < NQ) {
+                S.am[at] = -INFINITY;
+                S.al[at] = 0.f;
+            }
+            for (int o = at; o < items; o += kAttnThreads) S.qs[o] = __ldcg(qkvb + (size_t)g0 * GL * DH + o);
+            if (last) {
+                for (int o = at; o < HC * DH; o += kAttnThreads) {
+                    S.curk[o] = __float2half_rn(__ldcg(qkvb + (size_t)(p.HQ_L + g0) * DH + o));
+                    S.curv[o] = __float2half_rn(__ldcg(qkvb + (size_t)(p.HQ_L + p.HKV_L + g0) * DH + o));
+                }
+            }
+            attn_sync();
+            float acc[C::IPT];
+#pragma unroll
+            for (int i = 0; i < C::IPT; ++i) acc[i] = 0.f;
+            for (int t = 0; t < T_eff; ++t) {
+                const int n = t < T ? min(kt, n_prev - t * kt) : 0;
+                if (t < T) load_tile(l, cp.lane, g0, a + t * kt, n);
+                tile_update(n, last && t == T_eff - 1, acc);
+            }
+            float *dst = p.apart + (((size_t)l * p.n_cta + cta) * p.HQ_L + (size_t)g0 * GL) * (DH + 2);
+#pragma unroll
+            for (int i = 0; i < C::IPT; ++i) {
+                const int o = at + kAttnThreads * i;
+                if (o < items) dst[(o / DH) * (DH + 2) + o % DH] = acc[i];
+            }
+            if (at < NQ) {
+                dst[at * (DH + 2) + DH] = S.am[at];
+                dst[at * (DH + 2) + DH + 1] = S.al[at];
+            }
+            attn_sync();
+        }
+        if (at == 0 && !S.abort_) {
+            __threadfence();
+            atomicAdd(&p.barB[l * p.NL + cp.lane], 1u);
+        }
+    }
+
+    // Merge of all lane CTAs' attention partials for this CTA's o_proj input
+    // columns into S.obuf[l & 1]; then tells the streaming warps.
+    __device__ void merge(int l) {
+        const LayerPlan lp = p.lp[(size_t)cta * p.L + l];
+        const CtaPlan cp = p.cta[cta];
+        const int S_ = cp.S;
+        wait_geq(&p.barB[l * p.NL + cp.lane], p.epoch * (uint32_t)S_);
+        float *ob = S.obuf[l & 1];
+        if (lp.o_n > 0) {
+            const int a0 = lp.o_begin / DH, nh = (lp.o_begin + lp.o_n - 1) / DH - a0 + 1;
+            const size_t stride = (size_t)p.HQ_L * (DH + 2);
+            const float *base = p.apart + ((size_t)l * p.n_cta + cp.cta0) * stride;
+            for (int t = at; t < nh * S_; t += kAttnThreads) {
+                const int hh = t / S_, k = t % S_;
+                const float *q = base + k * stride + (size_t)(a0 + hh) * (DH + 2) + DH;
+                S.ml[hh][k] = make_float2(__ldcg(q), __ldcg(q + 1));
+            }
+            attn_sync();
+            // weights w_k = exp(m_k - M) / sum_k exp(m_k - M) l_k, one warp per head
+            for (int hh = awarp; hh < nh; hh += kAttnWarps) {
+                float M = -INFINITY;
+                for (int k = lane; k < S_; k += 32) M = fmaxf(M, S.ml[hh][k].x);
+                M = warp_max(M);
+                float den = 0.f;
+                for (int k = lane; k < S_; k += 32) {
+                    const float2 v = S.ml[hh][k];
+                    den += (v.x == -INFINITY) ? 0.f : expf(v.x - M) * v.y;
+                }
+                den = warp_sum(den);
+                for (int k = lane; k < S_; k += 32) {  // each lane rewrites only its own entries
+                    const float m = S.ml[hh][k].x;
+                    S.ml[hh][k].x = (m == -INFINITY) ? 0.f : expf(m - M) / den;
+                }
+            }
+            attn_sync();
+            // row r, CTA subset k = kk, kk+4, ...: 4 lanes per row
+            const int kk = at & 3;
+            for (int rb = 0; rb < lp.o_n; rb += kAttnThreads / 4) {
+                const int r = rb + (at >> 2);
+                float s = 0.f;
+                if (r < lp.o_n) {
+                    const int c = lp.o_begin + r, hh = c / DH - a0;
+                    const float *q = base + (size_t)(c / DH) * (DH + 2) + c % DH;
+#pragma unroll 4
+                    for (int k = kk; k < S_; k += 4) s = fmaf(S.ml[hh][k].x, __ldcg(q + k * stride), s);
+                }
+                s += __shfl_xor_sync(0xffffffffu, s, 1);
+                s += __shfl_xor_sync(0xffffffffu, s, 2);
+                if (kk == 0 && r < lp.o_n) ob[r] = s;
+            }
+        }
+        attn_sync();
+        if (at == 0) {
+            __threadfence_block();
+            S.oflag = l + 1;
+        }
+    }
+
+    __device__ void run() {
+        for (int oi = 0; oi < p.n_ops; ++oi) {
+            const int op = __ldg(p.ops + oi);
+            if (op_type(op) != OP_ATTN) continue;
+            cur_op = oi;
+            attention(op_arg(op));
+            merge(op_arg(op));
+        }
+        // after an error, let the last attention tile thread 0 issued land
+        // (tiles complete in order, so the last one's phase covers them all)
+        if (at == 0 && S.abort_ && issued > 0) {
+            const uint64_t dl = global_timer_ns() + 1000000000ull;
+            while (!mbar_try_wait(&S.abar, (issued - 1) & 1u) && global_timer_ns() < dl) {
+            }
+        }
+    }
+};
+
+// ================================================================= producer
 template <int D, int DH>
 __device__ void produce(const KParams &p, Smem<D, DH> &S, uint8_t *stages, uint64_t deadline) {
     using C = Cfg<D, DH>;
@@ -712,17 +915,18 @@ __device__ void produce(const KParams &p, Smem<D, DH> &S, uint8_t *stages, uint6
     const uint64_t pol = policy_evict_first();
     uint32_t it = 0;
     const uint8_t *w = reinterpret_cast<const uint8_t *>(p.wstream) + (size_t)cp.w_row0 * 2 * D;
+    const uint8_t *w_end = w + (size_t)cp.w_rows * 2 * D;
+    const uint8_t *pf = w;  // the L2 prefetch front of this CTA's weight stream
     bool stop = false;
 
     auto claim = [&](int &stage) -> bool {
-        stage = it % kStages;
-        if (it >= kStages) {
-            const uint32_t par = ((it / kStages) - 1) & 1u;
+        stage = it % C::STAGES;
+        if (it >= C::STAGES) {
+            const uint32_t par = ((it / C::STAGES) - 1) & 1u;
             while (!mbar_try_wait(&S.empty[stage], par)) {
                 if (S.abort_) return false;
                 if (global_timer_ns() > deadline) {
-                    if (atomicCAS(&p.err[0], 0u, 3u) == 0u) p.err[2] = (uint32_t)cta;
-                    S.abort_ = 1;
+                    record_error(p, &S.abort_, 3u, -1);
                     return false;
                 }
             }
@@ -735,6 +939,13 @@ __device__ void produce(const KParams &p, Smem<D, DH> &S, uint8_t *stages, uint6
             int stage;
             if (!claim(stage)) { stop = true; return; }
             const uint32_t bytes = (uint32_t)n * 2 * D;
+            const uint8_t *want = w + bytes + p.l2_prefetch_bytes;
+            if (want > w_end) want = w_end;
+            while (pf < want) {
+                const uint32_t nb = (uint32_t)min((size_t)kStageBytes, (size_t)(want - pf));
+                bulk_prefetch_l2(pf, nb);
+                pf += nb;
+            }
             mbar_arrive_expect_tx(&S.full[stage], bytes);
             bulk_g2s(stages + (size_t)stage * kStageBytes, w, bytes, &S.full[stage], pol);
             w += bytes;
@@ -745,65 +956,119 @@ __device__ void produce(const KParams &p, Smem<D, DH> &S, uint8_t *stages, uint6
     for (int oi = 0; oi < p.n_ops && !stop; ++oi) {
         const int op = __ldg(p.ops + oi);
         const int t = op_type(op), l = op_arg(op);
-        if (t == OP_QKV) {
-            rows(2 * p.lp[(size_t)cta * p.L + l].qkv_n);
-        } else if (t == OP_GATEUP) {
-            rows(2 * p.lp[(size_t)cta * p.L + l].ffn_n);
-        } else if (t == OP_DOWN) {
-            rows(p.lp[(size_t)cta * p.L + l].ffn_n);
-        } else if (t == OP_OPROJ) {
-            rows(p.lp[(size_t)cta * p.L + l].o_n);
-        } else if (t == OP_LMHEAD) {
-            rows(cp.lm_count);
-        } else if (t == OP_ATTN) {
-            int a, b;
-            attn_range(p.pos, p.window[l], cp.k, cp.S, &a, &b);
-            for (int g = 0; g < p.HKV_L && !stop; ++g) {
-                const size_t head = (((size_t)cp.lane * p.L + l) * p.HKV_L + g) * p.ctx;
-                for (int j0 = a; j0 < b; j0 += C::KPT) {
-                    const int n = min(C::KPT, b - j0);
-                    int stage;
-                    if (!claim(stage)) { stop = true; break; }
-                    const uint32_t bytes = (uint32_t)n * DH * 2;
-                    uint8_t *dst = stages + (size_t)stage * kStageBytes;
-                    mbar_arrive_expect_tx(&S.full[stage], 2 * bytes);
-                    bulk_g2s(dst, p.kc + (head + j0) * DH, bytes, &S.full[stage]);
-                    bulk_g2s(dst + kStageBytes / 2, p.vc + (head + j0) * DH, bytes, &S.full[stage]);
-                    ++it;
-                }
-            }
-        }
+        if (t == OP_QKV) rows(2 * p.lp[(size_t)cta * p.L + l].qkv_n);
+        else if (t == OP_GATEUP) rows(2 * p.lp[(size_t)cta * p.L + l].ffn_n);
+        else if (t == OP_DOWN) rows(p.lp[(size_t)cta * p.L + l].ffn_n);
+        else if (t == OP_OPROJ) rows(p.lp[(size_t)cta * p.L + l].o_n);
+        else if (t == OP_LMHEAD) rows(cp.lm_count);
     }
     S.issued = (int)it;
     __threadfence_block();
     S.prod_done = 1;
 }
 
+// =================================================================== helper
+// The delayed lane sum, off the streaming warps' path: for every REDUCE(u) of
+// the op list, chunk `cta` (32 floats) of R[u] = the sum over all CTAs k (in
+// order k = 0, 1, ...) of their partials of sub-block u.  The 32-float pieces
+// of all CTAs arrive by bulk copies in one round trip; each lane then sums one
+// float over the pieces, and the chunk is published with a release counter.
+template <int D, int DH>
+__device__ void help(const KParams &p, Smem<D, DH> &S, uint64_t deadline) {
+    const int lane = threadIdx.x & 31, cta = blockIdx.x;
+    if (cta >= p.nch) return;
+    const uint32_t target = p.epoch * (uint32_t)p.n_cta;
+    uint32_t nred = 0, issued = 0;
+    bool ok = true;
+    for (int oi = 0; oi < p.n_ops && ok; ++oi) {
+        const int op = __ldg(p.ops + oi);
+        if (op_type(op) != OP_REDUCE) continue;
+        const int u = op_arg(op);
+        if (lane == 0) {
+            while (true) {
+                if ((int)(ld_acquire(&p.cnt[u]) - target) >= 0) break;
+                if (S.abort_ || ld_relaxed(p.err) != 0u) { ok = false; break; }
+                if (global_timer_ns() > deadline) {
+                    record_error(p, &S.abort_, 4u, oi);
+                    ok = false;
+                    break;
+                }
+            }
+            if (ok) {
+                fence_proxy_async_global();
+                fence_proxy_async_shared();
+                mbar_arrive_expect_tx(&S.hbar, (uint32_t)p.n_cta * kRChunk * 4);
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        const float *src = p.part + (size_t)u * p.n_cta * D + kRChunk * cta;
+        for (int k = lane; k < p.n_cta; k += 32)
+            bulk_g2s(S.hbuf[k], src + (size_t)k * D, kRChunk * 4, &S.hbar);
+        ++issued;
+        while (!mbar_try_wait(&S.hbar, nred & 1u)) {
+            if (S.abort_ || global_timer_ns() > deadline) {
+                if (!S.abort_) record_error(p, &S.abort_, 4u, oi);
+                ok = false;
+                break;
+            }
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        ++nred;
+        float s = 0.f;
+        for (int k = 0; k < p.n_cta; ++k) s += S.hbuf[k][lane];
+        p.R[(size_t)u * D + kRChunk * cta + lane] = s;
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence();
+            atomicAdd(&p.ready[u], 1u);
+        }
+    }
+    // after an error, let pieces still in flight land before the CTA exits
+    if (lane == 0 && issued > nred) {
+        const uint64_t dl = global_timer_ns() + 1000000000ull;
+        while (!mbar_try_wait(&S.hbar, nred & 1u) && global_timer_ns() < dl) {
+        }
+    }
+}
+
 template <int D, int DH>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ KParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    using C = Cfg<D, DH>;
     uint8_t *stages = base;
-    Smem<D, DH> &S = *reinterpret_cast<Smem<D, DH> *>(base + (size_t)kStages * kStageBytes);
+    uint8_t *abuf = base + (size_t)C::STAGES * kStageBytes;
+    Smem<D, DH> &S = *reinterpret_cast<Smem<D, DH> *>(abuf + kAttnBuf);
     const uint64_t deadline = global_timer_ns() + p.timeout_ns;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < C::STAGES; ++i) {
             mbar_init(&S.full[i], 1);
             mbar_init(&S.empty[i], kConsWarps);
         }
+        mbar_init(&S.abar, 1);
+        mbar_init(&S.hbar, 1);
         S.abort_ = 0;
         S.prod_done = 0;
         S.issued = 0;
+        S.oflag = 0;
         S.last = 0;
         fence_barrier_init();
     }
     __syncthreads();
-    if (threadIdx.x >= kConsThreads) {
-        if (threadIdx.x == kConsThreads) produce<D, DH>(p, S, stages, deadline);
-        return;
+    const int t = threadIdx.x;
+    if (t < kConsThreads) {
+        Streamer<D, DH> s(p, S, stages, deadline);
+        s.run();
+    } else if (t < kConsThreads + kAttnThreads) {
+        Attention<D, DH> a(p, S, abuf, deadline);
+        a.run();
+    } else if (t < kConsThreads + kAttnThreads + 32) {
+        if (t == kConsThreads + kAttnThreads) produce<D, DH>(p, S, stages, deadline);
+    } else {
+        help<D, DH>(p, S, deadline);
     }
-    Consumer<D, DH> c(p, S, stages, deadline);
-    c.run();
 }
 
 template <int D, int DH>

@@ -12,12 +12,14 @@ namespace lf {
 struct KParams {
     // shape
     int L, D, DH, HQ_L, HKV_L, GL, F_L, V, NL, n_cta, ctx, n_ops, nch, qkv_l;
+    int hc, kt;  // attention: KV heads per chunk, keys per tile
     float eps, attn_scale;
     // this step
     int pos, token;
     uint32_t epoch;  // launches since the last reset; counters target epoch * n
     unsigned long long timeout_ns;
     int skip_arrive_cta;
+    unsigned l2_prefetch_bytes;  // weight-stream L2 prefetch distance beyond the stage ring
     int window[LF_MAX_LAYERS];
     // plan
     const int *ops;
@@ -42,6 +44,9 @@ struct KParams {
     float *logits;          // [V]
     int *argmax;            // [1]
     uint32_t *err;          // [4]: code, op index, cta, lane
+    // optional trace, [n_cta][n_ops][4]: op start, op end, ns blocked on
+    // cross-CTA counters, ns blocked on tile arrival (null = off)
+    unsigned long long *trace;
 };
 
 // Dynamic shared memory needed by the kernel for (D, DH); 0 if unsupported.

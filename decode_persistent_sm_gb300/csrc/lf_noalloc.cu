@@ -104,6 +104,8 @@ extern "C" lf_status lf_decode_step_static_scratch(lf_engine *e, int32_t token,
     k.L = s.L; k.D = s.D; k.DH = s.DH; k.HQ_L = s.HQ_L; k.HKV_L = s.HKV_L; k.GL = s.GL;
     k.F_L = s.F_L; k.V = s.V; k.NL = s.NL; k.n_cta = P.n_cta; k.ctx = s.ctx;
     k.n_ops = (int)P.ops.size(); k.nch = s.D / lf::kRChunk; k.qkv_l = (s.HQ_L + 2 * s.HKV_L) * s.DH;
+    k.hc = s.HC;
+    k.kt = s.KT;
     k.eps = e->cfg.rms_eps;
     k.attn_scale = (float)(1.0 / std::sqrt((double)s.DH));
     k.pos = e->pos;
@@ -111,6 +113,7 @@ extern "C" lf_status lf_decode_step_static_scratch(lf_engine *e, int32_t token,
     k.epoch = 1;  // counters were just cleared
     k.timeout_ns = e->timeout_ns;
     k.skip_arrive_cta = -1;
+    k.l2_prefetch_bytes = e->l2_prefetch_bytes;
     for (int l = 0; l < s.L; ++l) k.window[l] = e->cfg.swa_window[l];
     k.ops = e->d_ops; k.cta = e->d_cta; k.lp = e->d_lp;
     k.wstream = e->wstream; k.emb = e->emb; k.gains = e->gains; k.rope = e->rope;

@@ -58,8 +58,13 @@ lf_status derive_shape(const lf_config &c, Shape *sh) {
     const bool kern = (s.D == 4096 && s.DH == 128) || (s.D == 256 && s.DH == 32);
     // Attention: the q heads of a lane-local KV head times head_dim must tile
     // the 256 consumer threads.
-    const bool gl_ok = (s.GL == 1 || s.GL == 2 || s.GL == 4) && s.GL * s.DH <= kConsThreads;
+    const bool gl_ok = (s.GL == 1 || s.GL == 2 || s.GL == 4) && s.GL * s.DH <= 256;
     if (!kern || !gl_ok) return LF_ERR_UNSUPPORTED;
+    s.HC = s.HKV_L;
+    while (s.HC * s.GL * s.DH > kConsThreads) s.HC /= 2;
+    if (s.HC < 1 || s.HKV_L % s.HC) return LF_ERR_UNSUPPORTED;
+    s.KT = (kAttnBuf / 2) / (s.HC * s.DH * 2);
+    if (s.KT < 1 || s.HC * s.GL * (s.KT + 1) > kAttnScores) return LF_ERR_UNSUPPORTED;
     return LF_OK;
 }
 
@@ -145,7 +150,7 @@ lf_status build_plan(const lf_config &c, int n_cta, bool with_rows, Plan *plan) 
     lf_status st = derive_shape(c, &P.sh);
     if (st != LF_OK) return st;
     const Shape &s = P.sh;
-    if (n_cta < s.NL || n_cta < s.D / kRChunk) return LF_ERR_UNSUPPORTED;
+    if (n_cta < s.NL || n_cta < s.D / kRChunk || n_cta > kMaxCtas) return LF_ERR_UNSUPPORTED;
     P.n_cta = n_cta;
     P.rows_per_tile = kStageBytes / (2 * s.D);
 
@@ -156,7 +161,7 @@ lf_status build_plan(const lf_config &c, int n_cta, bool with_rows, Plan *plan) 
     P.lp.assign((size_t)n_cta * s.L, LayerPlan{});
     for (int i = 0; i < s.NL; ++i) {
         const int c0 = P.lane_start[i], S = P.lane_start[i + 1] - c0;
-        if (S > kConsThreads) return LF_ERR_UNSUPPORTED;  // attention merge: one thread per CTA
+        if (S > kMaxLaneCtas) return LF_ERR_UNSUPPORTED;  // attention merge: one thread per CTA
         int rot = 0;
         std::vector<int> qb, qn, fb, fn, ob, on;
         for (int l = 0; l < s.L; ++l) {
@@ -252,6 +257,8 @@ lf_status build_plan(const lf_config &c, int n_cta, bool with_rows, Plan *plan) 
         }
     }
     P.total_rows = row;
+    for (int k = 0; k < n_cta; ++k)
+        P.cta[k].w_rows = (k + 1 < n_cta ? P.cta[k + 1].w_row0 : row) - P.cta[k].w_row0;
     return LF_OK;
 }
 

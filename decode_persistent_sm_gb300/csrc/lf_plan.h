@@ -18,6 +18,8 @@ struct Shape {
     int F_L;    // FFN units per lane
     int NP;     // QKV row pairs per lane: (HQ_L + 2*HKV_L) * DH/2
     int NO;     // o_proj input columns per lane: HQ_L * DH
+    int HC;     // KV heads processed together in attention (HC * GL * DH <= 512)
+    int KT;     // keys per attention tile: K and V of HC heads fill one stage
     std::vector<int> kv_first;  // per lane: first global KV head it reads
     // element offsets in the FP16 blob
     long long off_E, per_layer, off_layer0, off_gf, off_lm, n_params;

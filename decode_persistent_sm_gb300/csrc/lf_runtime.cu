@@ -186,6 +186,7 @@ lf_status lf_plan_stats(const lf_config *cfg, int n_sm, int64_t stats[8]) {
 void lf_destroy(lf_engine *e) {
     if (!e) return;
     for (void *p : e->allocs) cudaFree(p);
+    if (e->trace) cudaFree(e->trace);
     if (e->h_status) cudaFreeHost(e->h_status);
     delete e;
 }
@@ -385,6 +386,8 @@ lf_status lf_decode_step(lf_engine *e, int32_t token, float *logits, int32_t *ar
     k.L = s.L; k.D = s.D; k.DH = s.DH; k.HQ_L = s.HQ_L; k.HKV_L = s.HKV_L; k.GL = s.GL;
     k.F_L = s.F_L; k.V = s.V; k.NL = s.NL; k.n_cta = P.n_cta; k.ctx = s.ctx;
     k.n_ops = (int)P.ops.size(); k.nch = s.D / lf::kRChunk; k.qkv_l = (s.HQ_L + 2 * s.HKV_L) * s.DH;
+    k.hc = s.HC;
+    k.kt = s.KT;
     k.eps = e->cfg.rms_eps;
     k.attn_scale = (float)(1.0 / std::sqrt((double)s.DH));
     k.pos = e->pos;
@@ -392,6 +395,7 @@ lf_status lf_decode_step(lf_engine *e, int32_t token, float *logits, int32_t *ar
     k.epoch = e->epoch + 1;
     k.timeout_ns = e->timeout_ns;
     k.skip_arrive_cta = e->skip_cta;
+    k.l2_prefetch_bytes = e->l2_prefetch_bytes;
     for (int l = 0; l < s.L; ++l) k.window[l] = e->cfg.swa_window[l];
     k.ops = e->d_ops; k.cta = e->d_cta; k.lp = e->d_lp;
     k.wstream = e->wstream; k.emb = e->emb; k.gains = e->gains; k.rope = e->rope;
@@ -405,6 +409,7 @@ lf_status lf_decode_step(lf_engine *e, int32_t token, float *logits, int32_t *ar
     k.cand_v = e->cand_v; k.cand_i = e->cand_i; k.logits = e->logits;
     k.argmax = reinterpret_cast<int *>(e->status);
     k.err = e->status + 4;
+    k.trace = e->trace;
 
     cudaError_t err = lf::launch_decode(k, e->stream);
     e->skip_cta = -1;
@@ -516,9 +521,53 @@ lf_status lf_set_timeout_ns(lf_engine *e, uint64_t ns) {
     return LF_OK;
 }
 
+lf_status lf_set_l2_prefetch(lf_engine *e, uint32_t bytes_per_sm) {
+    if (!e || (bytes_per_sm % 16) != 0 || bytes_per_sm > (64u << 20)) return LF_ERR_INVALID_ARG;
+    e->l2_prefetch_bytes = bytes_per_sm;
+    return LF_OK;
+}
+
 lf_status lf_debug_skip_arrival(lf_engine *e, int cta) {
     if (!e || cta < -1 || cta >= e->plan.n_cta) return LF_ERR_INVALID_ARG;
     e->skip_cta = cta;
+    return LF_OK;
+}
+
+lf_status lf_debug_trace(lf_engine *e, int enable) {
+    if (!e) return LF_ERR_INVALID_ARG;
+    if (e->poisoned != LF_OK) return e->poisoned;
+    if (!enable) {
+        if (e->trace) {
+            cudaError_t err = cudaStreamSynchronize(e->stream);
+            cudaFree(e->trace);
+            e->trace = nullptr;
+            if (err != cudaSuccess) return cuda_fail(e, err);
+        }
+        return LF_OK;
+    }
+    if (!e->trace) {
+        const size_t n = (size_t)e->plan.n_cta * e->plan.ops.size() * 4;
+        cudaError_t err = cudaMalloc(&e->trace, n * sizeof(unsigned long long));
+        if (err != cudaSuccess) {
+            e->trace = nullptr;
+            return err == cudaErrorMemoryAllocation ? LF_ERR_OOM : LF_ERR_CUDA;
+        }
+        err = cudaMemset(e->trace, 0, n * sizeof(unsigned long long));
+        if (err != cudaSuccess) return cuda_fail(e, err);
+    }
+    return LF_OK;
+}
+
+lf_status lf_debug_read_trace(lf_engine *e, uint64_t *out, size_t n_words, int32_t *ops) {
+    if (!e || !out) return LF_ERR_INVALID_ARG;
+    if (e->poisoned != LF_OK) return e->poisoned;
+    const size_t n = (size_t)e->plan.n_cta * e->plan.ops.size() * 4;
+    if (!e->trace || n_words != n) return LF_ERR_INVALID_ARG;
+    cudaError_t err = cudaStreamSynchronize(e->stream);
+    if (err == cudaSuccess)
+        err = cudaMemcpy(out, e->trace, n * sizeof(unsigned long long), cudaMemcpyDeviceToHost);
+    if (err != cudaSuccess) return cuda_fail(e, err);
+    if (ops) std::memcpy(ops, e->plan.ops.data(), e->plan.ops.size() * sizeof(int32_t));
     return LF_OK;
 }
 
@@ -531,7 +580,7 @@ lf_status lf_engine_info(const lf_engine *e, int64_t info[8]) {
     info[3] = (int64_t)lf::decode_smem_bytes(s.D, s.DH);
     info[4] = lf::kThreads;
     info[5] = e->launches;
-    info[6] = 0;
+    info[6] = (int64_t)e->plan.ops.size();
     info[7] = 0;
     return LF_OK;
 }

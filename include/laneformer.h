@@ -140,10 +140,25 @@ lf_status lf_read_kv(lf_engine *e, int layer, int kv_head, int pos, float *k, fl
  * runs out makes the step fail with LF_ERR_TIMEOUT instead of hanging. */
 lf_status lf_set_timeout_ns(lf_engine *e, uint64_t ns);
 
+/* Tuning: how far (bytes per SM, multiple of 16, default 128 KiB) each SM's
+ * weight stream is prefetched into L2 beyond its shared-memory stages, so
+ * that HBM keeps streaming while an SM does latency-bound work (attention,
+ * lane sums).  0 turns the prefetch off. */
+lf_status lf_set_l2_prefetch(lf_engine *e, uint32_t bytes_per_sm);
+
 /* Test hook: in the next decode step, CTA `cta` skips its first lane-barrier
  * arrival (-1 = off), so that the lane's other CTAs time out.  Proves that the
  * step ends with LF_ERR_TIMEOUT rather than a hang. */
 lf_status lf_debug_skip_arrival(lf_engine *e, int cta);
+
+/* Tracing: with enable != 0 every later step records, per CTA and per op of
+ * the step's op list, [start ns, end ns, ns blocked on cross-CTA counters, ns
+ * blocked on tile arrival] (global timer; allocates the buffer on first use).
+ * lf_debug_read_trace copies the last step's record: n_words must equal
+ * n_sm * n_ops * 4 (lf_engine_info [0] and [6]); `ops` (nullable, n_ops
+ * entries) receives the op list, each entry type | (argument << 8). */
+lf_status lf_debug_trace(lf_engine *e, int enable);
+lf_status lf_debug_read_trace(lf_engine *e, uint64_t *out, size_t n_words, int32_t *ops);
 
 /*
  * Decode step that allocates nothing.  The pages have no counterpart to this
@@ -187,7 +202,7 @@ lf_status lf_plan_stats(const lf_config *cfg, int n_sm, int64_t stats[8]);
 
 /* Engine facts: [0] SMs used, [1] weight-stream bytes, [2] device bytes
  * allocated, [3] smem bytes per CTA, [4] threads per CTA, [5] kernel launches
- * made since creation. */
+ * made since creation, [6] ops per step. */
 lf_status lf_engine_info(const lf_engine *e, int64_t info[8]);
 
 #ifdef __cplusplus
