@@ -183,7 +183,7 @@ def write_trace(eng, path, tokens, shape):
            "lmhead_start_ns_mean": float((tr[:, lm, 0] - t0).mean()),
            "by_op": {k: {"count": v[3], "mean_ns": v[0], "sync_wait_ns": v[1], "tile_wait_ns": v[2]}
                      for k, v in by.items()},
-           "per_op": [{"op": OP_NAMES[int(op) & 0xFF], "arg": int(op) >> 8,
+           "per_op": [{"op": OP_NAMES[int(op) & 0xFF], "arg": (int(op) >> 8) & 0xFF,
                        "start_ns_mean": float((tr[:, j, 0] - t0).mean()),
                        "dur_ns_mean": float(dur[:, j].mean()), "dur_ns_max": int(dur[:, j].max()),
                        "sync_ns_mean": float(tr[:, j, 2].mean()),

@@ -46,9 +46,14 @@ enum OpType : int {
     OP_REDUCE = 8,  // chunk of R[arg] = sum of all partials of sub-block arg
     OP_LMHEAD = 9,  // final logits rows and argmax
 };
+// An op word: bits 0-7 type, 8-15 argument, 16-23 gain index of the next
+// NORM after this op, 24-31 lane-sum index of the next ADD within the next 4
+// ops (255 = none in both; the planner fills them in).
 LF_HD int op_type(int op) { return op & 0xff; }
-LF_HD int op_arg(int op) { return op >> 8; }
-LF_HD int make_op(int type, int arg) { return type | (arg << 8); }
+LF_HD int op_arg(int op) { return (op >> 8) & 0xff; }
+LF_HD int op_next_norm(int op) { int v = (op >> 16) & 0xff; return v == 0xff ? -1 : v; }
+LF_HD int op_next_add(int op) { int v = (op >> 24) & 0xff; return v == 0xff ? -1 : v; }
+LF_HD int make_op(int type, int arg) { return type | (arg << 8) | (0xff << 16) | (0xff << 24); }
 
 struct CtaPlan {
     int lane;      // lane of this CTA

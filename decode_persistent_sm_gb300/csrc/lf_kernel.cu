@@ -128,7 +128,7 @@ struct Streamer {
     int tid, warp, lane, cta;
     uint64_t deadline;
     uint32_t it;
-    int npar;
+    int npar;          // RMSNorm slot in S.nred of the last NORM
     int pre_u, pre_g;  // lane sum prefetched into rpre / gains prefetched into S.gsm
     float x[C::NX], h[C::NX], rpre[C::NX];
 
@@ -241,12 +241,8 @@ struct Streamer {
     // At the start of a streaming op: if the lane sum of the next ADD (within
     // the next few ops) is already complete, fetch it now; its L2 latency then
     // hides behind the weight stream.
-    __device__ void prefetch_add(int oi) {
-        int u = -1;
-        for (int j = oi + 1; j < p.n_ops && j <= oi + 4; ++j) {
-            const int op = __ldg(p.ops + j);
-            if (op_type(op) == OP_ADD) { u = op_arg(op); break; }
-        }
+    __device__ void prefetch_add(int op) {
+        const int u = op_next_add(op);
         if (u < 0 || u == pre_u) return;
         const uint32_t v = ld_acquire(&p.ready[u]);
         if (!__all_sync(0xffffffffu, (int)(v - p.epoch * (uint32_t)p.nch) >= 0)) return;
@@ -254,24 +250,23 @@ struct Streamer {
         pre_u = u;
     }
 
-    // Gains of the next NORM after op oi into S.gsm (each thread its own chunks).
-    __device__ void prefetch_gains(int oi) {
+    // Gains of the next NORM after this op into S.gsm (each thread its own chunks).
+    __device__ void prefetch_gains(int op) {
         if constexpr (C::kBlockRow) {
-            for (int j = oi + 1; j < p.n_ops; ++j) {
-                const int op = __ldg(p.ops + j);
-                if (op_type(op) == OP_NORM) {
-                    const __half *g = p.gains + (size_t)op_arg(op) * D;
+            const int gi = op_next_norm(op);
+            if (gi < 0) return;
+            const __half *g = p.gains + (size_t)gi * D;
 #pragma unroll
-                    for (int i = 0; i < C::NCHT; ++i) cp_async16(&S.gsm[col(i)], g + col(i));
-                    cp_async_commit();
-                    pre_g = op_arg(op);
-                    return;
-                }
-            }
+            for (int i = 0; i < C::NCHT; ++i) cp_async16(&S.gsm[col(i)], g + col(i));
+            cp_async_commit();
+            pre_g = gi;
         }
     }
 
-    __device__ void norm(int gi, int oi) {
+    // h = g * x; the factor 1/rms(x) is a scalar, so it is applied to the GEMV
+    // row sums in the next op's epilogue (inv_rms()), where the warps meet
+    // anyway: no barrier here.  Each warp leaves its sum of squares in S.nred.
+    __device__ void norm(int gi, int op) {
         float gf[C::NX];
         if constexpr (C::kBlockRow) {
             if (pre_g != gi) {
@@ -292,18 +287,28 @@ struct Streamer {
         for (int i = 0; i < C::NX; ++i) ss += x[i] * x[i];
         ss = warp_sum(ss);
         if constexpr (C::kBlockRow) {
-            float *nr = S.nred[npar & 1];
             ++npar;
-            if (lane == 0) nr[warp] = ss;
-            cons_sync();
-            ss = 0.f;
+            if (lane == 0) S.nred[npar & 1][warp] = ss;
 #pragma unroll
-            for (int w = 0; w < kConsWarps; ++w) ss += nr[w];
+            for (int i = 0; i < C::NX; ++i) h[i] = x[i] * gf[i];
+        } else {  // every warp holds the whole row
+            const float inv = rsqrtf(ss / (float)D + p.eps);
+#pragma unroll
+            for (int i = 0; i < C::NX; ++i) h[i] = x[i] * inv * gf[i];
         }
-        const float inv = rsqrtf(ss / (float)D + p.eps);
+        prefetch_gains(op);
+    }
+
+    // 1/rms of the last NORM (call after a barrier that follows that NORM).
+    __device__ float inv_rms() const {
+        if constexpr (C::kBlockRow) {
+            float ss = 0.f;
 #pragma unroll
-        for (int i = 0; i < C::NX; ++i) h[i] = x[i] * inv * gf[i];
-        prefetch_gains(oi);
+            for (int w = 0; w < kConsWarps; ++w) ss += S.nred[npar & 1][w];
+            return rsqrtf(ss / (float)D + p.eps);
+        } else {
+            return 1.f;
+        }
     }
 
     // ----------------------------------------------------------------- GEMV
@@ -461,7 +466,8 @@ struct Streamer {
             if (t < nb / 2) {
                 const int j = lp.qkv_begin + b0 / 2 + t;
                 const int hs = j / half, c = j % half;
-                float a = row_sum(2 * t), b = row_sum(2 * t + 1);
+                const float inv = inv_rms();
+                float a = row_sum(2 * t) * inv, b = row_sum(2 * t + 1) * inv;
                 if (hs < p.HQ_L + p.HKV_L) {  // RoPE on q and k
                     const float2 cs = b0 == 0 ? cs0 : __ldg(p.rope + (size_t)p.pos * half + c);
                     const float a2 = a * cs.x - b * cs.y;
@@ -498,7 +504,8 @@ struct Streamer {
         dot_op(2 * lp.ffn_n, [&](int b0, int nb) {
             const int t = tid;
             if (t < nb / 2) {
-                const float a = row_sum(2 * t), b = row_sum(2 * t + 1);
+                const float inv = inv_rms();
+                const float a = row_sum(2 * t) * inv, b = row_sum(2 * t + 1) * inv;
                 S.ubuf[b0 / 2 + t] = a / (1.f + expf(-a)) * b;
             }
         });
@@ -555,7 +562,7 @@ struct Streamer {
         dot_op(cp.lm_count, [&](int b0, int nb) {
             if (tid < nb) {
                 const int v = cp.lm_begin + b0 + tid;
-                const float z = row_sum(tid);
+                const float z = row_sum(tid) * inv_rms();
                 p.logits[v] = z;
                 if (better(z, v, bv, bi)) { bv = z; bi = v; }
             }
@@ -595,11 +602,11 @@ struct Streamer {
                 S.t_sync = S.t_tile = 0;
             }
             const int t = op_type(op);
-            if (t == OP_QKV || t == OP_GATEUP || t == OP_DOWN || t == OP_OPROJ) prefetch_add(oi);
+            if (t == OP_QKV || t == OP_GATEUP || t == OP_DOWN || t == OP_OPROJ) prefetch_add(op);
             switch (t) {
-                case OP_EMBED: embed(); prefetch_gains(oi); break;
+                case OP_EMBED: embed(); prefetch_gains(op); break;
                 case OP_ADD: add(a); break;
-                case OP_NORM: norm(a, oi); break;
+                case OP_NORM: norm(a, op); break;
                 case OP_QKV: qkv(a); break;
                 case OP_GATEUP: gateup(a); break;
                 case OP_DOWN: down(a); break;
@@ -667,11 +674,11 @@ struct Attention {
         attn_sync();
     }
 
-    // Bulk-loads keys [j0, j0 + n) of the chunk's HC KV heads (K of head g at
-    // g*kt keys, V likewise in the second half) and waits for them.
-    __device__ void load_tile(int l, int lane_id, int g0, int j0, int n) {
+    // Bulk-loads keys [j0, j0 + n) of the chunk's HC KV heads into the tile
+    // buffer (K of head g at g*kt keys, V likewise in the second half).  Only
+    // thread 0 issues; the buffer must be free (after the previous tile).
+    __device__ void issue_tile(int l, int lane_id, int g0, int j0, int n) {
         const int kt = p.kt, HC = p.hc;
-        const uint32_t par = ntile & 1u;  // tile i completes phase i of S.abar
         if (at == 0 && !S.abort_ && issued == ntile) {
             const uint32_t bytes = (uint32_t)n * DH * 2;
             mbar_arrive_expect_tx(&S.abar, 2u * HC * bytes);
@@ -683,9 +690,13 @@ struct Attention {
             }
             ++issued;
         }
+    }
+
+    // Waits for the tile issued last (tile i completes phase i of S.abar).
+    __device__ void wait_tile() {
         attn_sync();
         // (in abort mode nothing may have been issued: the loop then stops at once)
-        while (!S.abort_ && !mbar_try_wait(&S.abar, par)) {
+        while (!S.abort_ && !mbar_try_wait(&S.abar, ntile & 1u)) {
             if (global_timer_ns() > deadline) fail(2);
         }
         ++ntile;
@@ -784,11 +795,14 @@ struct Attention {
     __device__ void attention(int l) {
         const CtaPlan cp = p.cta[cta];
         const int S_ = cp.S, GL = p.GL, HC = p.hc, kt = p.kt, NQ = HC * GL, items = NQ * DH;
-        wait_geq(&p.barA[l * p.NL + cp.lane], p.epoch * (uint32_t)S_);
         int a, b;
         attn_range(p.pos, p.window[l], cp.k, S_, &a, &b);
         const bool last = (cp.k == S_ - 1);
         const int n_prev = b - a, T = (n_prev + kt - 1) / kt, T_eff = (last && T == 0) ? 1 : T;
+        // earlier keys do not depend on this step: fetch the first tile before
+        // waiting for the lane's QKV rows
+        if (T > 0) issue_tile(l, cp.lane, 0, a, min(kt, n_prev));
+        wait_geq(&p.barA[l * p.NL + cp.lane], p.epoch * (uint32_t)S_);
         const float *qkvb = p.qkv + ((size_t)l * p.NL + cp.lane) * p.qkv_l;
         for (int g0 = 0; g0 < p.HKV_L; g0 += HC) {
             // one round trip: q of the chunk's heads and (last CTA) this step's k, v
@@ -809,7 +823,10 @@ struct Attention {
             for (int i = 0; i < C::IPT; ++i) acc[i] = 0.f;
             for (int t = 0; t < T_eff; ++t) {
                 const int n = t < T ? min(kt, n_prev - t * kt) : 0;
-                if (t < T) load_tile(l, cp.lane, g0, a + t * kt, n);
+                if (t < T) {
+                    if (!(g0 == 0 && t == 0)) issue_tile(l, cp.lane, g0, a + t * kt, n);
+                    wait_tile();
+                }
                 tile_update(n, last && t == T_eff - 1, acc);
             }
             float *dst = p.apart + (((size_t)l * p.n_cta + cta) * p.HQ_L + (size_t)g0 * GL) * (DH + 2);
@@ -831,7 +848,8 @@ struct Attention {
     }
 
     // Merge of all lane CTAs' attention partials for this CTA's o_proj input
-    // columns into S.obuf[l & 1]; then tells the streaming warps.
+    // columns into S.obuf[l & 1]; then tells the streaming warps.  The (m, l)
+    // pairs and the first accumulators are loaded in one round trip.
     __device__ void merge(int l) {
         const LayerPlan lp = p.lp[(size_t)cta * p.L + l];
         const CtaPlan cp = p.cta[cta];
@@ -842,6 +860,19 @@ struct Attention {
             const int a0 = lp.o_begin / DH, nh = (lp.o_begin + lp.o_n - 1) / DH - a0 + 1;
             const size_t stride = (size_t)p.HQ_L * (DH + 2);
             const float *base = p.apart + ((size_t)l * p.n_cta + cp.cta0) * stride;
+            const int kk = at & 3;
+            constexpr int PRE = 8;  // accumulators per thread fetched up front (CTAs kk, kk+4, ...)
+            float v[PRE];
+            {
+                const int r = at >> 2;
+                const int c = lp.o_begin + (r < lp.o_n ? r : 0);
+                const float *q = base + (size_t)(c / DH) * (DH + 2) + c % DH;
+#pragma unroll
+                for (int i = 0; i < PRE; ++i) {
+                    const int k = kk + 4 * i;
+                    v[i] = (r < lp.o_n && k < S_) ? __ldcg(q + k * stride) : 0.f;
+                }
+            }
             for (int t = at; t < nh * S_; t += kAttnThreads) {
                 const int hh = t / S_, k = t % S_;
                 const float *q = base + k * stride + (size_t)(a0 + hh) * (DH + 2) + DH;
@@ -855,8 +886,8 @@ struct Attention {
                 M = warp_max(M);
                 float den = 0.f;
                 for (int k = lane; k < S_; k += 32) {
-                    const float2 v = S.ml[hh][k];
-                    den += (v.x == -INFINITY) ? 0.f : expf(v.x - M) * v.y;
+                    const float2 w = S.ml[hh][k];
+                    den += (w.x == -INFINITY) ? 0.f : expf(w.x - M) * w.y;
                 }
                 den = warp_sum(den);
                 for (int k = lane; k < S_; k += 32) {  // each lane rewrites only its own entries
@@ -866,15 +897,24 @@ struct Attention {
             }
             attn_sync();
             // row r, CTA subset k = kk, kk+4, ...: 4 lanes per row
-            const int kk = at & 3;
             for (int rb = 0; rb < lp.o_n; rb += kAttnThreads / 4) {
                 const int r = rb + (at >> 2);
                 float s = 0.f;
                 if (r < lp.o_n) {
                     const int c = lp.o_begin + r, hh = c / DH - a0;
                     const float *q = base + (size_t)(c / DH) * (DH + 2) + c % DH;
-#pragma unroll 4
-                    for (int k = kk; k < S_; k += 4) s = fmaf(S.ml[hh][k].x, __ldcg(q + k * stride), s);
+                    int i = 0;
+                    for (int k = kk; k < S_; k += 4, ++i) {
+                        float val;
+                        if (rb == 0 && i < PRE) {
+                            val = 0.f;
+#pragma unroll
+                            for (int j = 0; j < PRE; ++j) val = (j == i) ? v[j] : val;
+                        } else {
+                            val = __ldcg(q + k * stride);
+                        }
+                        s = fmaf(S.ml[hh][k].x, val, s);
+                    }
                 }
                 s += __shfl_xor_sync(0xffffffffu, s, 1);
                 s += __shfl_xor_sync(0xffffffffu, s, 2);

@@ -114,9 +114,17 @@ static std::vector<int> build_ops(const Shape &s) {
             adds_upto(sf - 1 - 2 * d);
             ops.push_back(make_op(OP_NORM, L + l));
             ops.push_back(make_op(OP_GATEUP, l));
-            ops.push_back(make_op(OP_DOWN, l));
-            ops.push_back(make_op(OP_ATTN, l));
-            ops.push_back(make_op(OP_OPROJ, l));
+            if (l + 1 < L) {
+                ops.push_back(make_op(OP_DOWN, l));
+                ops.push_back(make_op(OP_ATTN, l));
+                ops.push_back(make_op(OP_OPROJ, l));
+            } else {
+                // last layer: o_proj first, so that its lane sum is formed
+                // while down_proj streams, shortening the drain
+                ops.push_back(make_op(OP_ATTN, l));
+                ops.push_back(make_op(OP_OPROJ, l));
+                ops.push_back(make_op(OP_DOWN, l));
+            }
         }
     }
     adds_upto(2 * L - 1);
@@ -141,6 +149,15 @@ static std::vector<int> build_ops(const Shape &s) {
     for (int i = 0; i <= (int)ops.size(); ++i) {
         for (int r : insert_before[i]) out.push_back(r);
         if (i < (int)ops.size()) out.push_back(ops[i]);
+    }
+    // lookahead fields used by the streaming warps' prefetches
+    for (int i = 0; i < (int)out.size(); ++i) {
+        int next_norm = 0xff, next_add = 0xff;
+        for (int j = i + 1; j < (int)out.size(); ++j)
+            if (op_type(out[j]) == OP_NORM) { next_norm = op_arg(out[j]); break; }
+        for (int j = i + 1; j < (int)out.size() && j <= i + 4; ++j)
+            if (op_type(out[j]) == OP_ADD) { next_add = op_arg(out[j]); break; }
+        out[i] = (out[i] & 0xffff) | (next_norm << 16) | ((unsigned)next_add << 24);
     }
     return out;
 }
