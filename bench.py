@@ -261,8 +261,9 @@ def run_ours(args, world, rank, local):
     eng.set_stream(stream.cuda_stream)
     eng.load_weights(blob)
     eng.load_kv(kv, POS)
-    if args.l2_prefetch_kb >= 0:
-        eng.set_l2_prefetch(args.l2_prefetch_kb * 1024)
+    if args.l2_prefetch_kb >= 0 or args.lm_prefetch_kb >= 0:
+        eng.set_l2_prefetch(max(args.l2_prefetch_kb, 0) * 1024 if args.l2_prefetch_kb >= 0 else 128 * 1024,
+                            args.lm_prefetch_kb * 1024 if args.lm_prefetch_kb >= 0 else 128 * 1024)
 
     def barrier():
         if world > 1:
@@ -360,6 +361,8 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--l2-prefetch-kb", type=int, default=-1,
                     help="weight-stream L2 prefetch distance per SM (default: the engine's)")
+    ap.add_argument("--lm-prefetch-kb", type=int, default=-1,
+                    help="LM-head L2 prefetch distance per SM (default: the engine's)")
     ap.add_argument("--trace", default="", help="write a one-step op trace (JSON) to this path")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: same width with fewer layers (not a bench number)")

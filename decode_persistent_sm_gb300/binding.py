@@ -42,7 +42,7 @@ _SIGS = {
     "lf_engine_info": (_ci, [_vp, _vp]),
     "lf_decode_step_static_scratch": (_ci, [_vp, _i32, _vp, _vp]),
     "lf_debug_trace": (_ci, [_vp, _ci]),
-    "lf_set_l2_prefetch": (_ci, [_vp, ctypes.c_uint32]),
+    "lf_set_l2_prefetch": (_ci, [_vp, ctypes.c_uint32, ctypes.c_uint32]),
     "lf_debug_read_trace": (_ci, [_vp, _vp, ctypes.c_size_t, _vp]),
 }
 
@@ -222,8 +222,9 @@ class Engine:
     def set_timeout_ns(self, ns: int):
         _check("lf_set_timeout_ns", self._lib.lf_set_timeout_ns(self._h, int(ns)))
 
-    def set_l2_prefetch(self, bytes_per_sm: int):
-        _check("lf_set_l2_prefetch", self._lib.lf_set_l2_prefetch(self._h, int(bytes_per_sm)))
+    def set_l2_prefetch(self, bytes_per_sm: int, lm_bytes_per_sm: int = 128 * 1024):
+        _check("lf_set_l2_prefetch",
+               self._lib.lf_set_l2_prefetch(self._h, int(bytes_per_sm), int(lm_bytes_per_sm)))
 
     def debug_skip_arrival(self, cta: int):
         _check("lf_debug_skip_arrival", self._lib.lf_debug_skip_arrival(self._h, int(cta)))

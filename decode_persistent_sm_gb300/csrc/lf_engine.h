@@ -35,6 +35,7 @@ struct lf_engine {
     unsigned long long timeout_ns = 2000000000ull;
     int skip_cta = -1;
     unsigned l2_prefetch_bytes = 128u * 1024u;
+    unsigned lm_prefetch_bytes = 128u * 1024u;
     size_t dev_bytes = 0;
     long long launches = 0;
     std::vector<void *> allocs;

@@ -514,7 +514,7 @@ struct Streamer {
     __device__ void down(int l) {
         const LayerPlan lp = p.lp[(size_t)cta * p.L + l];
         const int u = 2 * l + 1;
-        axpy_op(lp.ffn_n, S.ubuf, p.part + ((size_t)u * p.n_cta + cta) * D);
+        axpy_op(lp.ffn_n, S.ubuf, p.part + ((size_t)(u % p.pslots) * p.n_cta + cta) * D);
         arrive(&p.cnt[u]);
     }
 
@@ -533,7 +533,7 @@ struct Streamer {
         }
         cons_sync();
         const int u = 2 * l;
-        axpy_op(lp.o_n, S.obuf[l & 1], p.part + ((size_t)u * p.n_cta + cta) * D);
+        axpy_op(lp.o_n, S.obuf[l & 1], p.part + ((size_t)(u % p.pslots) * p.n_cta + cta) * D);
         arrive(&p.cnt[u]);
     }
 
@@ -973,13 +973,13 @@ __device__ void produce(const KParams &p, Smem<D, DH> &S, uint8_t *stages, uint6
         }
         return !S.abort_;
     };
-    auto rows = [&](int n_rows) {
+    auto rows = [&](int n_rows, unsigned ahead) {
         for (int r0 = 0; r0 < n_rows && !stop; r0 += C::RPT) {
             const int n = min(C::RPT, n_rows - r0);
             int stage;
             if (!claim(stage)) { stop = true; return; }
             const uint32_t bytes = (uint32_t)n * 2 * D;
-            const uint8_t *want = w + bytes + p.l2_prefetch_bytes;
+            const uint8_t *want = w + bytes + ahead;
             if (want > w_end) want = w_end;
             while (pf < want) {
                 const uint32_t nb = (uint32_t)min((size_t)kStageBytes, (size_t)(want - pf));
@@ -996,11 +996,12 @@ __device__ void produce(const KParams &p, Smem<D, DH> &S, uint8_t *stages, uint6
     for (int oi = 0; oi < p.n_ops && !stop; ++oi) {
         const int op = __ldg(p.ops + oi);
         const int t = op_type(op), l = op_arg(op);
-        if (t == OP_QKV) rows(2 * p.lp[(size_t)cta * p.L + l].qkv_n);
-        else if (t == OP_GATEUP) rows(2 * p.lp[(size_t)cta * p.L + l].ffn_n);
-        else if (t == OP_DOWN) rows(p.lp[(size_t)cta * p.L + l].ffn_n);
-        else if (t == OP_OPROJ) rows(p.lp[(size_t)cta * p.L + l].o_n);
-        else if (t == OP_LMHEAD) rows(cp.lm_count);
+        const unsigned ahead = p.l2_prefetch_bytes;
+        if (t == OP_QKV) rows(2 * p.lp[(size_t)cta * p.L + l].qkv_n, ahead);
+        else if (t == OP_GATEUP) rows(2 * p.lp[(size_t)cta * p.L + l].ffn_n, ahead);
+        else if (t == OP_DOWN) rows(p.lp[(size_t)cta * p.L + l].ffn_n, ahead);
+        else if (t == OP_OPROJ) rows(p.lp[(size_t)cta * p.L + l].o_n, ahead);
+        else if (t == OP_LMHEAD) rows(cp.lm_count, p.lm_prefetch_bytes);
     }
     S.issued = (int)it;
     __threadfence_block();
@@ -1042,7 +1043,7 @@ __device__ void help(const KParams &p, Smem<D, DH> &S, uint64_t deadline) {
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
-        const float *src = p.part + (size_t)u * p.n_cta * D + kRChunk * cta;
+        const float *src = p.part + (size_t)(u % p.pslots) * p.n_cta * D + kRChunk * cta;
         for (int k = lane; k < p.n_cta; k += 32)
             bulk_g2s(S.hbuf[k], src + (size_t)k * D, kRChunk * 4, &S.hbar);
         ++issued;

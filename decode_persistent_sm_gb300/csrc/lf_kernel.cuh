@@ -13,6 +13,7 @@ struct KParams {
     // shape
     int L, D, DH, HQ_L, HKV_L, GL, F_L, V, NL, n_cta, ctx, n_ops, nch, qkv_l;
     int hc, kt;  // attention: KV heads per chunk, keys per tile
+    int pslots;  // lane-sum partial slots
     float eps, attn_scale;
     // this step
     int pos, token;
@@ -20,6 +21,7 @@ struct KParams {
     unsigned long long timeout_ns;
     int skip_arrive_cta;
     unsigned l2_prefetch_bytes;  // weight-stream L2 prefetch distance beyond the stage ring
+    unsigned lm_prefetch_bytes;  // the same for the LM-head rows (the step's drain is idle HBM time)
     int window[LF_MAX_LAYERS];
     // plan
     const int *ops;
@@ -34,7 +36,7 @@ struct KParams {
     __half *kc, *vc;        // [lane][L][HKV_L][ctx][DH]
     float *qkv;             // [L][NL][qkv_l]
     float *apart;           // [L][n_cta][HQ_L][DH+2]: acc[DH], m, l
-    float *part;            // [2L][n_cta][D]
+    float *part;            // [pslots][n_cta][D], sub-block u in slot u % pslots
     float *R;               // [2L][D]
     uint32_t *barA, *barB;  // [L][NL]
     uint32_t *cnt, *ready;  // [2L]

@@ -59,7 +59,7 @@ Carve carve(const lf_engine *e) {
     const size_t qkv_l = (size_t)(s.HQ_L + 2 * s.HKV_L) * s.DH;
     Carve c{};
     size_t at = 0;
-    c.part = at; at += align256(2 * L * NC * s.D * sizeof(float));
+    c.part = at; at += align256((size_t)s.PS * NC * s.D * sizeof(float));
     c.R = at; at += align256(2 * L * s.D * sizeof(float));
     c.qkv = at; at += align256(L * s.NL * qkv_l * sizeof(float));
     c.apart = at; at += align256(L * NC * s.HQ_L * (s.DH + 2) * sizeof(float));
@@ -106,6 +106,7 @@ extern "C" lf_status lf_decode_step_static_scratch(lf_engine *e, int32_t token,
     k.n_ops = (int)P.ops.size(); k.nch = s.D / lf::kRChunk; k.qkv_l = (s.HQ_L + 2 * s.HKV_L) * s.DH;
     k.hc = s.HC;
     k.kt = s.KT;
+    k.pslots = s.PS;
     k.eps = e->cfg.rms_eps;
     k.attn_scale = (float)(1.0 / std::sqrt((double)s.DH));
     k.pos = e->pos;
@@ -114,6 +115,7 @@ extern "C" lf_status lf_decode_step_static_scratch(lf_engine *e, int32_t token,
     k.timeout_ns = e->timeout_ns;
     k.skip_arrive_cta = -1;
     k.l2_prefetch_bytes = e->l2_prefetch_bytes;
+    k.lm_prefetch_bytes = e->lm_prefetch_bytes;
     for (int l = 0; l < s.L; ++l) k.window[l] = e->cfg.swa_window[l];
     k.ops = e->d_ops; k.cta = e->d_cta; k.lp = e->d_lp;
     k.wstream = e->wstream; k.emb = e->emb; k.gains = e->gains; k.rope = e->rope;

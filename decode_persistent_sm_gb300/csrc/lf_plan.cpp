@@ -64,6 +64,10 @@ lf_status derive_shape(const lf_config &c, Shape *sh) {
     while (s.HC * s.GL * s.DH > kConsThreads) s.HC /= 2;
     if (s.HC < 1 || s.HKV_L % s.HC) return LF_ERR_UNSUPPORTED;
     s.KT = (kAttnBuf / 2) / (s.HC * s.DH * 2);
+    // Slot u % PS may be rewritten by sub-block u + PS once every CTA has
+    // added R[u], which happens before sub-block u + 1 + 2d; PS = 2d + 4
+    // keeps the partials few enough to stay in L2.
+    s.PS = std::min(2 * s.L, 2 * s.delay + 4);
     if (s.KT < 1 || s.HC * s.GL * (s.KT + 1) > kAttnScores) return LF_ERR_UNSUPPORTED;
     return LF_OK;
 }

@@ -20,6 +20,7 @@ struct Shape {
     int NO;     // o_proj input columns per lane: HQ_L * DH
     int HC;     // KV heads processed together in attention (HC * GL * DH <= 512)
     int KT;     // keys per attention tile: K and V of HC heads fill one stage
+    int PS;     // lane-sum partial slots (sub-block u uses slot u % PS)
     std::vector<int> kv_first;  // per lane: first global KV head it reads
     // element offsets in the FP16 blob
     long long off_E, per_layer, off_layer0, off_gf, off_lm, n_params;

@@ -234,7 +234,7 @@ lf_status lf_create(const lf_config *cfg, lf_engine **out) {
     ALLOC(vc, kv_elems);
     ALLOC(qkv, (size_t)L * s.NL * qkv_l);
     ALLOC(apart, (size_t)L * NC * s.HQ_L * (s.DH + 2));
-    ALLOC(part, (size_t)2 * L * NC * s.D);
+    ALLOC(part, (size_t)s.PS * NC * s.D);
     ALLOC(R, (size_t)2 * L * s.D);
     ALLOC(ctr, e->n_ctr);
     ALLOC(status, 8);
@@ -388,6 +388,7 @@ lf_status lf_decode_step(lf_engine *e, int32_t token, float *logits, int32_t *ar
     k.n_ops = (int)P.ops.size(); k.nch = s.D / lf::kRChunk; k.qkv_l = (s.HQ_L + 2 * s.HKV_L) * s.DH;
     k.hc = s.HC;
     k.kt = s.KT;
+    k.pslots = s.PS;
     k.eps = e->cfg.rms_eps;
     k.attn_scale = (float)(1.0 / std::sqrt((double)s.DH));
     k.pos = e->pos;
@@ -396,6 +397,7 @@ lf_status lf_decode_step(lf_engine *e, int32_t token, float *logits, int32_t *ar
     k.timeout_ns = e->timeout_ns;
     k.skip_arrive_cta = e->skip_cta;
     k.l2_prefetch_bytes = e->l2_prefetch_bytes;
+    k.lm_prefetch_bytes = e->lm_prefetch_bytes;
     for (int l = 0; l < s.L; ++l) k.window[l] = e->cfg.swa_window[l];
     k.ops = e->d_ops; k.cta = e->d_cta; k.lp = e->d_lp;
     k.wstream = e->wstream; k.emb = e->emb; k.gains = e->gains; k.rope = e->rope;
@@ -521,9 +523,12 @@ lf_status lf_set_timeout_ns(lf_engine *e, uint64_t ns) {
     return LF_OK;
 }
 
-lf_status lf_set_l2_prefetch(lf_engine *e, uint32_t bytes_per_sm) {
-    if (!e || (bytes_per_sm % 16) != 0 || bytes_per_sm > (64u << 20)) return LF_ERR_INVALID_ARG;
+lf_status lf_set_l2_prefetch(lf_engine *e, uint32_t bytes_per_sm, uint32_t lm_bytes_per_sm) {
+    if (!e || (bytes_per_sm % 16) != 0 || bytes_per_sm > (64u << 20) || (lm_bytes_per_sm % 16) != 0 ||
+        lm_bytes_per_sm > (64u << 20))
+        return LF_ERR_INVALID_ARG;
     e->l2_prefetch_bytes = bytes_per_sm;
+    e->lm_prefetch_bytes = lm_bytes_per_sm;
     return LF_OK;
 }
 

@@ -140,11 +140,13 @@ lf_status lf_read_kv(lf_engine *e, int layer, int kv_head, int pos, float *k, fl
  * runs out makes the step fail with LF_ERR_TIMEOUT instead of hanging. */
 lf_status lf_set_timeout_ns(lf_engine *e, uint64_t ns);
 
-/* Tuning: how far (bytes per SM, multiple of 16, default 128 KiB) each SM's
- * weight stream is prefetched into L2 beyond its shared-memory stages, so
- * that HBM keeps streaming while an SM does latency-bound work (attention,
- * lane sums).  0 turns the prefetch off. */
-lf_status lf_set_l2_prefetch(lf_engine *e, uint32_t bytes_per_sm);
+/* Tuning: how far (bytes per SM, multiples of 16) each SM's weight stream is
+ * prefetched into L2 beyond its shared-memory stages, so that HBM keeps
+ * streaming while the SM does latency-bound work.  bytes_per_sm applies to the
+ * layers (default 128 KiB), lm_bytes_per_sm to the LM-head rows, which are
+ * reached while the step drains its last lane sums (default 128 KiB).  0 turns
+ * a prefetch off. */
+lf_status lf_set_l2_prefetch(lf_engine *e, uint32_t bytes_per_sm, uint32_t lm_bytes_per_sm);
 
 /* Test hook: in the next decode step, CTA `cta` skips its first lane-barrier
  * arrival (-1 = off), so that the lane's other CTAs time out.  Proves that the
@@ -186,11 +188,11 @@ lf_status lf_debug_read_trace(lf_engine *e, uint64_t *out, size_t n_words, int32
  * streams, or from other engines on the same device) race on the array: issue
  * them one after another.  Synchronous: waits for the step and reports a
  * device-side timeout.  Returns LF_ERR_UNSUPPORTED when the engine's working
- * set does not fit the array (the full 2.3B lane model needs about 80 MB on
+ * set does not fit the array (the full 2.3B lane model needs about 26 MB on
  * 152 SMs), LF_ERR_INVALID_ARG for null outputs or another current device,
  * and the same statuses as lf_decode_step otherwise.
  */
-#define LF_STATIC_SCRATCH_BYTES (96u * 1024u * 1024u)
+#define LF_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
 lf_status lf_decode_step_static_scratch(lf_engine *e, int32_t token, float *logits_device,
                                         int32_t *argmax_device);
 

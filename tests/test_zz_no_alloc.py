@@ -75,7 +75,9 @@ def test_full_model_two_calls_match_decode_step():
 def test_rejects_working_set_beyond_the_array_and_null_outputs():
     import torch
     from decode_persistent_sm_gb300 import Engine
-    big = synth.FULL.replace(n_layers=24, swa_window=synth.FULL.swa_window + (0,) * 9, ctx_cap=64)
+    # 24 layers with delay 10: 24 slots of lane-sum partials (~60 MB) > the array
+    big = synth.FULL.replace(n_layers=24, swa_window=synth.FULL.swa_window + (0,) * 9, ctx_cap=64,
+                             dtp_delay=10)
     logits_dev = torch.empty(big.vocab, dtype=torch.float32, device="cuda")
     argmax_dev = torch.empty(1, dtype=torch.int32, device="cuda")
     with Engine.from_shape(big) as eng:
