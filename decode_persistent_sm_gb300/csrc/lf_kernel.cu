@@ -78,6 +78,7 @@ struct Smem {
     int last;
     volatile int cur_op;
     unsigned long long t_sync, t_tile;  // trace: blocked time in the current op (thread 0)
+    unsigned long long a_tbar, a_ttile; // trace: attention warps blocked on lane barriers / tiles
     volatile int oflag;                 // layers whose o_proj inputs are merged
     volatile int abort_;
     volatile int prod_done;
@@ -614,7 +615,7 @@ struct Streamer {
                 case OP_LMHEAD: lmhead(); break;
                 default: break;  // ATTN: attention warps; REDUCE: helper warp
             }
-            if (p.trace && tid == 0) {
+            if (p.trace && tid == 0 && t != OP_ATTN) {
                 unsigned long long *tr = p.trace + ((size_t)cta * p.n_ops + oi) * 4;
                 tr[0] = t_start;
                 tr[1] = global_timer_ns();
@@ -665,11 +666,13 @@ struct Attention {
 
     __device__ void wait_geq(const uint32_t *ptr, uint32_t target) {
         if (at == 0 && !S.abort_) {
+            const uint64_t t0 = p.trace ? global_timer_ns() : 0;
             while (true) {
                 if ((int)(ld_acquire(ptr) - target) >= 0) break;
                 if (ld_relaxed(p.err) != 0u) { S.abort_ = 1; break; }
                 if (global_timer_ns() > deadline) { fail(1); break; }
             }
+            if (p.trace) S.a_tbar += global_timer_ns() - t0;
         }
         attn_sync();
     }
@@ -695,10 +698,12 @@ struct Attention {
     // Waits for the tile issued last (tile i completes phase i of S.abar).
     __device__ void wait_tile() {
         attn_sync();
+        const uint64_t t0 = (p.trace && at == 0) ? global_timer_ns() : 0;
         // (in abort mode nothing may have been issued: the loop then stops at once)
         while (!S.abort_ && !mbar_try_wait(&S.abar, ntile & 1u)) {
             if (global_timer_ns() > deadline) fail(2);
         }
+        if (p.trace && at == 0) S.a_ttile += global_timer_ns() - t0;
         ++ntile;
     }
 
@@ -933,8 +938,17 @@ struct Attention {
             const int op = __ldg(p.ops + oi);
             if (op_type(op) != OP_ATTN) continue;
             cur_op = oi;
+            const uint64_t t_start = (p.trace && at == 0) ? global_timer_ns() : 0;
+            if (at == 0) S.a_tbar = S.a_ttile = 0;
             attention(op_arg(op));
             merge(op_arg(op));
+            if (p.trace && at == 0) {  // the ATTN op's trace slot belongs to these warps
+                unsigned long long *tr = p.trace + ((size_t)cta * p.n_ops + oi) * 4;
+                tr[0] = t_start;
+                tr[1] = global_timer_ns();
+                tr[2] = S.a_tbar;
+                tr[3] = S.a_ttile;
+            }
         }
         // after an error, let the last attention tile thread 0 issued land
         // (tiles complete in order, so the last one's phase covers them all)

@@ -110,21 +110,25 @@ static std::vector<int> build_ops(const Shape &s) {
             ops.push_back(make_op(OP_DOWN, l));
         } else {
             // With a delay the FFN of layer l does not read the attention of
-            // layer l, so it is streamed while the lane barrier of the QKV
-            // rows settles; o_proj comes last, after the attention barrier.
+            // layer l, so it is streamed while the attention runs beside it.
+            // With a delay of 2 or more, o_proj of layer l - 1 (whose lane sum
+            // is first read at sub-block 2l + 3) waits until after the QKV rows
+            // of layer l, which gives the attention warps a layer's worth of
+            // slack.  The last layer runs o_proj before down_proj, so that
+            // its lane sum is formed while down_proj streams.
+            const bool late = (d >= 2);
             adds_upto(sa - 1 - 2 * d);
             ops.push_back(make_op(OP_NORM, l));
             ops.push_back(make_op(OP_QKV, l));
+            if (late && l > 0) ops.push_back(make_op(OP_OPROJ, l - 1));
             adds_upto(sf - 1 - 2 * d);
             ops.push_back(make_op(OP_NORM, L + l));
             ops.push_back(make_op(OP_GATEUP, l));
             if (l + 1 < L) {
                 ops.push_back(make_op(OP_DOWN, l));
                 ops.push_back(make_op(OP_ATTN, l));
-                ops.push_back(make_op(OP_OPROJ, l));
+                if (!late) ops.push_back(make_op(OP_OPROJ, l));
             } else {
-                // last layer: o_proj first, so that its lane sum is formed
-                // while down_proj streams, shortening the drain
                 ops.push_back(make_op(OP_ATTN, l));
                 ops.push_back(make_op(OP_OPROJ, l));
                 ops.push_back(make_op(OP_DOWN, l));
