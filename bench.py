@@ -36,7 +36,16 @@ UNIT = "tokens/s"
 POS = 512
 SEED = 1
 PROFILE = os.path.join(ROOT, "profiles", "decode_kernel_full_p512.txt")
-KERNEL_SRC = os.path.join(ROOT, "decode_persistent_sm_gb300", "csrc", "lf_kernel.cu")
+# the sources that decide what the decode kernel reads and writes
+KERNEL_SRCS = [os.path.join(ROOT, "decode_persistent_sm_gb300", "csrc", f)
+               for f in ("lf_kernel.cu", "lf_kernel.cuh", "lf_ptx.cuh", "lf_common.h", "lf_plan.cpp")]
+
+
+def kernel_sources_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SRCS:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
 
 
 def algorithmic_bytes(shape, pos: int) -> int:
@@ -118,8 +127,7 @@ def profile_traffic():
         if "=" in line and not line.startswith("#"):
             k, v = line.split("=", 1)
             kv[k.strip()] = v.strip()
-    src_hash = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
-    if kv.get("kernel_source_sha256_16") != src_hash:
+    if kv.get("kernel_sources_sha256_16") != kernel_sources_hash():
         return None
     try:
         return int(float(kv["dram_bytes_per_launch"]))
@@ -165,35 +173,44 @@ def write_trace(eng, path, tokens, shape):
     tr, ops = eng.read_trace()
     eng.trace(False)
     tr = tr.astype(np.int64)
-    t0 = tr[:, 0, 0].min()
+    t0 = tr[:, 0, 0].min()  # EMBED, written by every CTA
     step_ns = int(tr[:, -1, 1].max() - t0)
     dur = tr[:, :, 1] - tr[:, :, 0]
     by = {}
+    # a REDUCE slot is written only by the CTAs that sum a chunk (others: 0)
+    rows = [np.nonzero(tr[:, j, 0])[0] for j in range(len(ops))]
     for j, op in enumerate(ops):
         name = OP_NAMES[int(op) & 0xFF]
-        b = by.setdefault(name, [0.0, 0.0, 0.0, 0])
-        b[0] += dur[:, j].mean()
-        b[1] += tr[:, j, 2].mean()
-        b[2] += tr[:, j, 3].mean()
+        b = by.setdefault(name, [0.0, 0.0, 0.0, 0, 0.0])
+        r = rows[j]
+        b[0] += dur[r, j].mean()
+        b[1] += tr[r, j, 2].mean()
+        b[2] += tr[r, j, 3].mean()
         b[3] += 1
+        b[4] += tr[r, j, 4].mean()
     start_skew = int(tr[:, 0, 0].max() - t0)
     end_spread = int(tr[:, -1, 1].max() - tr[:, -1, 1].min())
     lm = [j for j, op in enumerate(ops) if int(op) & 0xFF == 9][0]
     out = {"step_ns": step_ns, "cta_start_skew_ns": start_skew, "cta_end_spread_ns": end_spread,
            "lmhead_start_ns_mean": float((tr[:, lm, 0] - t0).mean()),
-           "by_op": {k: {"count": v[3], "mean_ns": v[0], "sync_wait_ns": v[1], "tile_wait_ns": v[2]}
-                     for k, v in by.items()},
+           "by_op": {k: {"count": v[3], "mean_ns": v[0], "sync_wait_ns": v[1], "tile_wait_ns": v[2],
+                         "copy_warp_blocked_ns": v[4]} for k, v in by.items()},
            "per_op": [{"op": OP_NAMES[int(op) & 0xFF], "arg": (int(op) >> 8) & 0xFF,
-                       "start_ns_mean": float((tr[:, j, 0] - t0).mean()),
-                       "dur_ns_mean": float(dur[:, j].mean()), "dur_ns_max": int(dur[:, j].max()),
-                       "sync_ns_mean": float(tr[:, j, 2].mean()),
-                       "tile_ns_mean": float(tr[:, j, 3].mean())} for j, op in enumerate(ops)]}
+                       "ctas": int(len(rows[j])),
+                       "start_ns_mean": float((tr[rows[j], j, 0] - t0).mean()),
+                       "end_ns_max": int((tr[rows[j], j, 1] - t0).max()),
+                       "dur_ns_mean": float(dur[rows[j], j].mean()), "dur_ns_max": int(dur[rows[j], j].max()),
+                       "sync_ns_mean": float(tr[rows[j], j, 2].mean()),
+                       "tile_ns_mean": float(tr[rows[j], j, 3].mean()),
+                       "copy_blocked_ns_mean": float(tr[rows[j], j, 4].mean())} for j, op in enumerate(ops)]}
     with open(path, "w") as f:
         json.dump(out, f, indent=1)
+    np.savez_compressed(os.path.splitext(path)[0] + "_raw.npz", trace=tr, ops=ops)
     print(f"traced step: {step_ns / 1e3:.1f} us; CTA start skew {start_skew / 1e3:.1f} us", file=sys.stderr)
     for k, v in out["by_op"].items():
         print(f"  {k:7s} x{v['count']:3d}  {v['mean_ns'] / 1e3:8.1f} us  sync {v['sync_wait_ns'] / 1e3:7.1f}"
-              f"  tiles {v['tile_wait_ns'] / 1e3:7.1f}", file=sys.stderr)
+              f"  tiles {v['tile_wait_ns'] / 1e3:7.1f}  copy warp blocked {v['copy_warp_blocked_ns'] / 1e3:7.1f}",
+              file=sys.stderr)
 
 
 def dist_setup():

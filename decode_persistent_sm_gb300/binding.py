@@ -10,6 +10,7 @@ import numpy as np
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "liblaneformer.so")
 MAX_LAYERS = 64
+TRACE_WORDS = 6  # LF_TRACE_WORDS
 
 STATUS = {
     0: "LF_OK", 1: "LF_ERR_INVALID_ARG", 2: "LF_ERR_OOM", 3: "LF_ERR_CUDA",
@@ -240,10 +241,11 @@ class Engine:
         _check("lf_debug_trace", self._lib.lf_debug_trace(self._h, 1 if enable else 0))
 
     def read_trace(self):
-        """(trace [n_sm, n_ops, 4] uint64, ops [n_ops] int32) of the last traced step."""
+        """(trace [n_sm, n_ops, TRACE_WORDS] uint64, ops [n_ops] int32) of the
+        last traced step; the words per op are those of lf_debug_trace."""
         inf = self.info()
         n_sm, n_ops = inf["n_sm"], inf["n_ops"]
-        out = np.zeros((n_sm, n_ops, 4), dtype=np.uint64)
+        out = np.zeros((n_sm, n_ops, TRACE_WORDS), dtype=np.uint64)
         ops = np.zeros(n_ops, dtype=np.int32)
         _check("lf_debug_read_trace", self._lib.lf_debug_read_trace(
             self._h, out.ctypes.data, out.size, ops.ctypes.data))

@@ -143,6 +143,9 @@ struct Streamer {
 
     __device__ CtaPlan plan() const { return p.cta[cta]; }
     __device__ int col(int i) const { return C::kBlockRow ? 8 * (tid + kConsThreads * i) : 8 * lane; }
+    // Lane-sum partials are chunk-major, [chunk][cta][32 floats], so that the
+    // pieces one chunk's summing warp needs are contiguous.
+    __device__ size_t pidx(int c) const { return ((size_t)(c >> 5) * p.n_cta + cta) * kRChunk + (c & 31); }
     __device__ void fail(uint32_t code) { record_error(p, &S.abort_, code, S.cur_op); }
 
     // Thread 0 polls `ptr` until it reaches `target` (wrap-safe), the global
@@ -394,12 +397,27 @@ struct Streamer {
         }
     }
 
-    // acc += sum_r coef[r] * row_r over n_rows rows of d_model; writes the
-    // full-width partial to `out` (global).
-    __device__ void axpy_op(int n_rows, const float *coef, float *out) {
+    // acc += sum_r coef[r] * row_r over n_rows rows of d_model; writes this
+    // CTA's full-width partial into the lane-sum slot `out`.  onto = true
+    // starts from the partial already there, which this same thread wrote.
+    __device__ void axpy_op(int n_rows, const float *coef, float *out, bool onto) {
         float acc[C::NX];
+        if constexpr (C::kBlockRow) {
 #pragma unroll
-        for (int i = 0; i < C::NX; ++i) acc[i] = 0.f;
+            for (int i = 0; i < C::NCHT; ++i) {
+                float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+                if (onto) {
+                    a = __ldcg(reinterpret_cast<const float4 *>(out + pidx(col(i))));
+                    b = __ldcg(reinterpret_cast<const float4 *>(out + pidx(col(i))) + 1);
+                }
+                acc[8 * i + 0] = a.x; acc[8 * i + 1] = a.y; acc[8 * i + 2] = a.z; acc[8 * i + 3] = a.w;
+                acc[8 * i + 4] = b.x; acc[8 * i + 5] = b.y; acc[8 * i + 6] = b.z; acc[8 * i + 7] = b.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < C::NX; ++i) acc[i] = 0.f;
+        }
+        const float base = (!C::kBlockRow && onto && tid < D) ? __ldcg(out + pidx(tid)) : 0.f;
         for (int r0 = 0; r0 < n_rows; r0 += C::RPT) {
             const int n = min(C::RPT, n_rows - r0);
             const uint8_t *tile = wait_tile();
@@ -434,9 +452,12 @@ struct Streamer {
         if constexpr (C::kBlockRow) {
 #pragma unroll
             for (int i = 0; i < C::NCHT; ++i) {
-                float4 *o = reinterpret_cast<float4 *>(out + col(i));
-                o[0] = make_float4(acc[8 * i + 0], acc[8 * i + 1], acc[8 * i + 2], acc[8 * i + 3]);
-                o[1] = make_float4(acc[8 * i + 4], acc[8 * i + 5], acc[8 * i + 6], acc[8 * i + 7]);
+                float4 *o = reinterpret_cast<float4 *>(out + pidx(col(i)));
+                const float4 v0 = make_float4(acc[8 * i + 0], acc[8 * i + 1], acc[8 * i + 2], acc[8 * i + 3]);
+                const float4 v1 = make_float4(acc[8 * i + 4], acc[8 * i + 5], acc[8 * i + 6], acc[8 * i + 7]);
+                const uint64_t keep = policy_evict_last();  // kept in L2 until summed
+                st_hint(o, v0, keep);
+                st_hint(o + 1, v1, keep);
             }
         } else {
 #pragma unroll
@@ -446,7 +467,7 @@ struct Streamer {
                 float s = 0.f;
 #pragma unroll
                 for (int w = 0; w < kConsWarps; ++w) s += S.axbuf[w][tid];
-                out[tid] = s;
+                st_hint(out + pidx(tid), base + s, policy_evict_last());
             }
         }
     }
@@ -512,10 +533,14 @@ struct Streamer {
         });
     }
 
+    // With a delay, nothing but the final drain reads the last layer's two
+    // sub-blocks, so their partials are added in each CTA (down_proj first,
+    // o_proj onto it) and take one lane sum, published as sub-block 2L - 1.
     __device__ void down(int l) {
         const LayerPlan lp = p.lp[(size_t)cta * p.L + l];
         const int u = 2 * l + 1;
-        axpy_op(lp.ffn_n, S.ubuf, p.part + ((size_t)(u % p.pslots) * p.n_cta + cta) * D);
+        axpy_op(lp.ffn_n, S.ubuf, p.part + (size_t)(u % p.pslots) * p.n_cta * D, false);
+        if (p.tail_fused && l == p.L - 1) return;  // each thread reads back only its own columns
         arrive(&p.cnt[u]);
     }
 
@@ -533,8 +558,9 @@ struct Streamer {
             if (p.trace) S.t_sync += global_timer_ns() - t0;
         }
         cons_sync();
-        const int u = 2 * l;
-        axpy_op(lp.o_n, S.obuf[l & 1], p.part + ((size_t)(u % p.pslots) * p.n_cta + cta) * D);
+        const bool fused = p.tail_fused && l == p.L - 1;
+        const int u = fused ? 2 * l + 1 : 2 * l;
+        axpy_op(lp.o_n, S.obuf[l & 1], p.part + (size_t)(u % p.pslots) * p.n_cta * D, fused);
         arrive(&p.cnt[u]);
     }
 
@@ -615,8 +641,8 @@ struct Streamer {
                 case OP_LMHEAD: lmhead(); break;
                 default: break;  // ATTN: attention warps; REDUCE: helper warp
             }
-            if (p.trace && tid == 0 && t != OP_ATTN) {
-                unsigned long long *tr = p.trace + ((size_t)cta * p.n_ops + oi) * 4;
+            if (p.trace && tid == 0 && t != OP_ATTN && t != OP_REDUCE) {
+                unsigned long long *tr = p.trace + ((size_t)cta * p.n_ops + oi) * LF_TRACE_WORDS;
                 tr[0] = t_start;
                 tr[1] = global_timer_ns();
                 tr[2] = S.t_sync;
@@ -834,15 +860,17 @@ struct Attention {
                 }
                 tile_update(n, last && t == T_eff - 1, acc);
             }
+            // scratch read back within this layer: kept in L2 ahead of the weight stream
             float *dst = p.apart + (((size_t)l * p.n_cta + cta) * p.HQ_L + (size_t)g0 * GL) * (DH + 2);
+            const uint64_t keep = policy_evict_last();
 #pragma unroll
             for (int i = 0; i < C::IPT; ++i) {
                 const int o = at + kAttnThreads * i;
-                if (o < items) dst[(o / DH) * (DH + 2) + o % DH] = acc[i];
+                if (o < items) st_hint(dst + (o / DH) * (DH + 2) + o % DH, acc[i], keep);
             }
             if (at < NQ) {
-                dst[at * (DH + 2) + DH] = S.am[at];
-                dst[at * (DH + 2) + DH + 1] = S.al[at];
+                st_hint(dst + at * (DH + 2) + DH, S.am[at], keep);
+                st_hint(dst + at * (DH + 2) + DH + 1, S.al[at], keep);
             }
             attn_sync();
         }
@@ -943,7 +971,7 @@ struct Attention {
             attention(op_arg(op));
             merge(op_arg(op));
             if (p.trace && at == 0) {  // the ATTN op's trace slot belongs to these warps
-                unsigned long long *tr = p.trace + ((size_t)cta * p.n_ops + oi) * 4;
+                unsigned long long *tr = p.trace + ((size_t)cta * p.n_ops + oi) * LF_TRACE_WORDS;
                 tr[0] = t_start;
                 tr[1] = global_timer_ns();
                 tr[2] = S.a_tbar;
@@ -973,16 +1001,21 @@ __device__ void produce(const KParams &p, Smem<D, DH> &S, uint8_t *stages, uint6
     const uint8_t *pf = w;  // the L2 prefetch front of this CTA's weight stream
     bool stop = false;
 
+    unsigned long long t_blocked = 0, t_first = 0;  // trace of the current op
     auto claim = [&](int &stage) -> bool {
         stage = it % C::STAGES;
         if (it >= C::STAGES) {
             const uint32_t par = ((it / C::STAGES) - 1) & 1u;
-            while (!mbar_try_wait(&S.empty[stage], par)) {
-                if (S.abort_) return false;
-                if (global_timer_ns() > deadline) {
-                    record_error(p, &S.abort_, 3u, -1);
-                    return false;
+            if (!mbar_try_wait(&S.empty[stage], par)) {
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(&S.empty[stage], par)) {
+                    if (S.abort_) return false;
+                    if (global_timer_ns() > deadline) {
+                        record_error(p, &S.abort_, 3u, -1);
+                        return false;
+                    }
                 }
+                if (p.trace) t_blocked += global_timer_ns() - t0;
             }
         }
         return !S.abort_;
@@ -1000,6 +1033,7 @@ __device__ void produce(const KParams &p, Smem<D, DH> &S, uint8_t *stages, uint6
                 bulk_prefetch_l2(pf, nb);
                 pf += nb;
             }
+            if (p.trace && t_first == 0) t_first = global_timer_ns();
             mbar_arrive_expect_tx(&S.full[stage], bytes);
             bulk_g2s(stages + (size_t)stage * kStageBytes, w, bytes, &S.full[stage], pol);
             w += bytes;
@@ -1011,11 +1045,17 @@ __device__ void produce(const KParams &p, Smem<D, DH> &S, uint8_t *stages, uint6
         const int op = __ldg(p.ops + oi);
         const int t = op_type(op), l = op_arg(op);
         const unsigned ahead = p.l2_prefetch_bytes;
+        t_blocked = t_first = 0;
         if (t == OP_QKV) rows(2 * p.lp[(size_t)cta * p.L + l].qkv_n, ahead);
         else if (t == OP_GATEUP) rows(2 * p.lp[(size_t)cta * p.L + l].ffn_n, ahead);
         else if (t == OP_DOWN) rows(p.lp[(size_t)cta * p.L + l].ffn_n, ahead);
         else if (t == OP_OPROJ) rows(p.lp[(size_t)cta * p.L + l].o_n, ahead);
         else if (t == OP_LMHEAD) rows(cp.lm_count, p.lm_prefetch_bytes);
+        if (p.trace) {
+            unsigned long long *tr = p.trace + ((size_t)cta * p.n_ops + oi) * LF_TRACE_WORDS;
+            tr[4] = t_blocked;
+            tr[5] = t_first;
+        }
     }
     S.issued = (int)it;
     __threadfence_block();
@@ -1026,8 +1066,9 @@ __device__ void produce(const KParams &p, Smem<D, DH> &S, uint8_t *stages, uint6
 // The delayed lane sum, off the streaming warps' path: for every REDUCE(u) of
 // the op list, chunk `cta` (32 floats) of R[u] = the sum over all CTAs k (in
 // order k = 0, 1, ...) of their partials of sub-block u.  The 32-float pieces
-// of all CTAs arrive by bulk copies in one round trip; each lane then sums one
-// float over the pieces, and the chunk is published with a release counter.
+// of all CTAs lie contiguous (chunk-major partials) and arrive by one bulk
+// copy; each lane then sums one float over the pieces, and the chunk is
+// published with a release counter.
 template <int D, int DH>
 __device__ void help(const KParams &p, Smem<D, DH> &S, uint64_t deadline) {
     const int lane = threadIdx.x & 31, cta = blockIdx.x;
@@ -1039,7 +1080,9 @@ __device__ void help(const KParams &p, Smem<D, DH> &S, uint64_t deadline) {
         const int op = __ldg(p.ops + oi);
         if (op_type(op) != OP_REDUCE) continue;
         const int u = op_arg(op);
+        uint64_t t_w0 = 0, t_w1 = 0, t_c = 0;
         if (lane == 0) {
+            if (p.trace) t_w0 = global_timer_ns();
             while (true) {
                 if ((int)(ld_acquire(&p.cnt[u]) - target) >= 0) break;
                 if (S.abort_ || ld_relaxed(p.err) != 0u) { ok = false; break; }
@@ -1049,6 +1092,7 @@ __device__ void help(const KParams &p, Smem<D, DH> &S, uint64_t deadline) {
                     break;
                 }
             }
+            if (p.trace) t_w1 = global_timer_ns();
             if (ok) {
                 fence_proxy_async_global();
                 fence_proxy_async_shared();
@@ -1057,9 +1101,8 @@ __device__ void help(const KParams &p, Smem<D, DH> &S, uint64_t deadline) {
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
-        const float *src = p.part + (size_t)(u % p.pslots) * p.n_cta * D + kRChunk * cta;
-        for (int k = lane; k < p.n_cta; k += 32)
-            bulk_g2s(S.hbuf[k], src + (size_t)k * D, kRChunk * 4, &S.hbar);
+        const float *src = p.part + ((size_t)(u % p.pslots) * p.n_cta * D + (size_t)cta * p.n_cta * kRChunk);
+        if (lane == 0) bulk_g2s(S.hbuf[0], src, (uint32_t)p.n_cta * kRChunk * 4, &S.hbar);
         ++issued;
         while (!mbar_try_wait(&S.hbar, nred & 1u)) {
             if (S.abort_ || global_timer_ns() > deadline) {
@@ -1071,13 +1114,24 @@ __device__ void help(const KParams &p, Smem<D, DH> &S, uint64_t deadline) {
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         ++nred;
+        if (p.trace && lane == 0) t_c = global_timer_ns();
+        // The pieces are dead now (the slot is rewritten only after ready[u]
+        // is seen): drop them from L2 so they are never written back to HBM.
+        for (int k = lane; k < p.n_cta; k += 32) discard_l2_line(src + (size_t)k * kRChunk);
         float s = 0.f;
         for (int k = 0; k < p.n_cta; ++k) s += S.hbuf[k][lane];
-        p.R[(size_t)u * D + kRChunk * cta + lane] = s;
+        st_hint(p.R + (size_t)u * D + kRChunk * cta + lane, s, policy_evict_last());
         __syncwarp();
         if (lane == 0) {
             __threadfence();
             atomicAdd(&p.ready[u], 1u);
+            if (p.trace) {  // the REDUCE op's trace slot belongs to this warp
+                unsigned long long *tr = p.trace + ((size_t)cta * p.n_ops + oi) * LF_TRACE_WORDS;
+                tr[0] = t_w0;
+                tr[1] = global_timer_ns();
+                tr[2] = t_w1 - t_w0;
+                tr[3] = t_c - t_w1;
+            }
         }
     }
     // after an error, let pieces still in flight land before the CTA exits

@@ -14,6 +14,7 @@ struct KParams {
     int L, D, DH, HQ_L, HKV_L, GL, F_L, V, NL, n_cta, ctx, n_ops, nch, qkv_l;
     int hc, kt;  // attention: KV heads per chunk, keys per tile
     int pslots;  // lane-sum partial slots
+    int tail_fused;  // 1: the last layer's two sub-blocks share one partial and one lane sum
     float eps, attn_scale;
     // this step
     int pos, token;
@@ -36,7 +37,7 @@ struct KParams {
     __half *kc, *vc;        // [lane][L][HKV_L][ctx][DH]
     float *qkv;             // [L][NL][qkv_l]
     float *apart;           // [L][n_cta][HQ_L][DH+2]: acc[DH], m, l
-    float *part;            // [pslots][n_cta][D], sub-block u in slot u % pslots
+    float *part;            // [pslots][D/32][n_cta][32], sub-block u in slot u % pslots
     float *R;               // [2L][D]
     uint32_t *barA, *barB;  // [L][NL]
     uint32_t *cnt, *ready;  // [2L]

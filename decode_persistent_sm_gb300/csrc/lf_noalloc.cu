@@ -107,6 +107,7 @@ extern "C" lf_status lf_decode_step_static_scratch(lf_engine *e, int32_t token,
     k.hc = s.HC;
     k.kt = s.KT;
     k.pslots = s.PS;
+    k.tail_fused = s.delay >= 1 ? 1 : 0;
     k.eps = e->cfg.rms_eps;
     k.attn_scale = (float)(1.0 / std::sqrt((double)s.DH));
     k.pos = e->pos;

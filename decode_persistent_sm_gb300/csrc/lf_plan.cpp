@@ -92,9 +92,14 @@ static std::vector<int> build_ops(const Shape &s) {
     const int L = s.L, d = s.delay;
     std::vector<int> ops;
     ops.push_back(make_op(OP_EMBED, 0));
+    // With a delay the final drain alone reads the last layer's two
+    // sub-blocks: they share one partial (down_proj first, o_proj onto it)
+    // and one lane sum, published as sub-block 2L - 1.
+    const int fused = d >= 1 ? 2 * L - 2 : -1;
     int next_add = 0;
     auto adds_upto = [&](int last) {
-        while (next_add <= last) ops.push_back(make_op(OP_ADD, next_add++));
+        for (; next_add <= last; ++next_add)
+            if (next_add != fused) ops.push_back(make_op(OP_ADD, next_add));
     };
     for (int l = 0; l < L; ++l) {
         const int sa = 2 * l, sf = 2 * l + 1;
@@ -114,8 +119,7 @@ static std::vector<int> build_ops(const Shape &s) {
             // With a delay of 2 or more, o_proj of layer l - 1 (whose lane sum
             // is first read at sub-block 2l + 3) waits until after the QKV rows
             // of layer l, which gives the attention warps a layer's worth of
-            // slack.  The last layer runs o_proj before down_proj, so that
-            // its lane sum is formed while down_proj streams.
+            // slack.  The last layer's o_proj closes the step.
             const bool late = (d >= 2);
             adds_upto(sa - 1 - 2 * d);
             ops.push_back(make_op(OP_NORM, l));
@@ -124,15 +128,9 @@ static std::vector<int> build_ops(const Shape &s) {
             adds_upto(sf - 1 - 2 * d);
             ops.push_back(make_op(OP_NORM, L + l));
             ops.push_back(make_op(OP_GATEUP, l));
-            if (l + 1 < L) {
-                ops.push_back(make_op(OP_DOWN, l));
-                ops.push_back(make_op(OP_ATTN, l));
-                if (!late) ops.push_back(make_op(OP_OPROJ, l));
-            } else {
-                ops.push_back(make_op(OP_ATTN, l));
-                ops.push_back(make_op(OP_OPROJ, l));
-                ops.push_back(make_op(OP_DOWN, l));
-            }
+            ops.push_back(make_op(OP_DOWN, l));
+            ops.push_back(make_op(OP_ATTN, l));
+            if (!late || l + 1 == L) ops.push_back(make_op(OP_OPROJ, l));
         }
     }
     adds_upto(2 * L - 1);
@@ -148,8 +146,13 @@ static std::vector<int> build_ops(const Shape &s) {
         if (t == OP_DOWN) prod[2 * a + 1] = i;
         if (t == OP_ADD) cons[a] = i;
     }
+    if (fused >= 0) {  // the op that completes the shared partial
+        if (prod[fused] < prod[fused + 1]) return {};
+        prod[fused + 1] = prod[fused];
+    }
     std::vector<std::vector<int>> insert_before(ops.size() + 1);
     for (int u = 0; u < 2 * L; ++u) {
+        if (u == fused) continue;
         int at = prod[u] + 1 + (cons[u] - prod[u] - 1) / 2;
         insert_before[at].push_back(make_op(OP_REDUCE, u));
     }
@@ -215,6 +218,7 @@ lf_status build_plan(const lf_config &c, int n_cta, bool with_rows, Plan *plan) 
         for (int k = 0; k < n_cta; ++k) { P.cta[k].lm_begin = b[k]; P.cta[k].lm_count = n[k]; }
     }
     P.ops = build_ops(s);
+    if (P.ops.empty()) return LF_ERR_UNSUPPORTED;  // op order the kernel cannot run
 
     // Weight stream: per CTA, the rows of its weight ops in op-list order.
     const long long D = s.D, Q = (long long)s.NQ * s.DH;

@@ -77,10 +77,33 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Drops one 128-byte line from L2 without writing it back (its contents
+// become undefined: a weak write as far as memory ordering goes).  For
+// scratch that is dead once read.
+__device__ __forceinline__ void discard_l2_line(const void *line) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     return pol;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Global stores with an L2 eviction-priority policy.
+__device__ __forceinline__ void st_hint(float4 *dst, float4 v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w), "l"(policy)
+                 : "memory");
+}
+__device__ __forceinline__ void st_hint(float *dst, float v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(dst), "f"(v), "l"(policy) : "memory");
 }
 
 // Bulk copy global -> own shared memory, completion counted on `bar` in bytes.

@@ -389,6 +389,7 @@ lf_status lf_decode_step(lf_engine *e, int32_t token, float *logits, int32_t *ar
     k.hc = s.HC;
     k.kt = s.KT;
     k.pslots = s.PS;
+    k.tail_fused = s.delay >= 1 ? 1 : 0;
     k.eps = e->cfg.rms_eps;
     k.attn_scale = (float)(1.0 / std::sqrt((double)s.DH));
     k.pos = e->pos;
@@ -551,7 +552,7 @@ lf_status lf_debug_trace(lf_engine *e, int enable) {
         return LF_OK;
     }
     if (!e->trace) {
-        const size_t n = (size_t)e->plan.n_cta * e->plan.ops.size() * 4;
+        const size_t n = (size_t)e->plan.n_cta * e->plan.ops.size() * LF_TRACE_WORDS;
         cudaError_t err = cudaMalloc(&e->trace, n * sizeof(unsigned long long));
         if (err != cudaSuccess) {
             e->trace = nullptr;
@@ -566,7 +567,7 @@ lf_status lf_debug_trace(lf_engine *e, int enable) {
 lf_status lf_debug_read_trace(lf_engine *e, uint64_t *out, size_t n_words, int32_t *ops) {
     if (!e || !out) return LF_ERR_INVALID_ARG;
     if (e->poisoned != LF_OK) return e->poisoned;
-    const size_t n = (size_t)e->plan.n_cta * e->plan.ops.size() * 4;
+    const size_t n = (size_t)e->plan.n_cta * e->plan.ops.size() * LF_TRACE_WORDS;
     if (!e->trace || n_words != n) return LF_ERR_INVALID_ARG;
     cudaError_t err = cudaStreamSynchronize(e->stream);
     if (err == cudaSuccess)

@@ -154,11 +154,20 @@ lf_status lf_set_l2_prefetch(lf_engine *e, uint32_t bytes_per_sm, uint32_t lm_by
 lf_status lf_debug_skip_arrival(lf_engine *e, int cta);
 
 /* Tracing: with enable != 0 every later step records, per CTA and per op of
- * the step's op list, [start ns, end ns, ns blocked on cross-CTA counters, ns
- * blocked on tile arrival] (global timer; allocates the buffer on first use).
+ * the step's op list, LF_TRACE_WORDS words (global timer ns; the buffer is
+ * allocated on first use):
+ *   [0] start, [1] end, [2] ns blocked on cross-CTA counters, [3] ns blocked
+ *   on tile arrival (streaming warps; attention warps for ATTN ops),
+ *   [4] ns the weight-copy warp waited for a free stage while issuing this
+ *   op's rows, [5] time of its first copy for this op (0 = op has no rows).
+ * The slot of a lane-sum op (REDUCE) holds, on the CTAs that sum a chunk
+ * (cta < d_model / 32), [wait start, publish time, ns waiting for the
+ * partials, ns copying them, 0, 0]; it stays zero on the other CTAs.
  * lf_debug_read_trace copies the last step's record: n_words must equal
- * n_sm * n_ops * 4 (lf_engine_info [0] and [6]); `ops` (nullable, n_ops
- * entries) receives the op list, each entry type | (argument << 8). */
+ * n_sm * n_ops * LF_TRACE_WORDS (lf_engine_info [0] and [6]); `ops`
+ * (nullable, n_ops entries) receives the op list, each entry
+ * type | (argument << 8). */
+#define LF_TRACE_WORDS 6
 lf_status lf_debug_trace(lf_engine *e, int enable);
 lf_status lf_debug_read_trace(lf_engine *e, uint64_t *out, size_t n_words, int32_t *ops);
 

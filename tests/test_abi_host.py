@@ -104,3 +104,9 @@ def test_unsupported_sm_count(lib):
     from decode_persistent_sm_gb300 import binding
     rc, _ = binding.plan_stats(cfg(synth.FULL), 64)  # fewer CTAs than lane-sum chunks
     assert rc == 7
+
+
+def test_trace_word_count_matches_the_header():
+    from decode_persistent_sm_gb300 import binding
+    m = re.search(r"#define\s+LF_TRACE_WORDS\s+(\d+)", open(HEADER).read())
+    assert m and int(m.group(1)) == binding.TRACE_WORDS
