@@ -9,6 +9,7 @@ delayed lane sum, LM head, argmax); the position is set back to 512 before
 every step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --workload e2e|long|sweep   # generation workloads, one line each
 
 Under torchrun (N > 1) every rank decodes its own replica on its own GPU (the
 path needs no exchange between GPUs); rank 0 prints one JSON line.
@@ -63,7 +64,7 @@ def algorithmic_bytes(shape, pos: int) -> int:
 
 def workload_config(shape):
     return {
-        "workload": "single decode step at position 512 (KV pre-filled N(0,1)), full 2.3B lane "
+        "workload": f"single decode step at position {POS} (KV pre-filled N(0,1)), full 2.3B lane "
                     "model: 15 layers, d_model 4096, 32 q / 16 KV heads x 128, FFN 7168, vocab 32000, "
                     "8 lanes, DTP delay 2, SWA 1024 on 10 layers",
         "batch": 1, "position": POS, "n_lanes": shape.n_lanes, "dtp_delay": shape.dtp_delay,
@@ -142,14 +143,15 @@ def peak_hbm():
     return 6800.0, "fallback"
 
 
-def oracle_rate(shape, blob, kv, tokens, budget_s: float, max_steps: int):
-    """Decode steps/s of the CPU oracle at position 512 on a bounded sample."""
+def oracle_rate(shape, blob, kv, tokens, budget_s: float, max_steps: int, pos: int = POS):
+    """Decode steps/s of the CPU oracle at position `pos` (cache filled with
+    `kv` up to there) on a bounded sample."""
     import oracle
     orc = oracle.Oracle(shape, blob)
-    orc.load_kv(kv, POS)
+    orc.load_kv(kv, pos)
     n, t0 = 0, time.perf_counter()
     while n < max_steps:
-        orc.set_pos(POS)
+        orc.set_pos(pos)
         orc.step(int(tokens[n % len(tokens)]))
         n += 1
         if time.perf_counter() - t0 >= budget_s:
@@ -340,7 +342,7 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = peak_hbm()
     achieved = nbytes / (ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": profile_traffic(),
+                "frac": achieved / peak, "traffic": profile_traffic() if POS == 512 else None,
                 "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                 "algorithmic_bytes_per_launch": nbytes}
 
@@ -368,7 +370,178 @@ def run_ours(args, world, rank, local):
         torch.distributed.destroy_process_group()
 
 
+# Generation workloads (not the default line): the end-to-end and long-context
+# runs and the delay x lane sweep, each timed step by step with CUDA events.
+GEN_WORKLOADS = {
+    "e2e": (128, 512, "end to end: prompt of 128 random ids (prefilled by decode steps), then 512 greedy "
+                      "tokens chained on the device (positions 128..639), full 2.3B lane model, 8 lanes, delay 2"),
+    "long": (3584, 512, "long context: prompt of 3584 random ids (prefilled by decode steps), then 512 greedy "
+                        "tokens chained on the device (positions 3584..4095), full 2.3B lane model, 8 lanes, "
+                        "delay 2"),
+}
+SWEEP_CTX, SWEEP_STEPS = 2048, 256
+
+
+def timed_generation(eng, stream, first_token: int, n: int):
+    """n chained greedy steps from the engine's position, an event between
+    every two; returns (tokens, per-step ms, total ms)."""
+    import torch
+    buf = torch.empty(n + 1, dtype=torch.int32, device="cuda")
+    buf[0] = int(first_token)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    base = buf.data_ptr()
+    torch.cuda.synchronize()
+    for i in range(n):
+        evs[i].record(stream)
+        eng.decode_step_chained(base + 4 * i, base + 4 * (i + 1))
+    evs[n].record(stream)
+    torch.cuda.synchronize()
+    eng.synchronize()
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(n)]
+    return buf[1:].cpu().numpy(), per, evs[0].elapsed_time(evs[n])
+
+
+def latency_summary(per_ms):
+    a = np.sort(np.asarray(per_ms))
+    return {"p50_ms": float(np.percentile(a, 50)), "p99_ms": float(np.percentile(a, 99)),
+            "max_ms": float(a[-1]), "mean_ms": float(a.mean())}
+
+
+def gen_roofline(shape, pos0: int, n: int, ms_per_step: float):
+    nbytes = sum(algorithmic_bytes(shape, p) for p in range(pos0, pos0 + n)) / n
+    peak, peak_kind = peak_hbm()
+    achieved = nbytes / (ms_per_step / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": None, "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+            "algorithmic_bytes_per_launch": nbytes}
+
+
+def run_generation(args, world, rank, local):
+    import torch
+    import synth
+    from decode_persistent_sm_gb300 import Engine
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def worst(x):  # max over ranks
+        if world == 1:
+            return x
+        t = torch.tensor([x], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    base = synth.FULL
+    blob = synth.make_weights(base, SEED)
+    stream = torch.cuda.current_stream()
+    data = "synthetic (seeded N(0,0.02) FP16 weights, uniform random token ids)"
+    common = {"n_gpus": world, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+              "dtype": "fp16 weights, fp32 accumulate", "unit": UNIT,
+              "parallelism": "replicas only" if world > 1 else "1 GPU, 8 lanes = SM groups"}
+
+    if args.workload == "sweep":
+        variants = {}
+        kv = synth.make_kv(base, SEED, SWEEP_CTX)
+        first = int(synth.make_tokens(SEED + rank, 1, base.vocab)[0])
+        clocks = ClockSampler(local)
+        clocks.start()
+        launches = 0
+        for delay in (0, 1, 2):
+            for lanes in (1, 8):
+                shape = base.replace(n_lanes=lanes, dtp_delay=delay)
+                with Engine.from_shape(shape) as eng:
+                    eng.set_stream(stream.cuda_stream)
+                    eng.load_weights(blob)
+                    eng.load_kv(kv, SWEEP_CTX)
+                    eng.generate(first, max(args.warmup, 3))
+                    eng.set_position(SWEEP_CTX)
+                    if world > 1:
+                        torch.distributed.barrier()
+                    _, per, total = timed_generation(eng, stream, first, SWEEP_STEPS)
+                    total = worst(total)
+                    launches += SWEEP_STEPS
+                variants[f"delay{delay}_lanes{lanes}"] = {
+                    "value": world * SWEEP_STEPS / (total / 1e3), "ms_per_step": total / SWEEP_STEPS,
+                    **latency_summary(per)}
+        clk = clocks.stop()
+        main_v = variants["delay2_lanes8"]
+        if rank == 0:
+            line = {"metric": "batch-1 greedy decode tokens/s per delay x lane variant", "value": main_v["value"],
+                    "steps": SWEEP_STEPS, "warmup": max(args.warmup, 3), "ms_per_step": main_v["ms_per_step"],
+                    "data": data + ", N(0,1) KV fill",
+                    "config": {"workload": f"sweep: KV pre-filled N(0,1) to {SWEEP_CTX}, then {SWEEP_STEPS} greedy "
+                                           "tokens chained on the device for delay in {0,1,2} x lanes in {1,8}; "
+                                           "value = delay 2, 8 lanes", "seed": SEED,
+                               "l2": "no flush: inputs larger than L2"},
+                    "variants": variants,
+                    "roofline": gen_roofline(base, SWEEP_CTX, SWEEP_STEPS, main_v["ms_per_step"]),
+                    "cpu_baseline": None, "e2e": None, "gpu_launches": launches, "clocks": clk, **common}
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    n_prompt, n_gen, desc = GEN_WORKLOADS[args.workload]
+    shape = base
+    prompt = synth.make_tokens(SEED + rank, n_prompt, shape.vocab)
+    pos0 = n_prompt - 1  # first decode position of the generation
+    eng = Engine.from_shape(shape)
+    eng.set_stream(stream.cuda_stream)
+    eng.load_weights(blob)
+    eng.generate(int(prompt[0]), max(args.warmup, 3))  # warm-up
+    eng.reset()
+    t0 = time.perf_counter()
+    eng.prefill(prompt[:-1], logits=False)
+    prefill_ms = (time.perf_counter() - t0) * 1e3
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    gen, per, total = timed_generation(eng, stream, int(prompt[-1]), n_gen)
+    clk = clocks.stop()
+    total = worst(total)
+    # end to end through lf_generate: tokens back in host memory
+    eng.reset()
+    eng.prefill(prompt[:-1], logits=False)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    gen2, _ = eng.generate(int(prompt[-1]), n_gen)
+    e2e_s = worst(time.perf_counter() - t0)
+    eng.close()
+    ms = total / n_gen
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        kv = synth.make_kv(shape, SEED, pos0)
+        rate, n, dt, cores = oracle_rate(shape, blob, kv, prompt, args.cpu_budget_s, 200, pos=pos0)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{n} decode steps at position {pos0} of the same model, cache filled with N(0,1) "
+                         f"({dt:.1f} s)"}
+    if rank == 0:
+        line = {"metric": "batch-1 greedy decode tokens/s (2.3B lane model, FP16)",
+                "value": world * n_gen / (total / 1e3), "steps": n_gen, "warmup": max(args.warmup, 3),
+                "ms_per_step": ms, "data": data,
+                "config": {"workload": desc, "prompt": n_prompt, "generated": n_gen, "seed": SEED,
+                           "l2": "no flush: inputs larger than L2 (4.4 GB streamed per step)"},
+                "latency": latency_summary(per),
+                "prefill_ms": prefill_ms, "prefill": f"{n_prompt - 1} decode steps, host-timed",
+                "chain_matches_lf_generate": bool(np.array_equal(gen, gen2)),
+                "roofline": gen_roofline(shape, pos0, n_gen, ms), "cpu_baseline": cpu,
+                "e2e": {"value": world * n_gen / e2e_s, "unit": UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 4 + 32 / n_gen,
+                        "call": "lf_generate (first token by value, tokens and status copied back once)"},
+                "gpu_launches": n_gen, "clocks": clk, **common}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
+    global POS
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
@@ -381,9 +554,15 @@ def main():
     ap.add_argument("--lm-prefetch-kb", type=int, default=-1,
                     help="LM-head L2 prefetch distance per SM (default: the engine's)")
     ap.add_argument("--trace", default="", help="write a one-step op trace (JSON) to this path")
+    ap.add_argument("--position", type=int, default=POS,
+                    help="step workload: decode position (KV pre-filled up to it); 512 is the default line")
+    ap.add_argument("--workload", choices=["step", "e2e", "long", "sweep"], default="step",
+                    help="step: the single-step microbench (default line); e2e / long / sweep: the "
+                         "generation workloads")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: same width with fewer layers (not a bench number)")
     args = ap.parse_args()
+    POS = args.position
     if args.warmup < 3:
         args.warmup = 3
     world, rank, local = dist_setup()
@@ -391,6 +570,8 @@ def main():
         if args.steps > 50:
             args.steps = 20  # each oracle step takes a fraction of a second
         run_reference(args, world, rank)
+    elif args.workload != "step":
+        run_generation(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
 

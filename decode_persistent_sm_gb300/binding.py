@@ -27,6 +27,8 @@ _SIGS = {
     "lf_load_kv": (_ci, [_vp, _vp, ctypes.c_size_t, _ci]),
     "lf_prefill": (_ci, [_vp, _vp, _ci, _vp, _vp]),
     "lf_decode_step": (_ci, [_vp, _i32, _vp, _vp]),
+    "lf_generate": (_ci, [_vp, _i32, _ci, _vp, _vp]),
+    "lf_decode_step_chained": (_ci, [_vp, _vp, _vp]),
     "lf_synchronize": (_ci, [_vp]),
     "lf_set_position": (_ci, [_vp, _ci]),
     "lf_get_position": (_ci, [_vp, ctypes.POINTER(_ci)]),
@@ -175,6 +177,22 @@ class Engine:
     def decode_step_async(self, token: int):
         """Enqueues one step; results stay on the device."""
         _check("lf_decode_step", self._lib.lf_decode_step(self._h, int(token), None, None))
+
+    def generate(self, first_token: int, n: int, logits: bool = False):
+        """Greedy generation of n steps chained on the device; returns
+        (tokens [n] int32, last step's logits or None)."""
+        toks = np.zeros(int(n), dtype=np.int32)
+        out = np.empty(self.vocab, dtype=np.float32) if logits else None
+        rc = self._lib.lf_generate(self._h, int(first_token), int(n), toks.ctypes.data,
+                                   out.ctypes.data if logits else None)
+        _check("lf_generate", rc)
+        return toks, out
+
+    def decode_step_chained(self, token_device_ptr: int, argmax_device_ptr: int):
+        """Enqueues one step whose token is read from, and whose argmax goes to,
+        device memory (raw pointers, e.g. torch tensors' data_ptr())."""
+        _check("lf_decode_step_chained",
+               self._lib.lf_decode_step_chained(self._h, token_device_ptr, argmax_device_ptr))
 
     def prefill(self, tokens: Sequence[int], logits: bool = True):
         t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))

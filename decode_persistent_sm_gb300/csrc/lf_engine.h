@@ -23,6 +23,7 @@ struct lf_engine {
     int *cand_i = nullptr, *d_ops = nullptr, *d_kvfirst = nullptr;
     uint32_t *ctr = nullptr;     // barA | barB | cnt | ready | fin
     uint32_t *status = nullptr;  // [0] argmax, [4..7] error word
+    int32_t *gen = nullptr;      // lf_generate: argmax of each step, [ctx_cap]
     lf::CtaPlan *d_cta = nullptr;
     lf::LayerPlan *d_lp = nullptr;
     size_t n_ctr = 0;

@@ -198,7 +198,15 @@ struct Streamer {
 
     // ------------------------------------------------------------- residual
     __device__ void embed() {
-        const __half *e = p.emb + (size_t)p.token * D;
+        int tok = p.token;
+        if (p.token_src) {  // written by an earlier launch on the same stream
+            tok = __ldcg(p.token_src);
+            if (tok < 0 || tok >= p.V) {
+                if (tid == 0) fail(6u);
+                tok = 0;
+            }
+        }
+        const __half *e = p.emb + (size_t)tok * D;
 #pragma unroll
         for (int i = 0; i < C::NCHT; ++i) {
             uint4 w = __ldg(reinterpret_cast<const uint4 *>(e + col(i)));

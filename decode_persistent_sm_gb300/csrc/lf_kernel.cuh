@@ -18,6 +18,7 @@ struct KParams {
     float eps, attn_scale;
     // this step
     int pos, token;
+    const int *token_src;  // non-null: the token is read here on the device (chained steps)
     uint32_t epoch;  // launches since the last reset; counters target epoch * n
     unsigned long long timeout_ns;
     int skip_arrive_cta;

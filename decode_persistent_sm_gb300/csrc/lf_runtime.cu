@@ -238,6 +238,7 @@ lf_status lf_create(const lf_config *cfg, lf_engine **out) {
     ALLOC(R, (size_t)2 * L * s.D);
     ALLOC(ctr, e->n_ctr);
     ALLOC(status, 8);
+    ALLOC(gen, s.ctx);
     ALLOC(cand_v, NC);
     ALLOC(cand_i, NC);
     ALLOC(logits, s.V);
@@ -269,6 +270,7 @@ lf_status lf_create(const lf_config *cfg, lf_engine **out) {
         err = cudaMemcpy(e->d_lp, P.lp.data(), P.lp.size() * sizeof(LayerPlan), cudaMemcpyHostToDevice);
     if (err == cudaSuccess) err = cudaMemset(e->ctr, 0, e->n_ctr * sizeof(uint32_t));
     if (err == cudaSuccess) err = cudaMemset(e->status, 0, 8 * sizeof(uint32_t));
+    if (err == cudaSuccess) err = cudaMemset(e->gen, 0, (size_t)s.ctx * sizeof(int32_t));
     if (err == cudaSuccess) err = cudaMemset(e->kc, 0, kv_elems * sizeof(__half));
     if (err == cudaSuccess) err = cudaMemset(e->vc, 0, kv_elems * sizeof(__half));
     if (err != cudaSuccess) {
@@ -366,22 +368,20 @@ static lf_status read_status(lf_engine *e, float *logits, int32_t *argmax) {
     if (err == cudaSuccess) err = cudaStreamSynchronize(e->stream);
     if (err != cudaSuccess) return cuda_fail(e, err);
     if (e->h_status[4] != 0) {
-        e->poisoned = LF_ERR_TIMEOUT;
-        return LF_ERR_TIMEOUT;
+        // code 6: a chained step read a token outside [0, vocab) on the device
+        e->poisoned = e->h_status[4] == 6u ? LF_ERR_INVALID_ARG : LF_ERR_TIMEOUT;
+        return e->poisoned;
     }
     if (argmax) *argmax = (int32_t)e->h_status[0];
     return LF_OK;
 }
 
-lf_status lf_decode_step(lf_engine *e, int32_t token, float *logits, int32_t *argmax) {
-    if (!e) return LF_ERR_INVALID_ARG;
-    if (e->poisoned != LF_OK) return e->poisoned;
-    if (!e->loaded) return LF_ERR_NOT_LOADED;
+// Enqueues one decode step at the current position (checked by the caller).
+// The input token is `token`, or *token_src read on the device when non-null;
+// the argmax goes to *argmax_dst (device).
+static lf_status enqueue_step(lf_engine *e, int32_t token, const int32_t *token_src, int32_t *argmax_dst) {
     const lf::Plan &P = e->plan;
     const lf::Shape &s = P.sh;
-    if (token < 0 || token >= s.V) return LF_ERR_INVALID_ARG;
-    if (e->pos >= s.ctx) return LF_ERR_CTX_OVERFLOW;
-
     lf::KParams k{};
     k.L = s.L; k.D = s.D; k.DH = s.DH; k.HQ_L = s.HQ_L; k.HKV_L = s.HKV_L; k.GL = s.GL;
     k.F_L = s.F_L; k.V = s.V; k.NL = s.NL; k.n_cta = P.n_cta; k.ctx = s.ctx;
@@ -394,6 +394,7 @@ lf_status lf_decode_step(lf_engine *e, int32_t token, float *logits, int32_t *ar
     k.attn_scale = (float)(1.0 / std::sqrt((double)s.DH));
     k.pos = e->pos;
     k.token = token;
+    k.token_src = token_src;
     k.epoch = e->epoch + 1;
     k.timeout_ns = e->timeout_ns;
     k.skip_arrive_cta = e->skip_cta;
@@ -410,7 +411,7 @@ lf_status lf_decode_step(lf_engine *e, int32_t token, float *logits, int32_t *ar
     k.ready = c; c += 2 * s.L;
     k.fin = c;
     k.cand_v = e->cand_v; k.cand_i = e->cand_i; k.logits = e->logits;
-    k.argmax = reinterpret_cast<int *>(e->status);
+    k.argmax = argmax_dst;
     k.err = e->status + 4;
     k.trace = e->trace;
 
@@ -420,8 +421,60 @@ lf_status lf_decode_step(lf_engine *e, int32_t token, float *logits, int32_t *ar
     e->epoch += 1;
     e->pos += 1;
     e->launches += 1;
+    return LF_OK;
+}
+
+lf_status lf_decode_step(lf_engine *e, int32_t token, float *logits, int32_t *argmax) {
+    if (!e) return LF_ERR_INVALID_ARG;
+    if (e->poisoned != LF_OK) return e->poisoned;
+    if (!e->loaded) return LF_ERR_NOT_LOADED;
+    const lf::Shape &s = e->plan.sh;
+    if (token < 0 || token >= s.V) return LF_ERR_INVALID_ARG;
+    if (e->pos >= s.ctx) return LF_ERR_CTX_OVERFLOW;
+    lf_status st = enqueue_step(e, token, nullptr, reinterpret_cast<int32_t *>(e->status));
+    if (st != LF_OK) return st;
     if (!logits && !argmax) return LF_OK;
     return read_status(e, logits, argmax);
+}
+
+// True if the kernel may read or write a 4-byte word at p (device, managed or
+// registered host memory of this engine's device).
+static bool device_word(const lf_engine *e, const void *p) {
+    if (!p || (reinterpret_cast<uintptr_t>(p) & 3u)) return false;
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    if (a.type == cudaMemoryTypeDevice) return a.device == e->device;
+    if (a.type == cudaMemoryTypeManaged || a.type == cudaMemoryTypeHost) return a.devicePointer != nullptr;
+    return false;
+}
+
+lf_status lf_decode_step_chained(lf_engine *e, const int32_t *token_device, int32_t *argmax_device) {
+    if (!e) return LF_ERR_INVALID_ARG;
+    if (e->poisoned != LF_OK) return e->poisoned;
+    if (!e->loaded) return LF_ERR_NOT_LOADED;
+    if (!device_word(e, token_device) || !device_word(e, argmax_device)) return LF_ERR_INVALID_ARG;
+    if (e->pos >= e->plan.sh.ctx) return LF_ERR_CTX_OVERFLOW;
+    return enqueue_step(e, 0, token_device, argmax_device);
+}
+
+lf_status lf_generate(lf_engine *e, int32_t first_token, int n, int32_t *tokens_out, float *logits) {
+    if (!e || n < 1 || !tokens_out) return LF_ERR_INVALID_ARG;
+    if (e->poisoned != LF_OK) return e->poisoned;
+    if (!e->loaded) return LF_ERR_NOT_LOADED;
+    const lf::Shape &s = e->plan.sh;
+    if (first_token < 0 || first_token >= s.V) return LF_ERR_INVALID_ARG;
+    if ((long long)e->pos + n > s.ctx) return LF_ERR_CTX_OVERFLOW;
+    for (int i = 0; i < n; ++i) {
+        lf_status st = enqueue_step(e, first_token, i ? e->gen + i - 1 : nullptr, e->gen + i);
+        if (st != LF_OK) return st;
+    }
+    cudaError_t err = cudaMemcpyAsync(tokens_out, e->gen, (size_t)n * sizeof(int32_t), cudaMemcpyDeviceToHost,
+                                      e->stream);
+    if (err != cudaSuccess) return cuda_fail(e, err);
+    return read_status(e, logits, nullptr);
 }
 
 lf_status lf_synchronize(lf_engine *e) {

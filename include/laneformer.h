@@ -13,9 +13,10 @@
  *  - Plain C types only; pointers are HOST pointers unless a name says
  *    "device".  The engine owns all device memory it allocates; the caller
  *    keeps ownership of every buffer it passes.
- *  - Every call returns an lf_status.  After LF_ERR_CUDA or LF_ERR_TIMEOUT the
- *    engine is poisoned: every call but lf_reset and lf_destroy returns that
- *    status again until lf_reset succeeds.
+ *  - Every call returns an lf_status.  After LF_ERR_CUDA or LF_ERR_TIMEOUT
+ *    (or a bad token found on the device by a chained step, reported as
+ *    LF_ERR_INVALID_ARG) the engine is poisoned: every call but lf_reset and
+ *    lf_destroy returns that status again until lf_reset succeeds.
  *  - Calls run on the engine stream (default: the legacy stream, or the one
  *    given to lf_set_stream) and are synchronous unless stated otherwise.
  *  - One engine per thread; there is no internal locking.
@@ -106,6 +107,29 @@ lf_status lf_prefill(lf_engine *e, const int32_t *tokens, int n, float *logits, 
  * results stay on the device (lf_get_logits_device, lf_get_argmax_device) and
  * a device-side error surfaces at the next synchronising call. */
 lf_status lf_decode_step(lf_engine *e, int32_t token, float *logits, int32_t *argmax);
+
+/* Greedy generation with no host round trip between steps: the per-request
+ * token rate at batch 1 that News (asector), "Performance and
+ * infrastructure", quotes, decoded greedily as in its "Training and data
+ * specialisation" section.  Runs n >= 1 decode steps from the current
+ * position: step 0 reads `first_token`, step i > 0 reads the argmax of step
+ * i - 1 straight from device memory.  tokens_out (host, n int32, required)
+ * receives the n argmax tokens; logits (host, vocab floats, nullable) those
+ * of the last step.  Advances the position by n.  Synchronous.
+ * LF_ERR_INVALID_ARG for n < 1, a NULL tokens_out or first_token outside
+ * [0, vocab); LF_ERR_CTX_OVERFLOW if position + n > ctx_cap (nothing run). */
+lf_status lf_generate(lf_engine *e, int32_t first_token, int n, int32_t *tokens_out, float *logits);
+
+/* One chained decode step, the building block of lf_generate: enqueued on the
+ * engine stream without waiting; its input token is read on the device from
+ * *token_device when the step starts (e.g. the previous step's argmax) and
+ * its argmax is written to *argmax_device.  Both must be 4-byte aligned words
+ * the GPU can access (device memory of the engine's device, managed or
+ * registered host memory), else LF_ERR_INVALID_ARG; they may be the same word.
+ * A token outside [0, vocab) found on the device is read as 0 and the next
+ * synchronising call returns LF_ERR_INVALID_ARG (engine poisoned until
+ * lf_reset).  LF_ERR_CTX_OVERFLOW at position == ctx_cap. */
+lf_status lf_decode_step_chained(lf_engine *e, const int32_t *token_device, int32_t *argmax_device);
 
 /* Waits for the engine stream and reports a device-side error, if any. */
 lf_status lf_synchronize(lf_engine *e);
