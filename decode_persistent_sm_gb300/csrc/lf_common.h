@@ -30,7 +30,10 @@ constexpr int kMaxORowsPerCta = 256;
 constexpr int kMaxGroup = 4;       // q heads per KV head inside one lane
 constexpr int kMaxLaneCtas = 160;  // CTAs per lane (attention merge weights)
 constexpr int kRedRows = 128;      // GEMV rows reduced per epilogue block
-constexpr int kAttnScores = 528;   // scores per attention tile (q heads x keys)
+constexpr int kAttnScores = 640;   // scores per attention tile (q heads x attn_ldk(keys))
+// Row stride of the attention score rows: room for the current key and a
+// float4 read past the last key, 16-byte aligned rows.
+LF_HD constexpr int attn_ldk(int kt) { return (kt + 7) & ~3; }
 constexpr int kMaxChunkHeads = 16; // q heads per attention chunk
 
 // Op list: every CTA walks the same list; an op's data differs per CTA.

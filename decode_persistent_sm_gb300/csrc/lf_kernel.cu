@@ -42,11 +42,15 @@ struct Cfg {
     static constexpr int RPT = kStageBytes / (2 * D);                 // weight rows per tile
     static_assert(!kBlockRow || RPT == 4, "block-row GEMV assumes 4 rows per tile");
     static_assert(kRedRows % RPT == 0, "reduction block");
-    static constexpr int TPK = DH / 16;                  // attention threads per (head, key)
-    static constexpr int PPP = kAttnThreads / TPK;       // (head, key) pairs per score pass
     static constexpr int GLMAX = 256 / DH < kMaxGroup ? 256 / DH : kMaxGroup;
-    static constexpr int IPT = kConsThreads / kAttnThreads;  // P.V outputs per attention thread
-    static_assert(DH % 16 == 0 && 32 % TPK == 0, "head_dim layout");
+    // attention q in shared memory: 8-float chunks at a stride of 12 floats,
+    // so that 8 threads reading 8 different chunks hit 8 different bank groups
+    static constexpr int QCH = DH / 8;
+    static constexpr int QST = QCH * 12;  // floats per q head
+    static_assert((QCH & (QCH - 1)) == 0, "head_dim chunks");
+    // attention: P.V by dimension pairs, at most 4 q heads per thread
+    static_assert((DH / 2 & (DH / 2 - 1)) == 0 && kAttnThreads % (DH / 2) == 0, "head_dim layout");
+    static_assert(512 / DH <= 4 * (kAttnThreads / (DH / 2)), "q heads per attention thread");
 };
 
 template <int D, int DH>
@@ -54,7 +58,7 @@ struct Smem {
     using C = Cfg<D, DH>;
     uint64_t full[C::STAGES];
     uint64_t empty[C::STAGES];
-    uint64_t abar;                    // attention KV tile arrival
+    uint64_t abarK, abarV;            // attention K / V tile arrival
     uint64_t hbar;                    // helper: partial pieces arrival
     // streaming warps
     float red[kConsWarps][kRedRows];  // GEMV row partials per warp (row sums in red[0] if warp-per-row)
@@ -66,8 +70,8 @@ struct Smem {
     float amv[kConsWarps];
     int ami[kConsWarps];
     // attention warps
-    __align__(16) float qs[kConsThreads];      // q of the current head chunk
-    float sc[kAttnScores];                     // scores / probabilities, [q head][key]
+    __align__(16) float qs[512 / DH * C::QST];  // q of the current head chunk, padded chunks
+    __align__(16) float sc[kAttnScores];       // scores / probabilities, [q head][attn_ldk(kt)]
     float am[kMaxChunkHeads], al[kMaxChunkHeads], alpha[kMaxChunkHeads];
     __align__(16) __half curk[kConsThreads];   // this step's key / value, per chunk head
     __align__(16) __half curv[kConsThreads];
@@ -79,6 +83,7 @@ struct Smem {
     volatile int cur_op;
     unsigned long long t_sync, t_tile;  // trace: blocked time in the current op (thread 0)
     unsigned long long a_tbar, a_ttile; // trace: attention warps blocked on lane barriers / tiles
+    unsigned long long a_tsc, a_tpv;    // trace: attention warps in the score / P.V phases
     volatile int oflag;                 // layers whose o_proj inputs are merged
     volatile int abort_;
     volatile int prod_done;
@@ -559,6 +564,7 @@ struct Streamer {
         if (tid == 0 && !S.abort_) {
             const uint64_t t0 = p.trace ? global_timer_ns() : 0;
             while (S.oflag < l + 1) {
+                __nanosleep(64);
                 if (S.abort_) break;
                 if (global_timer_ns() > deadline) { fail(5); break; }
             }
@@ -685,11 +691,11 @@ struct Attention {
     uint8_t *abuf;
     int at, awarp, lane, cta, cur_op;
     uint64_t deadline;
-    uint32_t ntile;   // attention tiles waited for (every attention thread keeps the count)
-    uint32_t issued;  // tiles whose copies thread 0 issued
+    uint32_t kwait, vwait;  // K / V tiles waited for (every attention thread keeps the counts)
+    uint32_t kiss, viss;    // K / V tiles whose copies thread 0 issued
 
     __device__ Attention(const KParams &p_, Smem<D, DH> &S_, uint8_t *ab, uint64_t dl)
-        : p(p_), S(S_), abuf(ab), deadline(dl), cur_op(0), ntile(0), issued(0) {
+        : p(p_), S(S_), abuf(ab), deadline(dl), cur_op(0), kwait(0), vwait(0), kiss(0), viss(0) {
         at = threadIdx.x - kConsThreads;
         awarp = at >> 5;
         lane = at & 31;
@@ -711,145 +717,226 @@ struct Attention {
         attn_sync();
     }
 
-    // Bulk-loads keys [j0, j0 + n) of the chunk's HC KV heads into the tile
-    // buffer (K of head g at g*kt keys, V likewise in the second half).  Only
-    // thread 0 issues; the buffer must be free (after the previous tile).
-    __device__ void issue_tile(int l, int lane_id, int g0, int j0, int n) {
-        const int kt = p.kt, HC = p.hc;
-        if (at == 0 && !S.abort_ && issued == ntile) {
+    // Bulk-loads keys [j0, j0 + n) of the chunk's HC KV heads: K into the
+    // first half of the tile buffer (head g at g*kt keys), V into the second.
+    // K and V have their own barriers, so the next tile's K can load while
+    // this tile's P.V runs and its V while the next scores run.  Only thread 0
+    // issues, at most one tile ahead of the waits.
+    __device__ void issue_k(int l, int lane_id, int g0, int j0, int n) {
+        if (at == 0 && !S.abort_ && kiss == kwait) {
             const uint32_t bytes = (uint32_t)n * DH * 2;
-            mbar_arrive_expect_tx(&S.abar, 2u * HC * bytes);
-            for (int g = 0; g < HC; ++g) {
+            mbar_arrive_expect_tx(&S.abarK, (uint32_t)p.hc * bytes);
+            for (int g = 0; g < p.hc; ++g) {
                 const size_t head = (((size_t)lane_id * p.L + l) * p.HKV_L + g0 + g) * p.ctx;
-                const size_t off = (size_t)g * kt * DH * 2;
-                bulk_g2s(abuf + off, p.kc + (head + j0) * DH, bytes, &S.abar);
-                bulk_g2s(abuf + kAttnBuf / 2 + off, p.vc + (head + j0) * DH, bytes, &S.abar);
+                bulk_g2s(abuf + (size_t)g * p.kt * DH * 2, p.kc + (head + j0) * DH, bytes, &S.abarK);
             }
-            ++issued;
+            ++kiss;
+        }
+    }
+    __device__ void issue_v(int l, int lane_id, int g0, int j0, int n) {
+        if (at == 0 && !S.abort_ && viss == vwait) {
+            const uint32_t bytes = (uint32_t)n * DH * 2;
+            mbar_arrive_expect_tx(&S.abarV, (uint32_t)p.hc * bytes);
+            for (int g = 0; g < p.hc; ++g) {
+                const size_t head = (((size_t)lane_id * p.L + l) * p.HKV_L + g0 + g) * p.ctx;
+                bulk_g2s(abuf + kAttnBuf / 2 + (size_t)g * p.kt * DH * 2, p.vc + (head + j0) * DH, bytes,
+                         &S.abarV);
+            }
+            ++viss;
         }
     }
 
-    // Waits for the tile issued last (tile i completes phase i of S.abar).
-    __device__ void wait_tile() {
-        attn_sync();
+    // Waits for the K (or V) tile issued last (tile i completes phase i).
+    __device__ void wait_kv(uint64_t *bar, uint32_t &count) {
         const uint64_t t0 = (p.trace && at == 0) ? global_timer_ns() : 0;
         // (in abort mode nothing may have been issued: the loop then stops at once)
-        while (!S.abort_ && !mbar_try_wait(&S.abar, ntile & 1u)) {
+        while (!S.abort_ && !mbar_try_wait(bar, count & 1u)) {
             if (global_timer_ns() > deadline) fail(2);
         }
         if (p.trace && at == 0) S.a_ttile += global_timer_ns() - t0;
-        ++ntile;
+        ++count;
     }
 
-    // Keys [0, n) from the tile buffer plus (has_cur) the current key from
-    // S.curk / S.curv at index n; all q heads of the chunk together.
-    __device__ void tile_update(int n, bool has_cur, float *acc) {
-        const int GL = p.GL, HC = p.hc, kt = p.kt, NQ = HC * GL, ldk = kt + 1;
-        const int nt = n + (has_cur ? 1 : 0);
+    // Scores of keys [0, n) of the tile plus (has_cur) the current key from
+    // S.curk at index n, for all q heads of the chunk: one (KV head, key)
+    // pair per thread over the whole head dimension, 8 dimensions per step.
+    // The chunk order is rotated by the key, so the 8 threads of a quarter
+    // warp read 8 different bank groups of K (rows 256 B apart) and of q.
+    template <int GL>
+    __device__ void scores_t(int n, bool has_cur) {
+        const int HC = p.hc, kt = p.kt, ldk = attn_ldk(kt), nt = n + (has_cur ? 1 : 0);
         const __half *kbase = reinterpret_cast<const __half *>(abuf);
-        const __half *vbase = reinterpret_cast<const __half *>(abuf + kAttnBuf / 2);
-        float *sc = S.sc;
-        {
-            const int c = at % C::TPK;
-            for (int q0 = 0; q0 < HC * nt; q0 += C::PPP) {
-                const int q = q0 + at / C::TPK;
-                float d[C::GLMAX];
+        for (int pi = at; pi < HC * nt; pi += kAttnThreads) {
+            const int g = pi / nt, j = pi - g * nt;
+            const uint4 *kr =
+                reinterpret_cast<const uint4 *>(j < n ? kbase + ((size_t)g * kt + j) * DH : S.curk + g * DH);
+            const float *qb = S.qs + (size_t)g * GL * C::QST;
+            float s0[GL], s1[GL];
 #pragma unroll
-                for (int gq = 0; gq < C::GLMAX; ++gq) d[gq] = 0.f;
-                const int g = q / max(nt, 1), j = q - g * nt;
-                if (q < HC * nt) {
-                    const __half *kp = j < n ? kbase + ((size_t)g * kt + j) * DH : S.curk + g * DH;
-                    float kf[16];
-                    h8_to_f(*reinterpret_cast<const uint4 *>(kp + 8 * c), kf);
-                    h8_to_f(*reinterpret_cast<const uint4 *>(kp + 8 * (c + C::TPK)), kf + 8);
+            for (int gq = 0; gq < GL; ++gq) s0[gq] = s1[gq] = 0.f;
+#pragma unroll 4
+            for (int cs = 0; cs < C::QCH; ++cs) {
+                const int c = (cs + j) & (C::QCH - 1);
+                float kf[8];
+                h8_to_f(kr[c], kf);
 #pragma unroll
-                    for (int gq = 0; gq < C::GLMAX; ++gq)
-                        if (gq < GL) {
-                            const float *qv = S.qs + (g * GL + gq) * DH;
-                            const float4 qa = *reinterpret_cast<const float4 *>(qv + 8 * c);
-                            const float4 qb = *reinterpret_cast<const float4 *>(qv + 8 * c + 4);
-                            const float4 qc = *reinterpret_cast<const float4 *>(qv + 8 * (c + C::TPK));
-                            const float4 qd = *reinterpret_cast<const float4 *>(qv + 8 * (c + C::TPK) + 4);
-                            const float qq[16] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w,
-                                                  qc.x, qc.y, qc.z, qc.w, qd.x, qd.y, qd.z, qd.w};
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) d[gq] = fmaf(qq[e], kf[e], d[gq]);
-                        }
-                }
-#pragma unroll
-                for (int gq = 0; gq < C::GLMAX; ++gq) {
-#pragma unroll
-                    for (int o = C::TPK / 2; o > 0; o >>= 1) d[gq] += __shfl_xor_sync(0xffffffffu, d[gq], o);
-                }
-                if (c == 0 && q < HC * nt) {
-#pragma unroll
-                    for (int gq = 0; gq < C::GLMAX; ++gq)
-                        if (gq < GL) sc[(g * GL + gq) * ldk + j] = d[gq] * p.attn_scale;
+                for (int gq = 0; gq < GL; ++gq) {
+                    const float4 qa = *reinterpret_cast<const float4 *>(qb + gq * C::QST + c * 12);
+                    const float4 qc = *reinterpret_cast<const float4 *>(qb + gq * C::QST + c * 12 + 4);
+                    s0[gq] = fmaf(qa.x, kf[0], s0[gq]);
+                    s1[gq] = fmaf(qc.x, kf[4], s1[gq]);
+                    s0[gq] = fmaf(qa.y, kf[1], s0[gq]);
+                    s1[gq] = fmaf(qc.y, kf[5], s1[gq]);
+                    s0[gq] = fmaf(qa.z, kf[2], s0[gq]);
+                    s1[gq] = fmaf(qc.z, kf[6], s1[gq]);
+                    s0[gq] = fmaf(qa.w, kf[3], s0[gq]);
+                    s1[gq] = fmaf(qc.w, kf[7], s1[gq]);
                 }
             }
+#pragma unroll
+            for (int gq = 0; gq < GL; ++gq) S.sc[(g * GL + gq) * ldk + j] = (s0[gq] + s1[gq]) * p.attn_scale;
         }
-        attn_sync();
-        // online softmax update, one warp per q head
-        for (int a = awarp; a < NQ; a += kAttnWarps) {
-            float *sa = sc + a * ldk;
-            const float mo = S.am[a];
-            float mt = -FLT_MAX;
-            for (int j = lane; j < nt; j += 32) mt = fmaxf(mt, sa[j]);
-            mt = warp_max(mt);
-            const float mn = fmaxf(mo, mt);
-            const float al = (mo == -INFINITY) ? 0.f : expf(mo - mn);
-            float sum = 0.f;
+    }
+    __device__ void scores(int n, bool has_cur) {
+        if (p.GL == 1) scores_t<1>(n, has_cur);
+        else if (p.GL == 2) scores_t<2>(n, has_cur);
+        else scores_t<4>(n, has_cur);
+    }
+
+    // Online softmax update over the tile's nt scores: each warp takes two q
+    // heads at a time (independent reductions interleaved); scores become
+    // probabilities, S.alpha the rescale of the older terms.
+    __device__ void softmax(int nt) {
+        const int NQ = p.hc * p.GL, ldk = attn_ldk(p.kt);
+        for (int a0 = awarp; a0 < NQ; a0 += 2 * kAttnWarps) {
+            const bool two = a0 + kAttnWarps < NQ;
+            const int a1 = two ? a0 + kAttnWarps : a0;  // (a lone head is reduced twice, written once)
+            float *s0 = S.sc + a0 * ldk, *s1 = S.sc + a1 * ldk;
+            const float mo0 = S.am[a0], mo1 = S.am[a1];
+            float m0 = -FLT_MAX, m1 = -FLT_MAX;
             for (int j = lane; j < nt; j += 32) {
-                const float pj = expf(sa[j] - mn);
-                sa[j] = pj;
-                sum += pj;
+                m0 = fmaxf(m0, s0[j]);
+                m1 = fmaxf(m1, s1[j]);
             }
-            sum = warp_sum(sum);
-            if (lane == 0) {
-                S.am[a] = mn;
-                S.al[a] = S.al[a] * al + sum;
-                S.alpha[a] = al;
-            }
-        }
-        attn_sync();
-        // acc = alpha * acc + sum_j p_j V_j for this thread's (q head, dim) outputs
-        const int items = NQ * DH;
 #pragma unroll
-        for (int i = 0; i < C::IPT; ++i) {
-            const int o = at + kAttnThreads * i;
-            if (o < items) {
-                const int a = o / DH, dd = o % DH, g = a / GL;
-                const float *pa = sc + a * ldk;
-                float s = acc[i] * S.alpha[a];
-                for (int j = 0; j < nt; ++j) {
-                    const __half *vp = j < n ? vbase + ((size_t)g * kt + j) * DH : S.curv + g * DH;
-                    s = fmaf(pa[j], __half2float(vp[dd]), s);
+            for (int o = 16; o > 0; o >>= 1) {
+                m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+                m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+            }
+            const float mn0 = fmaxf(mo0, m0), mn1 = fmaxf(mo1, m1);
+            float sum0 = 0.f, sum1 = 0.f;
+            for (int j = lane; j < nt; j += 32) {
+                const float p0 = expf(s0[j] - mn0), p1 = expf(s1[j] - mn1);
+                s0[j] = p0;
+                if (two) s1[j] = p1;
+                sum0 += p0;
+                sum1 += p1;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                sum0 += __shfl_xor_sync(0xffffffffu, sum0, o);
+                sum1 += __shfl_xor_sync(0xffffffffu, sum1, o);
+            }
+            if (lane == 0) {
+                const float al0 = (mo0 == -INFINITY) ? 0.f : expf(mo0 - mn0);
+                S.am[a0] = mn0;
+                S.al[a0] = S.al[a0] * al0 + sum0;
+                S.alpha[a0] = al0;
+                if (two) {
+                    const float al1 = (mo1 == -INFINITY) ? 0.f : expf(mo1 - mn1);
+                    S.am[a1] = mn1;
+                    S.al[a1] = S.al[a1] * al1 + sum1;
+                    S.alpha[a1] = al1;
                 }
-                acc[i] = s;
             }
         }
-        attn_sync();  // the tile buffer and the scores are free again
+    }
+
+    // o = alpha * o + sum_j p_j V_j.  Thread layout: dimension pair dp =
+    // at % (DH/2) of q heads grp + NG*r (r < 4), NG = threads / (DH/2); keys
+    // outer (probabilities as float4 over 4 keys), heads inner.  With one
+    // thread group (NG = 1) the GLT q heads of a KV head share its V loads.
+    template <int GLT>
+    __device__ void pv_t(int n, bool has_cur, float2 *o) {
+        constexpr int DP = DH / 2, NG = kAttnThreads / DP;
+        const int kt = p.kt, NQ = p.hc * GLT, ldk = attn_ldk(kt);
+        const int dp = at % DP, grp = at / DP;
+        const __half2 *vb = reinterpret_cast<const __half2 *>(abuf + kAttnBuf / 2);
+        int soff[4], voff[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int a = min(grp + NG * r, NQ - 1);
+            soff[r] = a * ldk;
+            voff[r] = (a / GLT) * kt * DP + dp;
+            const float al = S.alpha[a];
+            o[r].x *= al;
+            o[r].y *= al;
+        }
+#pragma unroll 2
+        for (int j0 = 0; j0 < n; j0 += 4) {
+            float4 pr[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) pr[r] = *reinterpret_cast<const float4 *>(S.sc + soff[r] + j0);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                if (j0 + jj < n) {
+                    float2 v;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        if (NG > 1 || r % GLT == 0) v = __half22float2(vb[voff[r] + (j0 + jj) * DP]);
+                        const float pj = jj == 0 ? pr[r].x : jj == 1 ? pr[r].y : jj == 2 ? pr[r].z : pr[r].w;
+                        o[r].x = fmaf(pj, v.x, o[r].x);
+                        o[r].y = fmaf(pj, v.y, o[r].y);
+                    }
+                }
+            }
+        }
+        if (has_cur) {
+            const __half2 *cv = reinterpret_cast<const __half2 *>(S.curv);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int a = min(grp + NG * r, NQ - 1);
+                const float pj = S.sc[soff[r] + n];
+                const float2 v = __half22float2(cv[(a / GLT) * DP + dp]);
+                o[r].x = fmaf(pj, v.x, o[r].x);
+                o[r].y = fmaf(pj, v.y, o[r].y);
+            }
+        }
+    }
+    __device__ void pv(int n, bool has_cur, float2 *o) {
+        if (p.GL == 1) pv_t<1>(n, has_cur, o);
+        else if (p.GL == 2) pv_t<2>(n, has_cur, o);
+        else pv_t<4>(n, has_cur, o);
     }
 
     __device__ void attention(int l) {
         const CtaPlan cp = p.cta[cta];
         const int S_ = cp.S, GL = p.GL, HC = p.hc, kt = p.kt, NQ = HC * GL, items = NQ * DH;
+        constexpr int DP = DH / 2, NG = kAttnThreads / DP;
         int a, b;
         attn_range(p.pos, p.window[l], cp.k, S_, &a, &b);
         const bool last = (cp.k == S_ - 1);
         const int n_prev = b - a, T = (n_prev + kt - 1) / kt, T_eff = (last && T == 0) ? 1 : T;
         // earlier keys do not depend on this step: fetch the first tile before
         // waiting for the lane's QKV rows
-        if (T > 0) issue_tile(l, cp.lane, 0, a, min(kt, n_prev));
+        if (T > 0) {
+            issue_k(l, cp.lane, 0, a, min(kt, n_prev));
+            issue_v(l, cp.lane, 0, a, min(kt, n_prev));
+        }
         wait_geq(&p.barA[l * p.NL + cp.lane], p.epoch * (uint32_t)S_);
         const float *qkvb = p.qkv + ((size_t)l * p.NL + cp.lane) * p.qkv_l;
         for (int g0 = 0; g0 < p.HKV_L; g0 += HC) {
+            if (g0 > 0 && T > 0) {  // the buffers are free since the previous chunk's last barrier
+                issue_k(l, cp.lane, g0, a, min(kt, n_prev));
+                issue_v(l, cp.lane, g0, a, min(kt, n_prev));
+            }
             // one round trip: q of the chunk's heads and (last CTA) this step's k, v
             if (at < NQ) {
                 S.am[at] = -INFINITY;
                 S.al[at] = 0.f;
             }
-            for (int o = at; o < items; o += kAttnThreads) S.qs[o] = __ldcg(qkvb + (size_t)g0 * GL * DH + o);
+            for (int o = at; o < items; o += kAttnThreads)
+                S.qs[(o / DH) * C::QST + (o % DH) / 8 * 12 + o % 8] = __ldcg(qkvb + (size_t)g0 * GL * DH + o);
             if (last) {
                 for (int o = at; o < HC * DH; o += kAttnThreads) {
                     S.curk[o] = __float2half_rn(__ldcg(qkvb + (size_t)(p.HQ_L + g0) * DH + o));
@@ -857,24 +944,40 @@ struct Attention {
                 }
             }
             attn_sync();
-            float acc[C::IPT];
+            float2 acc[4];
 #pragma unroll
-            for (int i = 0; i < C::IPT; ++i) acc[i] = 0.f;
+            for (int r = 0; r < 4; ++r) acc[r] = make_float2(0.f, 0.f);
             for (int t = 0; t < T_eff; ++t) {
-                const int n = t < T ? min(kt, n_prev - t * kt) : 0;
-                if (t < T) {
-                    if (!(g0 == 0 && t == 0)) issue_tile(l, cp.lane, g0, a + t * kt, n);
-                    wait_tile();
-                }
-                tile_update(n, last && t == T_eff - 1, acc);
+                const int n = t < T ? min(kt, n_prev - t * kt) : 0, nn = t + 1 < T ? min(kt, n_prev - (t + 1) * kt) : 0;
+                const bool has_cur = last && t == T_eff - 1;
+                if (t < T) wait_kv(&S.abarK, kwait);
+                const uint64_t t_sc = (p.trace && at == 0) ? global_timer_ns() : 0;
+                scores(n, has_cur);
+                attn_sync();  // scores visible; the K half of the buffer is free
+                if (p.trace && at == 0) S.a_tsc += global_timer_ns() - t_sc;
+                if (nn > 0) issue_k(l, cp.lane, g0, a + (t + 1) * kt, nn);
+                softmax(n + (has_cur ? 1 : 0));
+                attn_sync();  // probabilities and rescale factors visible
+                if (t < T) wait_kv(&S.abarV, vwait);
+                const uint64_t t_pv = (p.trace && at == 0) ? global_timer_ns() : 0;
+                pv(n, has_cur, acc);
+                attn_sync();  // the V half and the scores are free again
+                if (p.trace && at == 0) S.a_tpv += global_timer_ns() - t_pv;
+                if (nn > 0) issue_v(l, cp.lane, g0, a + (t + 1) * kt, nn);
             }
             // scratch read back within this layer: kept in L2 ahead of the weight stream
             float *dst = p.apart + (((size_t)l * p.n_cta + cta) * p.HQ_L + (size_t)g0 * GL) * (DH + 2);
             const uint64_t keep = policy_evict_last();
+            {
+                const int dp = at % DP, grp = at / DP;
 #pragma unroll
-            for (int i = 0; i < C::IPT; ++i) {
-                const int o = at + kAttnThreads * i;
-                if (o < items) st_hint(dst + (o / DH) * (DH + 2) + o % DH, acc[i], keep);
+                for (int r = 0; r < 4; ++r) {
+                    const int ah = grp + NG * r;
+                    if (ah < NQ) {
+                        st_hint(dst + ah * (DH + 2) + 2 * dp, acc[r].x, keep);
+                        st_hint(dst + ah * (DH + 2) + 2 * dp + 1, acc[r].y, keep);
+                    }
+                }
             }
             if (at < NQ) {
                 st_hint(dst + at * (DH + 2) + DH, S.am[at], keep);
@@ -975,7 +1078,7 @@ struct Attention {
             if (op_type(op) != OP_ATTN) continue;
             cur_op = oi;
             const uint64_t t_start = (p.trace && at == 0) ? global_timer_ns() : 0;
-            if (at == 0) S.a_tbar = S.a_ttile = 0;
+            if (at == 0) S.a_tbar = S.a_ttile = S.a_tsc = S.a_tpv = 0;
             attention(op_arg(op));
             merge(op_arg(op));
             if (p.trace && at == 0) {  // the ATTN op's trace slot belongs to these warps
@@ -984,14 +1087,20 @@ struct Attention {
                 tr[1] = global_timer_ns();
                 tr[2] = S.a_tbar;
                 tr[3] = S.a_ttile;
+                tr[4] = S.a_tsc;
+                tr[5] = S.a_tpv;
             }
         }
-        // after an error, let the last attention tile thread 0 issued land
+        // after an error, let the last K and V tiles thread 0 issued land
         // (tiles complete in order, so the last one's phase covers them all)
-        if (at == 0 && S.abort_ && issued > 0) {
+        if (at == 0 && S.abort_) {
             const uint64_t dl = global_timer_ns() + 1000000000ull;
-            while (!mbar_try_wait(&S.abar, (issued - 1) & 1u) && global_timer_ns() < dl) {
-            }
+            if (kiss > 0)
+                while (!mbar_try_wait(&S.abarK, (kiss - 1) & 1u) && global_timer_ns() < dl) {
+                }
+            if (viss > 0)
+                while (!mbar_try_wait(&S.abarV, (viss - 1) & 1u) && global_timer_ns() < dl) {
+                }
         }
     }
 };
@@ -1059,7 +1168,7 @@ __device__ void produce(const KParams &p, Smem<D, DH> &S, uint8_t *stages, uint6
         else if (t == OP_DOWN) rows(p.lp[(size_t)cta * p.L + l].ffn_n, ahead);
         else if (t == OP_OPROJ) rows(p.lp[(size_t)cta * p.L + l].o_n, ahead);
         else if (t == OP_LMHEAD) rows(cp.lm_count, p.lm_prefetch_bytes);
-        if (p.trace) {
+        if (p.trace && (t == OP_QKV || t == OP_GATEUP || t == OP_DOWN || t == OP_OPROJ || t == OP_LMHEAD)) {
             unsigned long long *tr = p.trace + ((size_t)cta * p.n_ops + oi) * LF_TRACE_WORDS;
             tr[4] = t_blocked;
             tr[5] = t_first;
@@ -1164,7 +1273,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             mbar_init(&S.full[i], 1);
             mbar_init(&S.empty[i], kConsWarps);
         }
-        mbar_init(&S.abar, 1);
+        mbar_init(&S.abarK, 1);
+        mbar_init(&S.abarV, 1);
         mbar_init(&S.hbar, 1);
         S.abort_ = 0;
         S.prod_done = 0;

@@ -68,7 +68,7 @@ lf_status derive_shape(const lf_config &c, Shape *sh) {
     // added R[u], which happens before sub-block u + 1 + 2d; PS = 2d + 4
     // keeps the partials few enough to stay in L2.
     s.PS = std::min(2 * s.L, 2 * s.delay + 4);
-    if (s.KT < 1 || s.HC * s.GL * (s.KT + 1) > kAttnScores) return LF_ERR_UNSUPPORTED;
+    if (s.KT < 1 || s.HC * s.GL * attn_ldk(s.KT) > kAttnScores) return LF_ERR_UNSUPPORTED;
     return LF_OK;
 }
 

@@ -183,7 +183,9 @@ lf_status lf_debug_skip_arrival(lf_engine *e, int cta);
  *   [0] start, [1] end, [2] ns blocked on cross-CTA counters, [3] ns blocked
  *   on tile arrival (streaming warps; attention warps for ATTN ops),
  *   [4] ns the weight-copy warp waited for a free stage while issuing this
- *   op's rows, [5] time of its first copy for this op (0 = op has no rows).
+ *   op's rows, [5] time of its first copy for this op (0 = op has no rows);
+ *   for an ATTN op [4] and [5] are the ns the attention warps spent in the
+ *   score and in the P.V phases.
  * The slot of a lane-sum op (REDUCE) holds, on the CTAs that sum a chunk
  * (cta < d_model / 32), [wait start, publish time, ns waiting for the
  * partials, ns copying them, 0, 0]; it stays zero on the other CTAs.
