@@ -27,6 +27,7 @@ _SIGS = {
     "lf_load_kv": (_ci, [_vp, _vp, ctypes.c_size_t, _ci]),
     "lf_prefill": (_ci, [_vp, _vp, _ci, _vp, _vp]),
     "lf_decode_step": (_ci, [_vp, _i32, _vp, _vp]),
+    "lf_matmul_f16": (_ci, [_vp, _vp, _vp, _ci, _ci, _ci, _vp]),
     "lf_generate": (_ci, [_vp, _i32, _ci, _vp, _vp]),
     "lf_decode_step_chained": (_ci, [_vp, _vp, _vp]),
     "lf_synchronize": (_ci, [_vp]),
@@ -107,6 +108,13 @@ def config_from_shape(shape, **overrides) -> LfConfig:
 def _check(call: str, code: int):
     if code != 0:
         raise LaneformerError(call, code)
+
+
+def matmul_f16(a_ptr: int, b_ptr: int, c_ptr: int, m: int, n: int, k: int, stream: Optional[int] = None):
+    """c[m][n] = a[m][k] . b[n][k]^T on the tensor cores (device pointers:
+    FP16 a, b row-major, fp32 c); waits for the stream."""
+    lib = load_library()
+    _check("lf_matmul_f16", lib.lf_matmul_f16(a_ptr, b_ptr, c_ptr, int(m), int(n), int(k), stream))
 
 
 def validate_config(cfg: LfConfig) -> int:

@@ -1,0 +1,21 @@
+// Tensor-core GEMM of the batched prefill (private to the library).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "laneformer.h"
+
+namespace lf {
+
+// C[M][N] (fp32, row stride ldc >= N) = A[M][K] * B[N][K]^T, A and B fp16
+// row-major device arrays (16-byte aligned), K a multiple of 64.  Enqueued
+// on `stream`; a device-side wait that runs out sets *err (device word) to 7.
+lf_status tc_gemm_f16(const __half *A, const __half *B, float *C, int M, int N, int K, int ldc, uint32_t *err,
+                      unsigned long long timeout_ns, cudaStream_t stream);
+
+// Dynamic shared memory the GEMM kernel uses per CTA.
+size_t tc_gemm_smem_bytes();
+
+}  // namespace lf

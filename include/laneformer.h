@@ -231,6 +231,19 @@ lf_status lf_debug_read_trace(lf_engine *e, uint64_t *out, size_t n_words, int32
 lf_status lf_decode_step_static_scratch(lf_engine *e, int32_t token, float *logits_device,
                                         int32_t *argmax_device);
 
+/* Tensor-core matrix product of the batched prefill (lf_prefill_batched),
+ * exported for tests and for callers that build their own batched passes:
+ * c[m][n] = sum_k a[m][k] * b[n][k], with a (m x k) and b (n x k) row-major
+ * FP16 DEVICE arrays (16-byte aligned) and c an m x n row-major fp32 DEVICE
+ * array, i.e. activations times a weight matrix in its [out][in] layout, the
+ * projection shape of every layer (Blog, "Designing the architecture": a
+ * standard decoder).  k must be a multiple of 64; m, n >= 1.  Runs on
+ * `cuda_stream` (NULL = legacy stream) and waits for it.  LF_ERR_INVALID_ARG
+ * for bad sizes, NULL or misaligned pointers; LF_ERR_TIMEOUT if a
+ * device-side wait ran out; LF_ERR_CUDA on a CUDA error. */
+lf_status lf_matmul_f16(const void *a_device, const void *b_device, float *c_device, int m, int n, int k,
+                        void *cuda_stream);
+
 /* Host-only plan statistics for `n_sm` SMs (no GPU needed): stats[0] = weight
  * rows in the stream, [1] = min rows per SM, [2] = max rows per SM, [3] = ops
  * per step, [4] = 1 if every weight row of every lane appears exactly once,

@@ -1,0 +1,56 @@
+"""The tensor-core GEMM of the batched prefill (lf_matmul_f16), through the
+C ABI, against the exact product of the same FP16 inputs in fp64 on the CPU.
+
+fp32 accumulation of K FP16 products: the error bound used is
+K * 2^-23 * sum_k |a_mk b_nk| (a loose form of the standard accumulation
+bound), checked element by element; ragged M and N exercise the tile edges
+(the tensor loads fill with zeros, the stores are masked)."""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+
+def run(m, n, k, seed):
+    import torch
+    from decode_persistent_sm_gb300 import matmul_f16
+    g = np.random.default_rng(seed)
+    a = g.standard_normal((m, k)).astype(np.float16)
+    b = (0.05 * g.standard_normal((n, k))).astype(np.float16)
+    ta = torch.from_numpy(a).cuda()
+    tb = torch.from_numpy(b).cuda()
+    tc = torch.full((m, n), float("nan"), dtype=torch.float32, device="cuda")
+    matmul_f16(ta.data_ptr(), tb.data_ptr(), tc.data_ptr(), m, n, k)
+    return a, b, tc.cpu().numpy()
+
+
+def check(a, b, c, rows=None):
+    rows = np.arange(a.shape[0]) if rows is None else rows
+    a64 = a[rows].astype(np.float64)
+    b64 = b.astype(np.float64)
+    ref = a64 @ b64.T
+    bound = a.shape[1] * 2.0 ** -23 * (np.abs(a64) @ np.abs(b64).T) + 1e-30
+    err = np.abs(c[rows] - ref)
+    assert np.all(np.isfinite(c[rows]))
+    assert np.all(err <= bound), f"max err/bound {np.max(err / bound):.3f}"
+
+
+@pytest.mark.parametrize("m,n,k", [(128, 256, 64), (128, 256, 4096), (200, 300, 128), (1, 16, 64),
+                                   (257, 513, 192), (64, 1024, 7168)])
+def test_matmul_matches_exact_product(m, n, k):
+    a, b, c = run(m, n, k, m * 7 + n + k)
+    check(a, b, c)
+
+
+def test_matmul_prefill_shape_sampled_rows():
+    # the QKV projection of a 3584-position prompt: 28 x 32 tiles
+    a, b, c = run(3584, 8192, 4096, 11)
+    check(a, b, c, rows=np.array([0, 1, 127, 128, 1000, 2047, 3583]))
+
+
+def test_matmul_rejects_bad_sizes():
+    import ctypes
+    from decode_persistent_sm_gb300 import load_library
+    lib = load_library()
+    assert lib.lf_matmul_f16(None, None, None, 1, 1, 64, None) == 1
+    assert lib.lf_matmul_f16(ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16), 1, 1, 65, None) == 1
