@@ -28,6 +28,7 @@ _SIGS = {
     "lf_prefill": (_ci, [_vp, _vp, _ci, _vp, _vp]),
     "lf_decode_step": (_ci, [_vp, _i32, _vp, _vp]),
     "lf_matmul_f16": (_ci, [_vp, _vp, _vp, _ci, _ci, _ci, _vp]),
+    "lf_prefill_batched": (_ci, [_vp, _vp, _ci, _vp, _vp]),
     "lf_generate": (_ci, [_vp, _i32, _ci, _vp, _vp]),
     "lf_decode_step_chained": (_ci, [_vp, _vp, _vp]),
     "lf_synchronize": (_ci, [_vp]),
@@ -209,6 +210,17 @@ class Engine:
         rc = self._lib.lf_prefill(self._h, t.ctypes.data, t.size,
                                   out.ctypes.data if logits else None, ctypes.byref(am))
         _check("lf_prefill", rc)
+        return out, am.value
+
+    def prefill_batched(self, tokens: Sequence[int], logits: bool = True):
+        """lf_prefill_batched: the prompt in one batched pass (tensor-core
+        GEMMs); returns (last logits or None, last argmax)."""
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        am = ctypes.c_int32(-1)
+        out = np.empty(self.vocab, dtype=np.float32) if logits else None
+        rc = self._lib.lf_prefill_batched(self._h, t.ctypes.data, t.size,
+                                          out.ctypes.data if logits else None, ctypes.byref(am))
+        _check("lf_prefill_batched", rc)
         return out, am.value
 
     def synchronize(self):

@@ -24,6 +24,10 @@ struct lf_engine {
     uint32_t *ctr = nullptr;     // barA | barB | cnt | ready | fin
     uint32_t *status = nullptr;  // [0] argmax, [4..7] error word
     int32_t *gen = nullptr;      // lf_generate: argmax of each step, [ctx_cap]
+    __half *blob = nullptr;      // FP16 weights in file layout: GEMM operands of lf_prefill_batched
+    void *pf_mem = nullptr;      // lf_prefill_batched scratch (grow-only, owned separately)
+    size_t pf_bytes = 0;
+    uint32_t *pf_err = nullptr;  // device word: GEMM wait timeouts during a batched prefill
     lf::CtaPlan *d_cta = nullptr;
     lf::LayerPlan *d_lp = nullptr;
     size_t n_ctr = 0;

@@ -1,14 +1,154 @@
 // Batched prefill: the whole prompt in one pass per sub-block, GEMMs on the
 // tensor cores (lf_tc_gemm.cu), and the C-ABI entry points that expose it.
+//
+// With the delayed lane sum every lane's copy of the residual is the same
+// vector, so the prompt's forward needs no lanes: sub-block s reads
+// x(s) = e + sum_{u <= s-1-2d} P[u], where P[u] is the full projection output
+// of sub-block u (the lanes' partials summed).  Each sub-block runs over all
+// n positions at once: RMSNorm to FP16, one tensor-core GEMM against the
+// weight matrix in its file layout, then RoPE + KV-cache append (attention)
+// or SwiGLU (FFN), causal windowed attention over the cache, and a second
+// GEMM whose output is P[s]; P[s] joins the residual 2d + 1 sub-blocks later.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cfloat>
+#include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "laneformer.h"
+#include "lf_engine.h"
 #include "lf_tc_gemm.h"
 
 namespace {
+
+// ------------------------------------------------------------ small kernels
+// x[i][:] = E[tok[i]][:] (fp32)
+__global__ void pf_embed(const __half *__restrict__ emb, const int *__restrict__ tok, float *__restrict__ x,
+                         int D) {
+    const size_t row = blockIdx.x;
+    const __half *e = emb + (size_t)tok[row] * D;
+    for (int c = threadIdx.x; c < D; c += blockDim.x) x[row * D + c] = __half2float(e[c]);
+}
+
+// x[i] += p[i] over n floats
+__global__ void pf_add(float *__restrict__ x, const float *__restrict__ p, size_t n) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        x[i] += p[i];
+}
+
+__device__ float block_sum(float v, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[w] = v;
+    __syncthreads();
+    float t = 0.f;
+    for (int i = 0; i < nw; ++i) t += red[i];
+    return t;
+}
+
+// h[i] = FP16(g * x[i] / sqrt(mean(x[i]^2) + eps)), one block per row
+__global__ void pf_rmsnorm(const float *__restrict__ x, const __half *__restrict__ g, __half *__restrict__ h,
+                           int D, float eps) {
+    __shared__ float red[32];
+    const float *xr = x + (size_t)blockIdx.x * D;
+    float ss = 0.f;
+    for (int c = threadIdx.x; c < D; c += blockDim.x) ss += xr[c] * xr[c];
+    const float inv = rsqrtf(block_sum(ss, red) / D + eps);
+    for (int c = threadIdx.x; c < D; c += blockDim.x)
+        h[(size_t)blockIdx.x * D + c] = __float2half_rn(__half2float(g[c]) * xr[c] * inv);
+}
+
+// RoPE on q and k (pairs c, c + dh/2; table rope[p][c] = (cos, sin)), q kept
+// in fp32, k and v rounded to FP16 into the cache of every lane that reads
+// that KV head.  One block per position.
+__global__ void pf_rope_kv(const float *__restrict__ qkv, const float2 *__restrict__ rope, float *__restrict__ q,
+                           __half *__restrict__ kc, __half *__restrict__ vc, const int *__restrict__ kv_first,
+                           int p0, int NQ, int NKV, int DH, int NL, int L, int l, int HKV_L, int ctx) {
+    const int i = blockIdx.x, p = p0 + i, half = DH / 2;
+    const float *row = qkv + (size_t)i * (NQ + 2 * NKV) * DH;
+    const float2 *cs = rope + (size_t)p * half;
+    for (int t = threadIdx.x; t < NQ * half; t += blockDim.x) {
+        const int hq = t / half, c = t % half;
+        const float a = row[hq * DH + c], b = row[hq * DH + c + half];
+        const float2 r = cs[c];
+        q[(size_t)i * NQ * DH + hq * DH + c] = a * r.x - b * r.y;
+        q[(size_t)i * NQ * DH + hq * DH + c + half] = a * r.y + b * r.x;
+    }
+    for (int t = threadIdx.x; t < NL * HKV_L * half; t += blockDim.x) {
+        const int lg = t / half, c = t % half, lam = lg / HKV_L, g = lg % HKV_L;
+        const int kh = kv_first[lam] + g;
+        const float a = row[(NQ + kh) * DH + c], b = row[(NQ + kh) * DH + c + half];
+        const float2 r = cs[c];
+        const size_t at = ((((size_t)lam * L + l) * HKV_L + g) * ctx + p) * DH;
+        kc[at + c] = __float2half_rn(a * r.x - b * r.y);
+        kc[at + c + half] = __float2half_rn(a * r.y + b * r.x);
+        vc[at + c] = __float2half_rn(row[(NQ + NKV + kh) * DH + c]);
+        vc[at + c + half] = __float2half_rn(row[(NQ + NKV + kh) * DH + c + half]);
+    }
+}
+
+// u = FP16(silu(gate) * up); gu rows are [gate (F) | up (F)]
+__global__ void pf_swiglu(const float *__restrict__ gu, __half *__restrict__ u, int F, size_t n) {
+    for (size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x; t < n; t += (size_t)gridDim.x * blockDim.x) {
+        const size_t i = t / F, f = t % F;
+        const float a = gu[i * 2 * F + f], b = gu[i * 2 * F + F + f];
+        u[t] = __float2half_rn(a / (1.f + expf(-a)) * b);
+    }
+}
+
+// logits[v] = W_lm[v] . (g_f * x / rms(x)) for the last position's residual x;
+// every block normalises x itself, then one warp per vocabulary row.
+__global__ void pf_lmhead(const float *__restrict__ x, const __half *__restrict__ gf, const __half *__restrict__ w,
+                          float *__restrict__ logits, int D, int V, float eps) {
+    extern __shared__ float hs[];
+    __shared__ float red[32];
+    float ss = 0.f;
+    for (int c = threadIdx.x; c < D; c += blockDim.x) ss += x[c] * x[c];
+    const float inv = rsqrtf(block_sum(ss, red) / D + eps);
+    for (int c = threadIdx.x; c < D; c += blockDim.x) hs[c] = __half2float(gf[c]) * x[c] * inv;
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int v = blockIdx.x * nw + warp; v < V; v += gridDim.x * nw) {
+        const __half2 *wr = reinterpret_cast<const __half2 *>(w + (size_t)v * D);
+        float acc = 0.f;
+        for (int c = lane; c < D / 2; c += 32) {
+            const float2 wf = __half22float2(wr[c]);
+            acc = fmaf(wf.x, hs[2 * c], fmaf(wf.y, hs[2 * c + 1], acc));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) logits[v] = acc;
+    }
+}
+
+// argmax over logits (lowest index among equal maxima), one block
+__global__ void pf_argmax(const float *__restrict__ logits, int V, int *__restrict__ out) {
+    __shared__ float bv[32];
+    __shared__ int bi[32];
+    float best = -INFINITY;
+    int idx = 0x7fffffff;
+    for (int v = threadIdx.x; v < V; v += blockDim.x)
+        if (logits[v] > best) { best = logits[v]; idx = v; }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+        if (ov > best || (ov == best && oi < idx)) { best = ov; idx = oi; }
+    }
+    if ((threadIdx.x & 31) == 0) { bv[threadIdx.x >> 5] = best; bi[threadIdx.x >> 5] = idx; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        best = bv[0];
+        idx = bi[0];
+        for (int w = 1; w < (int)(blockDim.x >> 5); ++w)
+            if (bv[w] > best || (bv[w] == best && bi[w] < idx)) { best = bv[w]; idx = bi[w]; }
+        *out = idx;
+    }
+}
 
 constexpr unsigned long long kGemmTimeoutNs = 2000000000ull;
 
@@ -40,4 +180,294 @@ extern "C" lf_status lf_matmul_f16(const void *a_device, const void *b_device, f
         cudaStreamSynchronize(s) != cudaSuccess)
         return LF_ERR_CUDA;
     return h ? LF_ERR_TIMEOUT : LF_OK;
+}
+
+namespace {
+
+__device__ __forceinline__ void pf_h8(uint4 w, float *f) {
+    const __half2 *h = reinterpret_cast<const __half2 *>(&w);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 t = __half22float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+constexpr int PF_QB = 64, PF_KB = 64, PF_QW = 16;  // queries per block, keys per tile, queries per warp
+
+template <int DH>
+constexpr size_t pf_attn_smem() {
+    return (size_t)PF_QB * DH * 4 + 2 * (size_t)PF_KB * (DH + 8) * 2 + (size_t)4 * PF_QW * PF_KB * 4;
+}
+
+// Causal attention with a per-layer window over the KV cache, for the n new
+// positions p0 .. p0 + n - 1 (keys j of query p: p - W < j <= p, or all
+// j <= p when W = 0).  Block = 64 queries of one q head, 4 warps of 16
+// queries; keys in tiles of 64 (K and V from the lane's FP16 cache, rows
+// padded to dh + 8 halves so that 8 lanes reading 8 rows hit 8 bank groups).
+// Lane t scores keys t and t + 32 of the tile for its warp's 16 queries,
+// keeps an online softmax per query, and owns dh/32 output dimensions.
+template <int DH>
+__global__ void __launch_bounds__(128) pf_attention(const float *__restrict__ q, const __half *__restrict__ kc,
+                                                    const __half *__restrict__ vc, __half *__restrict__ o, int M,
+                                                    int p0, int NQ, int HQ_L, int GL, int HKV_L, int L, int l,
+                                                    int ctx, int window, float scale) {
+    constexpr int KS = DH + 8, DPL = DH / 32, NCH = DH / 8;
+    extern __shared__ __align__(16) uint8_t pf_smem[];
+    float *qs = reinterpret_cast<float *>(pf_smem);          // [QB][DH], pre-scaled
+    __half *ks = reinterpret_cast<__half *>(qs + PF_QB * DH);  // [KB][KS]
+    __half *vs = ks + PF_KB * KS;                              // [KB][KS]
+    float *ps = reinterpret_cast<float *>(vs + PF_KB * KS);    // [4 warps][QW][KB] probabilities
+    const int h = blockIdx.y, i0 = blockIdx.x * PF_QB;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int lam = h / HQ_L, g = (h % HQ_L) / GL;
+    const size_t kvbase = (((size_t)lam * L + l) * HKV_L + g) * ctx * DH;
+    for (int t = threadIdx.x; t < PF_QB * DH; t += blockDim.x) {
+        const int r = t / DH, c = t % DH;
+        qs[t] = (i0 + r < M) ? q[(size_t)(i0 + r) * NQ * DH + (size_t)h * DH + c] * scale : 0.f;
+    }
+    const int p_hi = p0 + min(i0 + PF_QB, M) - 1;
+    const int p_lo = window > 0 ? max(0, p0 + i0 - window + 1) : 0;
+    float m[PF_QW], lsum[PF_QW], acc[PF_QW][DPL];
+#pragma unroll
+    for (int r = 0; r < PF_QW; ++r) {
+        m[r] = -INFINITY;
+        lsum[r] = 0.f;
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) acc[r][d] = 0.f;
+    }
+    float *pw = ps + warp * PF_QW * PF_KB;
+    for (int k0 = p_lo; k0 <= p_hi; k0 += PF_KB) {
+        __syncthreads();  // the previous tile is consumed (and qs written, first time)
+        for (int t = threadIdx.x; t < PF_KB * NCH; t += blockDim.x) {
+            const int r = t / NCH, c = t % NCH, j = k0 + r;
+            uint4 kv = make_uint4(0, 0, 0, 0), vv = kv;
+            if (j <= p_hi) {
+                kv = *reinterpret_cast<const uint4 *>(kc + kvbase + (size_t)j * DH + 8 * c);
+                vv = *reinterpret_cast<const uint4 *>(vc + kvbase + (size_t)j * DH + 8 * c);
+            }
+            *reinterpret_cast<uint4 *>(ks + r * KS + 8 * c) = kv;
+            *reinterpret_cast<uint4 *>(vs + r * KS + 8 * c) = vv;
+        }
+        __syncthreads();
+        float s1[PF_QW], s2[PF_QW];
+#pragma unroll
+        for (int r = 0; r < PF_QW; ++r) s1[r] = s2[r] = 0.f;
+#pragma unroll 2
+        for (int c = 0; c < NCH; ++c) {
+            float ka[8], kb[8];
+            pf_h8(*reinterpret_cast<const uint4 *>(ks + lane * KS + 8 * c), ka);
+            pf_h8(*reinterpret_cast<const uint4 *>(ks + (lane + 32) * KS + 8 * c), kb);
+#pragma unroll
+            for (int r = 0; r < PF_QW; ++r) {
+                const float *qr = qs + (warp * PF_QW + r) * DH + 8 * c;
+                const float4 qa = *reinterpret_cast<const float4 *>(qr);
+                const float4 qb = *reinterpret_cast<const float4 *>(qr + 4);
+                const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    s1[r] = fmaf(qv[e], ka[e], s1[r]);
+                    s2[r] = fmaf(qv[e], kb[e], s2[r]);
+                }
+            }
+        }
+        const int j1 = k0 + lane, j2 = k0 + lane + 32;
+#pragma unroll
+        for (int r = 0; r < PF_QW; ++r) {
+            const int pos = p0 + i0 + warp * PF_QW + r;
+            const int lo = window > 0 ? pos - window + 1 : 0;
+            const float v1 = (j1 <= pos && j1 >= lo && j1 <= p_hi) ? s1[r] : -INFINITY;
+            const float v2 = (j2 <= pos && j2 >= lo && j2 <= p_hi) ? s2[r] : -INFINITY;
+            float mt = fmaxf(v1, v2);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+            float e1 = 0.f, e2 = 0.f;
+            if (mt != -INFINITY) {  // warp-uniform
+                const float mn = fmaxf(m[r], mt);
+                const float al = (m[r] == -INFINITY) ? 0.f : expf(m[r] - mn);
+                e1 = (v1 == -INFINITY) ? 0.f : expf(v1 - mn);
+                e2 = (v2 == -INFINITY) ? 0.f : expf(v2 - mn);
+                float sum = e1 + e2;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+                lsum[r] = lsum[r] * al + sum;
+                m[r] = mn;
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) acc[r][d] *= al;
+            }
+            pw[r * PF_KB + lane] = e1;
+            pw[r * PF_KB + lane + 32] = e2;
+        }
+        __syncwarp();
+        for (int j = 0; j < PF_KB; j += 4) {
+            float vf[4][DPL];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const __half *vr = vs + (j + jj) * KS + lane * DPL;
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) vf[jj][d] = __half2float(vr[d]);
+            }
+#pragma unroll
+            for (int r = 0; r < PF_QW; ++r) {
+                const float4 pr = *reinterpret_cast<const float4 *>(pw + r * PF_KB + j);
+#pragma unroll
+                for (int d = 0; d < DPL; ++d)
+                    acc[r][d] = fmaf(pr.x, vf[0][d], fmaf(pr.y, vf[1][d], fmaf(pr.z, vf[2][d], fmaf(pr.w, vf[3][d], acc[r][d]))));
+            }
+        }
+        __syncwarp();
+    }
+#pragma unroll
+    for (int r = 0; r < PF_QW; ++r) {
+        const int row = i0 + warp * PF_QW + r;
+        if (row < M) {
+#pragma unroll
+            for (int d = 0; d < DPL; ++d)
+                o[(size_t)row * NQ * DH + (size_t)h * DH + lane * DPL + d] = __float2half_rn(acc[r][d] / lsum[r]);
+        }
+    }
+}
+
+
+size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+// Scratch of one batched prefill of M positions, carved from one allocation.
+struct PfBufs {
+    int *tok;
+    float *x, *ring, *qkv, *qf, *gu;
+    __half *h, *o, *u;
+    size_t bytes;
+};
+
+PfBufs carve(uint8_t *base, const lf::Shape &s, int M) {
+    const size_t D = s.D, QD = (size_t)s.NQ * s.DH, QKVN = (size_t)(s.NQ + 2 * s.NKV) * s.DH, F = s.F;
+    const size_t R = 2 * (size_t)s.delay + 1;
+    PfBufs b{};
+    size_t at = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t *p = base ? base + at : nullptr;
+        at += align256(bytes);
+        return p;
+    };
+    b.tok = reinterpret_cast<int *>(take(M * sizeof(int)));
+    b.x = reinterpret_cast<float *>(take(M * D * 4));
+    b.ring = reinterpret_cast<float *>(take(R * M * D * 4));
+    b.qkv = reinterpret_cast<float *>(take(M * QKVN * 4));
+    b.qf = reinterpret_cast<float *>(take(M * QD * 4));
+    b.gu = reinterpret_cast<float *>(take(M * 2 * F * 4));
+    b.h = reinterpret_cast<__half *>(take(M * std::max(D, F) * 2));
+    b.o = reinterpret_cast<__half *>(take(M * QD * 2));
+    b.u = reinterpret_cast<__half *>(take(M * F * 2));
+    b.bytes = at;
+    return b;
+}
+
+lf_status pf_fail(lf_engine *e) {
+    e->poisoned = LF_ERR_CUDA;
+    return LF_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" lf_status lf_prefill_batched(lf_engine *e, const int32_t *tokens, int n, float *logits, int32_t *argmax) {
+    if (!e || n < 1 || !tokens) return LF_ERR_INVALID_ARG;
+    if (e->poisoned != LF_OK) return e->poisoned;
+    if (!e->loaded) return LF_ERR_NOT_LOADED;
+    const lf::Shape &s = e->plan.sh;
+    if ((long long)e->pos + n > s.ctx) return LF_ERR_CTX_OVERFLOW;
+    for (int i = 0; i < n; ++i)
+        if (tokens[i] < 0 || tokens[i] >= s.V) return LF_ERR_INVALID_ARG;
+    if (!e->blob) return LF_ERR_OOM;
+    const int D = s.D, DH = s.DH, NQ = s.NQ, NKV = s.NKV, F = s.F, L = s.L, QD = NQ * DH;
+    const int QKVN = (NQ + 2 * NKV) * DH, R = 2 * s.delay + 1, M = n, p0 = e->pos;
+    if (D % 64 || QD % 64 || F % 64 || (DH != 128 && DH != 32)) return LF_ERR_UNSUPPORTED;
+    cudaStream_t st = e->stream;
+
+    const PfBufs need = carve(nullptr, s, M);
+    if (need.bytes > e->pf_bytes) {
+        if (e->pf_mem) cudaFree(e->pf_mem);
+        e->pf_mem = nullptr;
+        e->pf_bytes = 0;
+        if (cudaMalloc(&e->pf_mem, need.bytes) != cudaSuccess) {
+            (void)cudaGetLastError();
+            e->pf_mem = nullptr;
+            return LF_ERR_OOM;
+        }
+        e->pf_bytes = need.bytes;
+    }
+    const PfBufs b = carve(static_cast<uint8_t *>(e->pf_mem), s, M);
+
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(pf_attention<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)pf_attn_smem<128>());
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(pf_attention<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)pf_attn_smem<32>());
+    });
+    if (attr_err != cudaSuccess) return pf_fail(e);
+
+    if (cudaMemcpyAsync(b.tok, tokens, (size_t)M * sizeof(int), cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemsetAsync(e->pf_err, 0, sizeof(uint32_t), st) != cudaSuccess)
+        return pf_fail(e);
+    pf_embed<<<M, 256, 0, st>>>(e->emb, b.tok, b.x, D);
+
+    const float scale = (float)(1.0 / std::sqrt((double)DH)), eps = e->cfg.rms_eps;
+    const size_t MD = (size_t)M * D;
+    const int add_blocks = (int)std::min<size_t>((MD + 255) / 256, 4096);
+    for (int sb = 0; sb < 2 * L; ++sb) {
+        const int l = sb / 2, ua = sb - 1 - 2 * s.delay;
+        if (ua >= 0) pf_add<<<add_blocks, 256, 0, st>>>(b.x, b.ring + (size_t)(ua % R) * MD, MD);
+        const __half *lw = e->blob + s.off_layer0 + (long long)l * s.per_layer;
+        float *P = b.ring + (size_t)(sb % R) * MD;
+        lf_status gs;
+        if (sb % 2 == 0) {
+            pf_rmsnorm<<<M, 256, 0, st>>>(b.x, e->gains + (size_t)l * D, b.h, D, eps);
+            gs = lf::tc_gemm_f16(b.h, lw + s.o_wq, b.qkv, M, QKVN, D, QKVN, e->pf_err, kGemmTimeoutNs, st);
+            if (gs != LF_OK) return gs == LF_ERR_CUDA ? pf_fail(e) : gs;
+            pf_rope_kv<<<M, 256, 0, st>>>(b.qkv, e->rope, b.qf, e->kc, e->vc, e->d_kvfirst, p0, NQ, NKV, DH, s.NL,
+                                          L, l, s.HKV_L, s.ctx);
+            const dim3 ag((M + PF_QB - 1) / PF_QB, NQ);
+            if (DH == 128)
+                pf_attention<128><<<ag, 128, pf_attn_smem<128>(), st>>>(b.qf, e->kc, e->vc, b.o, M, p0, NQ, s.HQ_L,
+                                                                         s.GL, s.HKV_L, L, l, s.ctx,
+                                                                         e->cfg.swa_window[l], scale);
+            else
+                pf_attention<32><<<ag, 128, pf_attn_smem<32>(), st>>>(b.qf, e->kc, e->vc, b.o, M, p0, NQ, s.HQ_L,
+                                                                       s.GL, s.HKV_L, L, l, s.ctx,
+                                                                       e->cfg.swa_window[l], scale);
+            gs = lf::tc_gemm_f16(b.o, lw + s.o_wo, P, M, D, QD, D, e->pf_err, kGemmTimeoutNs, st);
+        } else {
+            pf_rmsnorm<<<M, 256, 0, st>>>(b.x, e->gains + (size_t)(L + l) * D, b.h, D, eps);
+            gs = lf::tc_gemm_f16(b.h, lw + s.o_wg, b.gu, M, 2 * F, D, 2 * F, e->pf_err, kGemmTimeoutNs, st);
+            if (gs != LF_OK) return gs == LF_ERR_CUDA ? pf_fail(e) : gs;
+            const size_t nf = (size_t)M * F;
+            pf_swiglu<<<(int)std::min<size_t>((nf + 255) / 256, 4096), 256, 0, st>>>(b.gu, b.u, F, nf);
+            gs = lf::tc_gemm_f16(b.u, lw + s.o_wd, P, M, D, F, D, e->pf_err, kGemmTimeoutNs, st);
+        }
+        if (gs != LF_OK) return gs == LF_ERR_CUDA ? pf_fail(e) : gs;
+    }
+    // drain for the last position: the partials not yet in its residual
+    float *xl = b.x + (size_t)(M - 1) * D;
+    for (int u = std::max(0, 2 * L - 1 - 2 * s.delay); u < 2 * L; ++u)
+        pf_add<<<(D + 255) / 256, 256, 0, st>>>(xl, b.ring + (size_t)(u % R) * MD + (size_t)(M - 1) * D, D);
+    pf_lmhead<<<608, 256, D * sizeof(float), st>>>(xl, e->gains + (size_t)2 * L * D, e->blob + s.off_lm, e->logits,
+                                                   D, s.V, eps);
+    pf_argmax<<<1, 1024, 0, st>>>(e->logits, s.V, reinterpret_cast<int *>(e->status));
+    if (cudaGetLastError() != cudaSuccess) return pf_fail(e);
+    e->pos += n;
+    uint32_t gerr = 0;
+    cudaError_t err = cudaMemcpyAsync(&gerr, e->pf_err, sizeof(gerr), cudaMemcpyDeviceToHost, st);
+    if (err == cudaSuccess && logits)
+        err = cudaMemcpyAsync(logits, e->logits, (size_t)s.V * sizeof(float), cudaMemcpyDeviceToHost, st);
+    if (err == cudaSuccess && argmax) err = cudaMemcpyAsync(argmax, e->status, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(st);
+    if (err != cudaSuccess) return pf_fail(e);
+    if (gerr) {
+        e->poisoned = LF_ERR_TIMEOUT;
+        return LF_ERR_TIMEOUT;
+    }
+    return LF_OK;
 }

@@ -187,6 +187,7 @@ void lf_destroy(lf_engine *e) {
     if (!e) return;
     for (void *p : e->allocs) cudaFree(p);
     if (e->trace) cudaFree(e->trace);
+    if (e->pf_mem) cudaFree(e->pf_mem);
     if (e->h_status) cudaFreeHost(e->h_status);
     delete e;
 }
@@ -239,6 +240,7 @@ lf_status lf_create(const lf_config *cfg, lf_engine **out) {
     ALLOC(ctr, e->n_ctr);
     ALLOC(status, 8);
     ALLOC(gen, s.ctx);
+    ALLOC(pf_err, 1);
     ALLOC(cand_v, NC);
     ALLOC(cand_i, NC);
     ALLOC(logits, s.V);
@@ -314,6 +316,14 @@ lf_status lf_load_weights(lf_engine *e, const void *host_blob, size_t nbytes) {
     if (err == cudaSuccess)
         err = cudaMemcpy(e->emb, staging + s.off_E, (size_t)s.V * D * sizeof(__half),
                          cudaMemcpyDeviceToDevice);
+    // the file layout stays resident for the batched prefill's GEMMs (skipped
+    // when the device has no room: lf_prefill_batched then reports OOM)
+    if (err == cudaSuccess && !e->blob && dalloc(e, &e->blob, (size_t)s.n_params) != cudaSuccess) {
+        (void)cudaGetLastError();
+        e->blob = nullptr;
+    }
+    if (err == cudaSuccess && e->blob)
+        err = cudaMemcpy(e->blob, staging, (size_t)s.n_params * sizeof(__half), cudaMemcpyDeviceToDevice);
     for (int l = 0; l < s.L && err == cudaSuccess; ++l) {
         const long long lb = s.off_layer0 + l * s.per_layer;
         err = cudaMemcpy(e->gains + (size_t)l * D, staging + lb + s.o_gattn, D * sizeof(__half),

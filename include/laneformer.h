@@ -231,6 +231,27 @@ lf_status lf_debug_read_trace(lf_engine *e, uint64_t *out, size_t n_words, int32
 lf_status lf_decode_step_static_scratch(lf_engine *e, int32_t token, float *logits_device,
                                         int32_t *argmax_device);
 
+/* Prefill of n tokens from the current position in one batched pass: the
+ * same function as lf_prefill (each position's logits depend only on the
+ * positions before it, Blog, "Designing the architecture": causal GQA with
+ * sliding windows; the lane sums delayed as in "Hiding overhead"), computed
+ * sub-block by sub-block over all n positions at once, with the projections
+ * as tensor-core GEMMs (lf_matmul_f16) against the FP16 weights in file
+ * layout, which the engine keeps on the device from lf_load_weights on.
+ * Because every lane's residual copy is the same vector under the delayed
+ * sum, sub-block s of every position reads e + the projection outputs of
+ * sub-blocks u <= s - 1 - 2d.  Appends all n positions to the KV cache,
+ * advances the position by n; logits (host, vocab floats, nullable) and
+ * argmax (host, nullable) receive the last position's result, which also
+ * stays on the device (lf_get_logits_device / lf_get_argmax_device).
+ * Scratch is allocated on first use and kept (about 0.25 MB per position
+ * at full shape, delay 2).  Synchronous.  LF_ERR_INVALID_ARG for n < 1, a
+ * NULL tokens array or a token outside [0, vocab); LF_ERR_CTX_OVERFLOW if
+ * position + n > ctx_cap; LF_ERR_OOM when the resident weights or the
+ * scratch could not be allocated; LF_ERR_TIMEOUT if a GEMM's device-side
+ * wait ran out (engine poisoned). */
+lf_status lf_prefill_batched(lf_engine *e, const int32_t *tokens, int n, float *logits, int32_t *argmax);
+
 /* Tensor-core matrix product of the batched prefill (lf_prefill_batched),
  * exported for tests and for callers that build their own batched passes:
  * c[m][n] = sum_k a[m][k] * b[n][k], with a (m x k) and b (n x k) row-major

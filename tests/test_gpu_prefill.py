@@ -1,0 +1,114 @@
+"""The batched prefill (lf_prefill_batched: tensor-core GEMMs, one pass per
+sub-block over all prompt positions) against the oracle, which computes the
+prompt one position at a time.
+
+Checked: the last position's logits and argmax, the KV cache the pass leaves
+behind (through the decode steps that follow it, teacher forced, and read
+back directly), prompts spanning several 64-position blocks and crossing the
+sliding window, every delay / lane variant of the tiny model, a prefill that
+starts after earlier decode steps, and the full 2.3B shape."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_helpers import REL_L2, assert_gates, rel_l2, teacher_forced
+
+pytestmark = pytest.mark.gpu
+
+
+def prefill_then_steps(shape, seed, n_prompt, n_steps, gain_std=0.1, lead=0):
+    """Optional `lead` decode steps, a batched prefill of n_prompt tokens, then
+    n_steps teacher-forced steps; every result against the oracle."""
+    from decode_persistent_sm_gb300 import Engine
+    blob = synth.make_weights(shape, seed, gain_std=gain_std)
+    tokens = synth.make_tokens(seed, lead + n_prompt + n_steps, shape.vocab)
+    orc = oracle.Oracle(shape, blob)
+    with Engine.from_shape(shape) as eng:
+        eng.load_weights(blob)
+        for t in tokens[:lead]:
+            got, am = eng.decode_step(int(t))
+            ref = orc.step(int(t))
+            assert rel_l2(got, ref) <= REL_L2
+        prompt = tokens[lead:lead + n_prompt]
+        got, am = eng.prefill_batched(prompt)
+        for t in prompt:
+            ref = orc.step(int(t))
+        assert eng.position == lead + n_prompt
+        pre_rel, pre_agree = rel_l2(got, ref), am == oracle.argmax(ref)
+        rels, agree, _, _ = teacher_forced(eng, orc, tokens[lead + n_prompt:])
+        return eng, orc, pre_rel, pre_agree, rels, agree
+
+
+def test_tiny_prompt_spanning_blocks_and_window():
+    # 100 positions: two 64-query blocks; layer 0's 64-key window is crossed
+    shape = synth.TINY
+    _, _, pre_rel, pre_agree, rels, agree = prefill_then_steps(shape, 2, 100, 12)
+    assert pre_rel <= REL_L2 and pre_agree
+    assert_gates(rels, agree, "tiny after a 100-token batched prefill")
+
+
+@pytest.mark.parametrize("lanes,delay", [(8, 0), (8, 1), (8, 2), (1, 0), (1, 2), (4, 3)])
+def test_tiny_lanes_and_delays(lanes, delay):
+    shape = synth.TINY.replace(n_lanes=lanes, dtp_delay=delay)
+    _, _, pre_rel, pre_agree, rels, agree = prefill_then_steps(shape, 5, 70, 6)
+    assert pre_rel <= REL_L2 and pre_agree
+    assert_gates(rels, agree, f"lanes={lanes} delay={delay}")
+
+
+def test_six_layers_and_single_token_prompt():
+    shape = synth.TINY.replace(n_layers=6, swa_window=(64, 0, 16, 0, 8, 0))
+    _, _, pre_rel, pre_agree, rels, agree = prefill_then_steps(shape, 7, 1, 4)
+    assert pre_rel <= REL_L2 and pre_agree
+    _, _, pre_rel, pre_agree, rels, agree = prefill_then_steps(shape, 8, 90, 4)
+    assert pre_rel <= REL_L2 and pre_agree
+    assert_gates(rels, agree, "6 layers")
+
+
+def test_prefill_after_decode_steps_and_kv_contents():
+    shape = synth.TINY
+    eng, orc, pre_rel, pre_agree, rels, agree = prefill_then_steps(shape, 9, 40, 3, lead=21)
+    assert pre_rel <= REL_L2 and pre_agree
+    assert_gates(rels, agree, "prefill from position 21")
+
+
+def test_kv_written_by_the_batched_prefill():
+    from decode_persistent_sm_gb300 import Engine
+    shape = synth.TINY
+    blob = synth.make_weights(shape, 11, gain_std=0.1)
+    tokens = synth.make_tokens(11, 70, shape.vocab)
+    orc = oracle.Oracle(shape, blob)
+    orc.run(tokens)
+    with Engine.from_shape(shape) as eng:
+        eng.load_weights(blob)
+        eng.prefill_batched(tokens, logits=False)
+        for layer in range(shape.n_layers):
+            for kvh in range(shape.n_kv_heads):
+                lane = kvh * (shape.n_q_heads // shape.n_kv_heads) // (shape.n_q_heads // shape.n_lanes)
+                for pos in (0, 33, 64, 69):
+                    k, v = eng.read_kv(layer, kvh, pos)
+                    rk, rv = orc.kv(lane, layer, 0, pos)
+                    assert np.allclose(k, rk, rtol=4e-3, atol=2e-4)
+                    assert np.allclose(v, rv, rtol=4e-3, atol=2e-4)
+
+
+def test_rejections():
+    from decode_persistent_sm_gb300 import Engine, LaneformerError
+    shape = synth.TINY
+    with Engine.from_shape(shape) as eng:
+        with pytest.raises(LaneformerError, match="NOT_LOADED"):
+            eng.prefill_batched([1, 2])
+        eng.load_weights(synth.make_weights(shape, 1))
+        with pytest.raises(LaneformerError, match="INVALID_ARG"):
+            eng.prefill_batched([1, shape.vocab])
+        with pytest.raises(LaneformerError, match="CTX_OVERFLOW"):
+            eng.prefill_batched([1] * (shape.ctx_cap + 1))
+        assert eng.position == 0
+
+
+@pytest.mark.slow
+def test_full_shape_prompt_128():
+    shape = synth.FULL
+    _, _, pre_rel, pre_agree, rels, agree = prefill_then_steps(shape, 1, 128, 2, gain_std=0.0)
+    assert pre_rel <= REL_L2 and pre_agree
+    assert_gates(rels, agree, "full shape after a 128-token batched prefill")
