@@ -136,6 +136,33 @@ def profile_traffic():
         return None
 
 
+def peak_tensor(sustained: bool):
+    """Measured dense bf16 tensor throughput (FP16 has the same nominal rate)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["bf16_tflops_sustained" if sustained else "bf16_tflops"]), "measured"
+    return (1700.0 if sustained else 1900.0), "fallback"
+
+
+def prefill_flops(shape, n: int, p0: int = 0):
+    """Algorithmic FLOPs of a batched prefill of n positions from p0: the
+    projections (2 per weight per position) plus attention (QK and PV, 2 per
+    key per head dimension each) over each position's visible keys; the LM
+    head of the last position."""
+    d, dh = shape.d_model, shape.head_dim
+    qkvn = (shape.n_q_heads + 2 * shape.n_kv_heads) * dh
+    per_tok = 2 * (qkvn * d + d * shape.n_q_heads * dh + 2 * shape.ffn_dim * d + d * shape.ffn_dim)
+    gemm = per_tok * n * shape.n_layers
+    attn = 0
+    for w in shape.swa_window:
+        keys = 0
+        for p in range(p0, p0 + n):
+            keys += p + 1 if w == 0 else min(p + 1, w)
+        attn += 4 * shape.n_q_heads * dh * keys
+    return gemm, attn, 2 * shape.vocab * d
+
+
 def peak_hbm():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -380,6 +407,7 @@ GEN_WORKLOADS = {
                         "delay 2"),
 }
 SWEEP_CTX, SWEEP_STEPS = 2048, 256
+PREFILL_N = 3584
 
 
 def timed_generation(eng, stream, first_token: int, n: int):
@@ -443,6 +471,69 @@ def run_generation(args, world, rank, local):
               "dtype": "fp16 weights, fp32 accumulate", "unit": UNIT,
               "parallelism": "replicas only" if world > 1 else "1 GPU, 8 lanes = SM groups"}
 
+    if args.workload == "prefill":
+        shape = base
+        prompt = synth.make_tokens(SEED + rank, PREFILL_N, shape.vocab)
+        with Engine.from_shape(shape) as eng:
+            eng.set_stream(stream.cuda_stream)
+            eng.load_weights(blob)
+            for _ in range(max(args.warmup, 3)):
+                eng.reset()
+                eng.prefill_batched(prompt, logits=False)
+            clocks = ClockSampler(local)
+            clocks.start()
+            times = []
+            reps = max(1, min(args.steps, 10))
+            for _ in range(reps):
+                eng.reset()
+                torch.cuda.synchronize()
+                if world > 1:
+                    torch.distributed.barrier()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                eng.prefill_batched(prompt, logits=False)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                times.append(worst(e0.elapsed_time(e1)))
+            clk = clocks.stop()
+            eng.reset()
+            t0 = time.perf_counter()
+            _, am = eng.prefill_batched(prompt, logits=True)
+            e2e_s = worst(time.perf_counter() - t0)
+        ms = float(np.median(times))
+        gemm, attn, lm = prefill_flops(shape, PREFILL_N)
+        peak, kind = peak_tensor(sustained=False)
+        achieved = (gemm + attn + lm) / (ms / 1e3) / 1e12
+        cpu = None
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            kv = synth.make_kv(shape, SEED, 512)
+            rate, n_o, dt, cores = oracle_rate(shape, blob, kv, prompt, args.cpu_budget_s, 200)
+            cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                   "sample": f"{n_o} positions of the prompt computed one by one at position 512 ({dt:.1f} s)"}
+        if rank == 0:
+            line = {"metric": "batched prefill tokens/s (prompt of 3584 ids, 2.3B lane model, FP16)",
+                    "value": world * PREFILL_N / (ms / 1e3), "steps": reps, "warmup": max(args.warmup, 3),
+                    "ms_per_step": ms, "ttft_ms": ms, "data": data,
+                    "config": {"workload": "prefill of a 3584-id prompt from an empty cache (batched: one pass "
+                                           "per sub-block, tensor-core GEMMs), full 2.3B lane model, 8 lanes, "
+                                           "delay 2", "prompt": PREFILL_N, "seed": SEED,
+                               "l2": "no flush: 4.4 GB of weights per pass vs 129 MB L2"},
+                    "flops": {"gemm": gemm, "attention": attn, "lm_head": lm},
+                    "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                                 "frac": achieved / peak, "traffic": None,
+                                 "peak_source": f"{kind} dense bf16 burst (MEASURED_PEAKS.json bf16_tflops); "
+                                                "FP16 has the same nominal rate"},
+                    "cpu_baseline": cpu,
+                    "e2e": {"value": world * PREFILL_N / e2e_s, "unit": "tokens/s",
+                            "h2d_bytes_per_step": PREFILL_N * 4, "d2h_bytes_per_step": shape.vocab * 4 + 4,
+                            "call": "lf_prefill_batched with host token ids and host logits"},
+                    "gpu_launches": None, "clocks": clk, **common}
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
     if args.workload == "sweep":
         variants = {}
         kv = synth.make_kv(base, SEED, SWEEP_CTX)
@@ -496,6 +587,10 @@ def run_generation(args, world, rank, local):
     eng.reset()
     t0 = time.perf_counter()
     eng.prefill(prompt[:-1], logits=False)
+    loop_prefill_ms = (time.perf_counter() - t0) * 1e3
+    eng.reset()
+    t0 = time.perf_counter()
+    eng.prefill_batched(prompt[:-1], logits=False)
     prefill_ms = (time.perf_counter() - t0) * 1e3
     clocks = ClockSampler(local)
     clocks.start()
@@ -506,7 +601,7 @@ def run_generation(args, world, rank, local):
     total = worst(total)
     # end to end through lf_generate: tokens back in host memory
     eng.reset()
-    eng.prefill(prompt[:-1], logits=False)
+    eng.prefill_batched(prompt[:-1], logits=False)
     if world > 1:
         torch.distributed.barrier()
     t0 = time.perf_counter()
@@ -528,7 +623,8 @@ def run_generation(args, world, rank, local):
                 "config": {"workload": desc, "prompt": n_prompt, "generated": n_gen, "seed": SEED,
                            "l2": "no flush: inputs larger than L2 (4.4 GB streamed per step)"},
                 "latency": latency_summary(per),
-                "prefill_ms": prefill_ms, "prefill": f"{n_prompt - 1} decode steps, host-timed",
+                "prefill_ms": prefill_ms, "prefill": f"{n_prompt - 1} positions, lf_prefill_batched, host-timed",
+                "prefill_ms_decode_loop": loop_prefill_ms,
                 "chain_matches_lf_generate": bool(np.array_equal(gen, gen2)),
                 "roofline": gen_roofline(shape, pos0, n_gen, ms), "cpu_baseline": cpu,
                 "e2e": {"value": world * n_gen / e2e_s, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -556,7 +652,7 @@ def main():
     ap.add_argument("--trace", default="", help="write a one-step op trace (JSON) to this path")
     ap.add_argument("--position", type=int, default=POS,
                     help="step workload: decode position (KV pre-filled up to it); 512 is the default line")
-    ap.add_argument("--workload", choices=["step", "e2e", "long", "sweep"], default="step",
+    ap.add_argument("--workload", choices=["step", "e2e", "long", "sweep", "prefill"], default="step",
                     help="step: the single-step microbench (default line); e2e / long / sweep: the "
                          "generation workloads")
     ap.add_argument("--layers", type=int, default=0,
