@@ -76,6 +76,9 @@ def lib():
         L.orc_argmax.argtypes = [vp, ci]
         L.orc_rope.argtypes = [vp, ci, ci, cd]
         L.orc_threads.restype = ci
+        L.orc_philox4x32_10.argtypes = [vp, vp, vp]
+        L.orc_sample.restype = ci
+        L.orc_sample.argtypes = [vp, ci, cd, cd, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32, vp, vp]
         _lib = L
     return _lib
 
@@ -179,3 +182,24 @@ def rope(x: np.ndarray, pos: int, theta: float) -> np.ndarray:
 
 def threads() -> int:
     return lib().orc_threads()
+
+
+def philox(ctr: Sequence[int], key: Sequence[int]) -> tuple:
+    """Philox4x32-10 of a 4-word counter and 2-word key (four 32-bit words)."""
+    c = np.array(ctr, dtype=np.uint32)
+    k = np.array(key, dtype=np.uint32)
+    out = np.zeros(4, dtype=np.uint32)
+    lib().orc_philox4x32_10(c.ctypes.data, k.ctypes.data, out.ctypes.data)
+    return tuple(int(v) for v in out)
+
+
+def sample(logits: np.ndarray, temperature: float, top_p: float, seed: int, position: int, sample: int):
+    """(token, u, tau): temperature + nucleus sampling with the Philox draw of
+    (seed, position, sample); tau is the kept-set threshold relative to the
+    largest probability."""
+    x = np.ascontiguousarray(logits, dtype=np.float64)
+    u = ctypes.c_double(0.0)
+    tau = ctypes.c_double(0.0)
+    tok = lib().orc_sample(x.ctypes.data, x.size, float(temperature), float(top_p), int(seed) & (2 ** 64 - 1),
+                           int(position), int(sample), ctypes.byref(u), ctypes.byref(tau))
+    return tok, u.value, tau.value

@@ -39,6 +39,7 @@
  */
 #include "oracle.h"
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -400,4 +401,83 @@ extern "C" int orc_step(orc_state *s, int token, double *logits) {
     gemv(s, s->wlm, D, 0, 0, c.vocab, D, h.data(), logits);
     s->pos = p + 1;
     return 0;
+}
+
+/* ------------------------------------------------------------- sampling */
+
+/* Philox4x32-10 as defined in the SC 2011 paper: per round, with multipliers
+ * M0 = 0xD2511F53 and M1 = 0xCD9E8D57, (hi0, lo0) = M0 * c0 and
+ * (hi1, lo1) = M1 * c2 as 64-bit products; the new counter is
+ * (hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0); between rounds the key grows by
+ * the Weyl constants (0x9E3779B9, 0xBB67AE85). */
+extern "C" void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        const uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+        const uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+        const uint32_t n0 = hi1 ^ c1 ^ k0, n1 = lo1, n2 = hi0 ^ c3 ^ k1, n3 = lo0;
+        c0 = n0;
+        c1 = n1;
+        c2 = n2;
+        c3 = n3;
+    }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+extern "C" int orc_sample(const double *logits, int n, double temperature, double top_p, uint64_t seed,
+                          uint32_t position, uint32_t sample, double *u_out, double *tau_out) {
+    if (n < 1) return -1;
+    if (temperature <= 0.0) return orc_argmax(logits, n);
+    double m = logits[0];
+    for (int i = 1; i < n; ++i) m = logits[i] > m ? logits[i] : m;
+    std::vector<double> p(n);
+    double z = 0.0;
+    for (int i = 0; i < n; ++i) {
+        p[i] = std::exp((logits[i] - m) / temperature);
+        z += p[i];
+    }
+    /* nucleus threshold: walk the probabilities from the largest down until
+       the running mass reaches top_p of the total; every token tied with the
+       value reached is kept as well */
+    std::vector<double> sorted(p);
+    std::sort(sorted.begin(), sorted.end(), [](double a, double b) { return a > b; });
+    const double target = top_p * z;
+    double run = 0.0, tau = sorted[n - 1];
+    for (int k = 0; k < n; ++k) {
+        run += sorted[k];
+        if (run >= target) {
+            tau = sorted[k];
+            break;
+        }
+    }
+    double kept = 0.0;
+    for (int i = 0; i < n; ++i)
+        if (p[i] >= tau) kept += p[i];
+    const uint32_t ctr[4] = {position, sample, 0u, 0u};
+    const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t x[4];
+    orc_philox4x32_10(ctr, key, x);
+    const double u = (double)(x[0] >> 8) / 16777216.0;
+    if (u_out) *u_out = u;
+    if (tau_out) *tau_out = tau;
+    const double t = u * kept;
+    double acc = 0.0;
+    int last = 0;
+    for (int i = 0; i < n; ++i) {
+        if (p[i] < tau) continue;
+        acc += p[i];
+        last = i;
+        if (acc > t) return i;
+    }
+    return last;
 }

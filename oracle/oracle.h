@@ -58,6 +58,26 @@ int orc_argmax(const double *x, int n);
 void orc_rope(double *x, int head_dim, int pos, double theta);
 int orc_threads(void);
 
+/* Philox4x32-10 counter-based generator (Salmon, Moraes, Dror and Shaw,
+ * "Parallel random numbers: as easy as 1, 2, 3", SC 2011): ten rounds of the
+ * Philox S-box on a 4-word counter with a 2-word key bumped by the Weyl
+ * constants between rounds. */
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
+
+/* One sampled token from `n` logits (stochastic decoding for pass@N, News
+ * (asector), "Performance and infrastructure"; the pages fix no method, the
+ * reading is temperature + nucleus sampling): p_i = exp((z_i - max z) / T);
+ * the kept set is every token whose p_i is at least the threshold tau, the
+ * largest p value for which the tokens at or above it hold at least top_p of
+ * the total mass (ties at the threshold are all kept); u = (x0 >> 8) / 2^24
+ * with x0 the first Philox word for key (seed low, seed high) and counter
+ * (position, sample, 0, 0); the token is the first kept index, in index
+ * order, whose running kept mass exceeds u times the kept mass.  T == 0 is
+ * greedy (lowest index among equal maxima).  *u_out (nullable) gets u,
+ * *tau_out (nullable) the threshold relative to the largest p. */
+int orc_sample(const double *logits, int n, double temperature, double top_p, uint64_t seed, uint32_t position,
+               uint32_t sample, double *u_out, double *tau_out);
+
 #ifdef __cplusplus
 }
 #endif
