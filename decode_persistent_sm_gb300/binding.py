@@ -30,6 +30,10 @@ _SIGS = {
     "lf_matmul_f16": (_ci, [_vp, _vp, _vp, _ci, _ci, _ci, _vp]),
     "lf_prefill_batched": (_ci, [_vp, _vp, _ci, _vp, _vp]),
     "lf_generate": (_ci, [_vp, _i32, _ci, _vp, _vp]),
+    "lf_generate_sampled": (_ci, [_vp, _i32, _ci, ctypes.c_float, ctypes.c_float, ctypes.c_uint64, ctypes.c_uint32,
+                                  _vp, _vp]),
+    "lf_sample": (_ci, [_vp, _ci, ctypes.c_float, ctypes.c_float, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
+                        _vp, _vp]),
     "lf_decode_step_chained": (_ci, [_vp, _vp, _vp]),
     "lf_synchronize": (_ci, [_vp]),
     "lf_set_position": (_ci, [_vp, _ci]),
@@ -118,6 +122,14 @@ def matmul_f16(a_ptr: int, b_ptr: int, c_ptr: int, m: int, n: int, k: int, strea
     _check("lf_matmul_f16", lib.lf_matmul_f16(a_ptr, b_ptr, c_ptr, int(m), int(n), int(k), stream))
 
 
+def sample_token(logits_ptr: int, vocab: int, temperature: float, top_p: float, seed: int, position: int,
+                 sample: int, token_ptr: int, stream: Optional[int] = None):
+    """lf_sample: enqueue one draw from device logits into a device int32."""
+    lib = load_library()
+    _check("lf_sample", lib.lf_sample(logits_ptr, int(vocab), float(temperature), float(top_p),
+                                      int(seed) & (2 ** 64 - 1), int(position), int(sample), token_ptr, stream))
+
+
 def validate_config(cfg: LfConfig) -> int:
     return load_library().lf_validate_config(ctypes.byref(cfg))
 
@@ -195,6 +207,18 @@ class Engine:
         rc = self._lib.lf_generate(self._h, int(first_token), int(n), toks.ctypes.data,
                                    out.ctypes.data if logits else None)
         _check("lf_generate", rc)
+        return toks, out
+
+    def generate_sampled(self, first_token: int, n: int, temperature: float, top_p: float, seed: int,
+                         sample: int = 0, logits: bool = False):
+        """lf_generate_sampled: n steps, each token drawn from the step's logits
+        (temperature + nucleus, Philox stream (seed, position, sample))."""
+        toks = np.zeros(int(n), dtype=np.int32)
+        out = np.empty(self.vocab, dtype=np.float32) if logits else None
+        rc = self._lib.lf_generate_sampled(self._h, int(first_token), int(n), float(temperature), float(top_p),
+                                           int(seed) & (2 ** 64 - 1), int(sample), toks.ctypes.data,
+                                           out.ctypes.data if logits else None)
+        _check("lf_generate_sampled", rc)
         return toks, out
 
     def decode_step_chained(self, token_device_ptr: int, argmax_device_ptr: int):

@@ -12,6 +12,7 @@
 
 #include "laneformer.h"
 #include "lf_engine.h"
+#include "lf_sample.h"
 #include "lf_kernel.cuh"
 #include "lf_plan.h"
 
@@ -468,6 +469,29 @@ lf_status lf_decode_step_chained(lf_engine *e, const int32_t *token_device, int3
     if (!device_word(e, token_device) || !device_word(e, argmax_device)) return LF_ERR_INVALID_ARG;
     if (e->pos >= e->plan.sh.ctx) return LF_ERR_CTX_OVERFLOW;
     return enqueue_step(e, 0, token_device, argmax_device);
+}
+
+lf_status lf_generate_sampled(lf_engine *e, int32_t first_token, int n, float temperature, float top_p,
+                              uint64_t seed, uint32_t sample, int32_t *tokens_out, float *logits) {
+    if (!e || n < 1 || !tokens_out || !(temperature >= 0.f) || !(top_p > 0.f && top_p <= 1.f))
+        return LF_ERR_INVALID_ARG;
+    if (e->poisoned != LF_OK) return e->poisoned;
+    if (!e->loaded) return LF_ERR_NOT_LOADED;
+    const lf::Shape &s = e->plan.sh;
+    if (first_token < 0 || first_token >= s.V) return LF_ERR_INVALID_ARG;
+    if ((long long)e->pos + n > s.ctx) return LF_ERR_CTX_OVERFLOW;
+    if (lf::sample_smem_bytes(s.V) > lf::kSampleMaxSmem) return LF_ERR_UNSUPPORTED;
+    for (int i = 0; i < n; ++i) {
+        const uint32_t position = (uint32_t)e->pos;
+        lf_status st = enqueue_step(e, first_token, i ? e->gen + i - 1 : nullptr, e->gen + i);
+        if (st == LF_OK)
+            st = lf::launch_sample(e->logits, s.V, temperature, top_p, seed, position, sample, e->gen + i, e->stream);
+        if (st != LF_OK) return st == LF_ERR_CUDA ? cuda_fail(e, cudaErrorLaunchFailure) : st;
+    }
+    cudaError_t err = cudaMemcpyAsync(tokens_out, e->gen, (size_t)n * sizeof(int32_t), cudaMemcpyDeviceToHost,
+                                      e->stream);
+    if (err != cudaSuccess) return cuda_fail(e, err);
+    return read_status(e, logits, nullptr);
 }
 
 lf_status lf_generate(lf_engine *e, int32_t first_token, int n, int32_t *tokens_out, float *logits) {

@@ -1,0 +1,195 @@
+// Stochastic decoding for pass@N: one token drawn from the logits with a
+// temperature and a nucleus (top-p) cut, the draw from Philox4x32-10
+// (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as easy as 1, 2,
+// 3", SC 2011) keyed by the seed, with counter (position, sample, 0, 0).
+//
+// Definition: p_i = exp((z_i - max z) / T); the kept set is every token with
+// p_i >= tau, tau the largest p value such that the tokens at or above it
+// hold at least top_p of the total mass (ties at tau all kept);
+// u = (x0 >> 8) / 2^24 from the first Philox word; the token is the first
+// kept index, in index order, whose running kept mass exceeds u times the
+// kept mass.  T == 0 is greedy (lowest index among equal maxima).
+//
+// One CTA of 1024 threads: the probabilities live in shared memory; tau is
+// found by bisection on the fp32 bit pattern (the mass above a threshold only
+// changes at the p values, and positive floats order like their bits); the
+// crossing is found with a block scan over contiguous index chunks.
+#include <cuda_runtime.h>
+
+#include <cfloat>
+#include <climits>
+#include <mutex>
+
+#include "lf_sample.h"
+
+namespace lf {
+namespace {
+
+constexpr int SMP_THREADS = 1024;
+
+__device__ __forceinline__ void philox4x32_10(uint32_t c[4], uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t lo0 = 0xD2511F53u * c[0], hi0 = __umulhi(0xD2511F53u, c[0]);
+        const uint32_t lo1 = 0xCD9E8D57u * c[2], hi1 = __umulhi(0xCD9E8D57u, c[2]);
+        const uint32_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
+        c[0] = n0;
+        c[1] = lo1;
+        c[2] = n2;
+        c[3] = lo0;
+    }
+}
+
+// Block-wide reductions; every thread gets the result.
+__device__ float bsum(float v, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float t = 0.f;
+#pragma unroll 1
+    for (int w = 0; w < SMP_THREADS / 32; ++w) t += red[w];
+    return t;
+}
+__device__ float bmax(float v, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float t = -INFINITY;
+#pragma unroll 1
+    for (int w = 0; w < SMP_THREADS / 32; ++w) t = fmaxf(t, red[w]);
+    return t;
+}
+
+__global__ void __launch_bounds__(SMP_THREADS, 1)
+    sample_kernel(const float *__restrict__ logits, int V, float temperature, float top_p, uint32_t key0,
+                  uint32_t key1, uint32_t position, uint32_t sample, int *__restrict__ out) {
+    extern __shared__ float pv[];  // [V] unnormalised probabilities
+    __shared__ float red[SMP_THREADS / 32];
+    __shared__ float wsum[SMP_THREADS / 32];
+    __shared__ int tok;
+    __shared__ float u_sh;
+    const int tid = threadIdx.x;
+    if (tid == 0) tok = INT_MAX;
+
+    if (temperature <= 0.f) {  // greedy
+        float best = -INFINITY;
+        int idx = INT_MAX;
+        for (int i = tid; i < V; i += SMP_THREADS)
+            if (logits[i] > best) { best = logits[i]; idx = i; }
+        const float m = bmax(best, red);
+        if (best == m && idx != INT_MAX) atomicMin(&tok, idx);
+        __syncthreads();
+        if (tid == 0) *out = tok == INT_MAX ? 0 : tok;
+        return;
+    }
+
+    float m = -INFINITY;
+    for (int i = tid; i < V; i += SMP_THREADS) m = fmaxf(m, logits[i]);
+    m = bmax(m, red);
+    const float inv_t = 1.f / temperature;
+    float z = 0.f;
+    for (int i = tid; i < V; i += SMP_THREADS) {
+        const float p = expf((logits[i] - m) * inv_t);
+        pv[i] = p;
+        z += p;
+    }
+    const float total = bsum(z, red);
+    const float target = top_p * total;
+    // largest bit pattern b with mass(b) >= target; mass(0) = total >= target
+    uint32_t lo = 0, hi = __float_as_uint(1.0f);
+    float kept = total;
+    while (lo < hi) {
+        const uint32_t mid = lo + (hi - lo + 1) / 2;
+        float s = 0.f;
+        for (int i = tid; i < V; i += SMP_THREADS)
+            if (__float_as_uint(pv[i]) >= mid) s += pv[i];
+        const float mass = bsum(s, red);
+        if (mass >= target) {
+            lo = mid;
+            kept = mass;
+        } else {
+            hi = mid - 1;
+        }
+    }
+    if (tid == 0) {
+        uint32_t c[4] = {position, sample, 0u, 0u};
+        philox4x32_10(c, key0, key1);
+        u_sh = (float)(c[0] >> 8) * (1.0f / 16777216.0f);
+    }
+    __syncthreads();
+    const float t = u_sh * kept;
+    // contiguous chunks in index order, exclusive scan of their kept mass
+    const int chunk = (V + SMP_THREADS - 1) / SMP_THREADS, b0 = tid * chunk, b1 = min(V, b0 + chunk);
+    float s = 0.f;
+    for (int i = b0; i < b1; ++i)
+        if (__float_as_uint(pv[i]) >= lo) s += pv[i];
+    float inc = s;
+    const int lane = tid & 31, w = tid >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    if (lane == 31) wsum[w] = inc;
+    __syncthreads();
+    float before = 0.f;
+    for (int k = 0; k < w; ++k) before += wsum[k];
+    const float excl = before + inc - s;
+    if (s > 0.f && excl <= t && t < excl + s) {
+        float run = excl;
+        for (int i = b0; i < b1; ++i) {
+            if (__float_as_uint(pv[i]) < lo) continue;
+            run += pv[i];
+            if (run > t) {
+                atomicMin(&tok, i);
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    if (tok == INT_MAX) {  // rounding put t at or past the scanned total: the last kept index
+        int last = -1;
+        for (int i = b0; i < b1; ++i)
+            if (__float_as_uint(pv[i]) >= lo) last = i;
+        const float lm = bmax((float)last, red);
+        if (tid == 0) tok = (int)lm;
+        __syncthreads();
+    }
+    if (tid == 0) *out = tok;
+}
+
+}  // namespace
+
+size_t sample_smem_bytes(int vocab) { return (size_t)vocab * sizeof(float); }
+
+lf_status launch_sample(const float *logits, int vocab, float temperature, float top_p, uint64_t seed,
+                        uint32_t position, uint32_t sample, int32_t *token, cudaStream_t stream) {
+    if (!logits || !token || vocab < 1 || !(temperature >= 0.f) || !(top_p > 0.f && top_p <= 1.f))
+        return LF_ERR_INVALID_ARG;
+    if (sample_smem_bytes(vocab) > kSampleMaxSmem) return LF_ERR_UNSUPPORTED;
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSampleMaxSmem);
+    });
+    if (attr != cudaSuccess) return LF_ERR_CUDA;
+    sample_kernel<<<1, SMP_THREADS, sample_smem_bytes(vocab), stream>>>(
+        logits, vocab, temperature, top_p, (uint32_t)seed, (uint32_t)(seed >> 32), position, sample, token);
+    return cudaGetLastError() == cudaSuccess ? LF_OK : LF_ERR_CUDA;
+}
+
+}  // namespace lf
+
+extern "C" lf_status lf_sample(const float *logits_device, int vocab, float temperature, float top_p, uint64_t seed,
+                               uint32_t position, uint32_t sample, int32_t *token_device, void *cuda_stream) {
+    return lf::launch_sample(logits_device, vocab, temperature, top_p, seed, position, sample, token_device,
+                             static_cast<cudaStream_t>(cuda_stream));
+}

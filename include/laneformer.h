@@ -120,6 +120,34 @@ lf_status lf_decode_step(lf_engine *e, int32_t token, float *logits, int32_t *ar
  * [0, vocab); LF_ERR_CTX_OVERFLOW if position + n > ctx_cap (nothing run). */
 lf_status lf_generate(lf_engine *e, int32_t first_token, int n, int32_t *tokens_out, float *logits);
 
+/* Stochastic decoding for pass@N (News (asector), "Performance and
+ * infrastructure": several sampled solutions per prompt are affordable
+ * because one pass is fast; the pages name no method, this is temperature +
+ * nucleus sampling): like lf_generate, but each step's token is drawn from
+ * its logits instead of taken as the argmax.  p_i = exp((z_i - max z) / T);
+ * the kept set is every token whose p_i is at least tau, the largest p value
+ * for which the tokens at or above it hold at least top_p of the total mass;
+ * u = (x0 >> 8) / 2^24 with x0 the first word of Philox4x32-10 (Salmon et
+ * al., SC 2011) for key (seed low 32 bits, seed high 32 bits) and counter
+ * (position of the step, sample, 0, 0); the token is the first kept index
+ * whose running kept mass exceeds u times the kept mass.  Different `sample`
+ * values give independent streams, so N samples from the same prompt state
+ * are N calls that each start at the prompt's end (lf_set_position).
+ * temperature == 0 is greedy.  tokens_out (host, n int32) receives the n
+ * sampled tokens, logits (host, nullable) the last step's logits.
+ * LF_ERR_INVALID_ARG for n < 1, NULL tokens_out, first_token outside
+ * [0, vocab), temperature < 0 or top_p outside (0, 1]; LF_ERR_CTX_OVERFLOW if
+ * position + n > ctx_cap; LF_ERR_UNSUPPORTED for a vocabulary above 51200. */
+lf_status lf_generate_sampled(lf_engine *e, int32_t first_token, int n, float temperature, float top_p,
+                              uint64_t seed, uint32_t sample, int32_t *tokens_out, float *logits);
+
+/* The draw of lf_generate_sampled on its own: *token_device = sample of the
+ * vocab fp32 logits at logits_device (both DEVICE pointers), enqueued on
+ * cuda_stream (NULL = legacy stream) without waiting.  Same definition and
+ * error statuses as lf_generate_sampled. */
+lf_status lf_sample(const float *logits_device, int vocab, float temperature, float top_p, uint64_t seed,
+                    uint32_t position, uint32_t sample, int32_t *token_device, void *cuda_stream);
+
 /* One chained decode step, the building block of lf_generate: enqueued on the
  * engine stream without waiting; its input token is read on the device from
  * *token_device when the step starts (e.g. the previous step's argmax) and
