@@ -9,7 +9,7 @@ delayed lane sum, LM head, argmax); the position is set back to 512 before
 every step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-  python bench.py --workload e2e|long|sweep   # generation workloads, one line each
+  python bench.py --workload e2e|long|sweep|prefill|passn   # further workloads, one line each
 
 Under torchrun (N > 1) every rank decodes its own replica on its own GPU (the
 path needs no exchange between GPUs); rank 0 prints one JSON line.
@@ -408,6 +408,7 @@ GEN_WORKLOADS = {
 }
 SWEEP_CTX, SWEEP_STEPS = 2048, 256
 PREFILL_N = 3584
+PASSN = (128, 8, 256, 0.8, 0.95)  # prompt, samples, tokens per sample, temperature, top_p
 
 
 def timed_generation(eng, stream, first_token: int, n: int):
@@ -534,6 +535,54 @@ def run_generation(args, world, rank, local):
             torch.distributed.destroy_process_group()
         return
 
+    if args.workload == "passn":
+        n_prompt, n_samp, n_tok, temp, top_p = PASSN
+        shape = base
+        prompt = synth.make_tokens(SEED + rank, n_prompt, shape.vocab)
+        with Engine.from_shape(shape) as eng:
+            eng.set_stream(stream.cuda_stream)
+            eng.load_weights(blob)
+            eng.prefill_batched(prompt[:-1], logits=False)
+            eng.generate_sampled(int(prompt[-1]), max(args.warmup, 3), temp, top_p, SEED, sample=999)
+            clocks = ClockSampler(local)
+            clocks.start()
+            if world > 1:
+                torch.distributed.barrier()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            outs = []
+            for k in range(n_samp):
+                eng.set_position(n_prompt - 1)
+                toks, _ = eng.generate_sampled(int(prompt[-1]), n_tok, temp, top_p, SEED, sample=k)
+                outs.append(toks)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            clk = clocks.stop()
+            total = worst(e0.elapsed_time(e1))
+        ms = total / (n_samp * n_tok)
+        distinct = len({tuple(o) for o in outs})
+        if rank == 0:
+            line = {"metric": "batch-1 sampled decode tokens/s for pass@N (2.3B lane model, FP16)",
+                    "value": world * n_samp * n_tok / (total / 1e3), "steps": n_samp * n_tok,
+                    "warmup": max(args.warmup, 3), "ms_per_step": ms, "data": data,
+                    "config": {"workload": f"pass@{n_samp}: prompt of {n_prompt} random ids (batched prefill), then "
+                                           f"{n_samp} samples of {n_tok} tokens, temperature {temp}, top-p {top_p}, "
+                                           "each sample restarting at the prompt's end; samples run one after "
+                                           "another (no batch-N decode)", "seed": SEED,
+                               "l2": "no flush: inputs larger than L2"},
+                    "distinct_samples": distinct,
+                    "roofline": gen_roofline(shape, n_prompt - 1, n_tok, ms), "cpu_baseline": None,
+                    "e2e": {"value": world * n_samp * n_tok / (total / 1e3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                            "d2h_bytes_per_step": 4 + 32 / n_tok,
+                            "call": "lf_generate_sampled per sample (tokens copied back once per sample)"},
+                    "gpu_launches": 2 * n_samp * n_tok, "clocks": clk, **common}
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
     if args.workload == "sweep":
         variants = {}
         kv = synth.make_kv(base, SEED, SWEEP_CTX)
@@ -652,7 +701,7 @@ def main():
     ap.add_argument("--trace", default="", help="write a one-step op trace (JSON) to this path")
     ap.add_argument("--position", type=int, default=POS,
                     help="step workload: decode position (KV pre-filled up to it); 512 is the default line")
-    ap.add_argument("--workload", choices=["step", "e2e", "long", "sweep", "prefill"], default="step",
+    ap.add_argument("--workload", choices=["step", "e2e", "long", "sweep", "prefill", "passn"], default="step",
                     help="step: the single-step microbench (default line); e2e / long / sweep: the "
                          "generation workloads")
     ap.add_argument("--layers", type=int, default=0,
