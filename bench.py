@@ -535,6 +535,49 @@ def run_generation(args, world, rank, local):
             torch.distributed.destroy_process_group()
         return
 
+    if args.workload == "gemm":  # the prefill's tensor-core GEMM on its QKV shape
+        from decode_persistent_sm_gb300 import matmul_f16
+        M, N, K = PREFILL_N, 8192, 4096
+        g = torch.Generator(device="cuda").manual_seed(SEED)
+        a = torch.randn(M, K, device="cuda", generator=g).half()
+        b = (0.02 * torch.randn(N, K, device="cuda", generator=g)).half()
+        c = torch.empty(M, N, device="cuda", dtype=torch.float32)
+        for _ in range(max(args.warmup, 3)):
+            matmul_f16(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, stream.cuda_stream)
+        reps = max(1, min(args.steps, 50))
+        clocks = ClockSampler(local)
+        clocks.start()
+        times = []
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            matmul_f16(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, stream.cuda_stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        clk = clocks.stop()
+        ms = worst(float(np.median(times)))
+        flop = 2.0 * M * N * K
+        peak, kind = peak_tensor(sustained=False)
+        ach = flop / (ms / 1e3) / 1e12
+        if rank == 0:
+            print(json.dumps({
+                "metric": "tensor-core GEMM TFLOP/s (prefill QKV shape, FP16 in, fp32 out)", "value": world * ach,
+                "unit": "TFLOP/s", "steps": reps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16 x fp16 -> fp32",
+                "data": "synthetic N(0,1) x N(0,0.02)", "n_gpus": world,
+                "config": {"workload": f"C[{M}][{N}] = A[{M}][{K}] . B[{N}][{K}]^T through lf_matmul_f16 "
+                                       "(median call, events include the call's error-word set and read-back)",
+                           "l2": "operands 87 MB < L2: warm"},
+                "roofline": {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                             "frac": ach / peak, "traffic": None,
+                             "peak_source": f"{kind} dense bf16 burst (MEASURED_PEAKS.json bf16_tflops)"},
+                "cpu_baseline": None, "e2e": None, "gpu_launches": reps, "clocks": clk}), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
     if args.workload == "passn":
         n_prompt, n_samp, n_tok, temp, top_p = PASSN
         shape = base
@@ -701,7 +744,8 @@ def main():
     ap.add_argument("--trace", default="", help="write a one-step op trace (JSON) to this path")
     ap.add_argument("--position", type=int, default=POS,
                     help="step workload: decode position (KV pre-filled up to it); 512 is the default line")
-    ap.add_argument("--workload", choices=["step", "e2e", "long", "sweep", "prefill", "passn"], default="step",
+    ap.add_argument("--workload", choices=["step", "e2e", "long", "sweep", "prefill", "passn", "gemm"],
+                    default="step",
                     help="step: the single-step microbench (default line); e2e / long / sweep: the "
                          "generation workloads")
     ap.add_argument("--layers", type=int, default=0,
