@@ -48,6 +48,9 @@ enum OpType : int {
     OP_OPROJ = 7,   // merge + o_proj^T rows (waits B): partial of sub-block 2*arg
     OP_REDUCE = 8,  // chunk of R[arg] = sum of all partials of sub-block arg
     OP_LMHEAD = 9,  // final logits rows and argmax
+    // own-lane-immediate reading only (each lane adds its own partial at once):
+    OP_LREDUCE = 10,  // this CTA's chunks of RL[arg][lane] = sum of the lane's partials of sub-block arg
+    OP_LADD = 11,     // x += RL[arg][lane] (waits for the lane's sum)
 };
 // An op word: bits 0-7 type, 8-15 argument, 16-23 gain index of the next
 // NORM after this op, 24-31 lane-sum index of the next ADD within the next 4

@@ -18,6 +18,7 @@ struct lf_engine {
     // device memory
     __half *wstream = nullptr, *emb = nullptr, *gains = nullptr, *kc = nullptr, *vc = nullptr;
     float2 *rope = nullptr;
+    float *RL = nullptr;  // own-lane reading: [PS][NL][D] lane sums
     float *qkv = nullptr, *apart = nullptr, *part = nullptr, *R = nullptr, *cand_v = nullptr,
           *logits = nullptr;
     int *cand_i = nullptr, *d_ops = nullptr, *d_kvfirst = nullptr;

@@ -168,6 +168,18 @@ struct Streamer {
         cons_sync();
     }
 
+    // This CTA's partial of sub-block u is written: count it for the global
+    // sum and, in the own-lane reading, for the lane's sum.
+    __device__ void arrive_partial(int u) {
+        fence_proxy_async_global();  // read by other SMs' bulk copies
+        cons_sync();
+        if (tid == 0 && !S.abort_) {
+            __threadfence();
+            atomicAdd(&p.cnt[u], 1u);
+            if (p.own_lane) atomicAdd(&p.lcnt[u * p.NL + plan().lane], 1u);
+        }
+    }
+
     __device__ void arrive(uint32_t *ctr) {
         fence_proxy_async_global();  // these writes are read by other SMs' bulk copies
         cons_sync();
@@ -233,11 +245,51 @@ struct Streamer {
 
     // x += R[u].  Warp-local: each warp owns its residual columns, so no CTA
     // barrier; uses the copy prefetched into registers when there is one.
+    // Own-lane reading: x -= RL[u][lane] (already added by LADD(u), so that
+    // x += R[u] - RL[u][lane] adds the other lanes' share).
+    __device__ void sub_own(int u) {
+        const float *r = p.RL + ((size_t)(u % p.pslots) * p.NL + plan().lane) * D;
+#pragma unroll
+        for (int i = 0; i < C::NCHT; ++i) {
+            const float4 a = __ldcg(reinterpret_cast<const float4 *>(r + col(i)));
+            const float4 b = __ldcg(reinterpret_cast<const float4 *>(r + col(i) + 4));
+            x[8 * i + 0] -= a.x; x[8 * i + 1] -= a.y; x[8 * i + 2] -= a.z; x[8 * i + 3] -= a.w;
+            x[8 * i + 4] -= b.x; x[8 * i + 5] -= b.y; x[8 * i + 6] -= b.z; x[8 * i + 7] -= b.w;
+        }
+    }
+
+    // Own-lane reading: x += RL[u][lane], the lane's own partial of the
+    // sub-block just produced (warp-local, like add).
+    __device__ void ladd(int u) {
+        const int lam = plan().lane;
+        const uint32_t target = p.epoch * (uint32_t)plan().S;
+        if (lane == 0 && !S.abort_) {
+            const uint64_t t0 = (p.trace && tid == 0) ? global_timer_ns() : 0;
+            while (true) {
+                if ((int)(ld_acquire(&p.lready[u * p.NL + lam]) - target) >= 0) break;
+                if (ld_relaxed(p.err) != 0u) { S.abort_ = 1; break; }
+                if (global_timer_ns() > deadline) { fail(1); break; }
+            }
+            if (p.trace && tid == 0) S.t_sync += global_timer_ns() - t0;
+        }
+        __syncwarp();
+        (void)ld_acquire(&p.lready[u * p.NL + lam]);
+        const float *r = p.RL + ((size_t)(u % p.pslots) * p.NL + lam) * D;
+#pragma unroll
+        for (int i = 0; i < C::NCHT; ++i) {
+            const float4 a = __ldcg(reinterpret_cast<const float4 *>(r + col(i)));
+            const float4 b = __ldcg(reinterpret_cast<const float4 *>(r + col(i) + 4));
+            x[8 * i + 0] += a.x; x[8 * i + 1] += a.y; x[8 * i + 2] += a.z; x[8 * i + 3] += a.w;
+            x[8 * i + 4] += b.x; x[8 * i + 5] += b.y; x[8 * i + 6] += b.z; x[8 * i + 7] += b.w;
+        }
+    }
+
     __device__ void add(int u) {
         if (pre_u == u) {
 #pragma unroll
             for (int i = 0; i < C::NX; ++i) x[i] += rpre[i];
             pre_u = -1;
+            if (p.own_lane) sub_own(u);
             return;
         }
         const uint32_t target = p.epoch * (uint32_t)p.nch;
@@ -253,6 +305,7 @@ struct Streamer {
         __syncwarp();
         (void)ld_acquire(&p.ready[u]);
         load_r(u, x, true);
+        if (p.own_lane) sub_own(u);
     }
 
     // At the start of a streaming op: if the lane sum of the next ADD (within
@@ -554,7 +607,7 @@ struct Streamer {
         const int u = 2 * l + 1;
         axpy_op(lp.ffn_n, S.ubuf, p.part + (size_t)(u % p.pslots) * p.n_cta * D, false);
         if (p.tail_fused && l == p.L - 1) return;  // each thread reads back only its own columns
-        arrive(&p.cnt[u]);
+        arrive_partial(u);
     }
 
     // o_proj of layer l: waits for the attention warps to merge this CTA's
@@ -575,7 +628,7 @@ struct Streamer {
         const bool fused = p.tail_fused && l == p.L - 1;
         const int u = fused ? 2 * l + 1 : 2 * l;
         axpy_op(lp.o_n, S.obuf[l & 1], p.part + (size_t)(u % p.pslots) * p.n_cta * D, fused);
-        arrive(&p.cnt[u]);
+        arrive_partial(u);
     }
 
     // ---------------------------------------------------------- LM + argmax
@@ -653,9 +706,10 @@ struct Streamer {
                 case OP_DOWN: down(a); break;
                 case OP_OPROJ: oproj(a); break;
                 case OP_LMHEAD: lmhead(); break;
-                default: break;  // ATTN: attention warps; REDUCE: helper warp
+                case OP_LADD: ladd(a); break;
+                default: break;  // ATTN: attention warps; REDUCE, LREDUCE: helper warp
             }
-            if (p.trace && tid == 0 && t != OP_ATTN && t != OP_REDUCE) {
+            if (p.trace && tid == 0 && t != OP_ATTN && t != OP_REDUCE && t != OP_LREDUCE) {
                 unsigned long long *tr = p.trace + ((size_t)cta * p.n_ops + oi) * LF_TRACE_WORDS;
                 tr[0] = t_start;
                 tr[1] = global_timer_ns();
@@ -1185,56 +1239,103 @@ __device__ void produce(const KParams &p, Smem<D, DH> &S, uint8_t *stages, uint6
 // order k = 0, 1, ...) of their partials of sub-block u.  The 32-float pieces
 // of all CTAs lie contiguous (chunk-major partials) and arrive by one bulk
 // copy; each lane then sums one float over the pieces, and the chunk is
-// published with a release counter.
+// published with a release counter.  In the own-lane reading the same warp
+// also forms, for every LREDUCE(u), its CTA's chunks of the lane's own sum
+// RL[u][lane] (every CTA of the lane takes every S-th chunk).
 template <int D, int DH>
 __device__ void help(const KParams &p, Smem<D, DH> &S, uint64_t deadline) {
     const int lane = threadIdx.x & 31, cta = blockIdx.x;
-    if (cta >= p.nch) return;
-    const uint32_t target = p.epoch * (uint32_t)p.n_cta;
+    const CtaPlan cp = p.cta[cta];
     uint32_t nred = 0, issued = 0;
     bool ok = true;
-    for (int oi = 0; oi < p.n_ops && ok; ++oi) {
-        const int op = __ldg(p.ops + oi);
-        if (op_type(op) != OP_REDUCE) continue;
-        const int u = op_arg(op);
-        uint64_t t_w0 = 0, t_w1 = 0, t_c = 0;
+    // lane 0 waits until *ctr reaches target; false after an error or timeout
+    auto wait_count = [&](const uint32_t *ctr, uint32_t target, int oi) -> bool {
+        bool good = true;
         if (lane == 0) {
-            if (p.trace) t_w0 = global_timer_ns();
             while (true) {
-                if ((int)(ld_acquire(&p.cnt[u]) - target) >= 0) break;
-                if (S.abort_ || ld_relaxed(p.err) != 0u) { ok = false; break; }
+                if ((int)(ld_acquire(ctr) - target) >= 0) break;
+                if (S.abort_ || ld_relaxed(p.err) != 0u) { good = false; break; }
                 if (global_timer_ns() > deadline) {
                     record_error(p, &S.abort_, 4u, oi);
-                    ok = false;
+                    good = false;
                     break;
                 }
             }
-            if (p.trace) t_w1 = global_timer_ns();
-            if (ok) {
-                fence_proxy_async_global();
-                fence_proxy_async_shared();
-                mbar_arrive_expect_tx(&S.hbar, (uint32_t)p.n_cta * kRChunk * 4);
-            }
         }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        const float *src = p.part + ((size_t)(u % p.pslots) * p.n_cta * D + (size_t)cta * p.n_cta * kRChunk);
-        if (lane == 0) bulk_g2s(S.hbuf[0], src, (uint32_t)p.n_cta * kRChunk * 4, &S.hbar);
+        return __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
+    };
+    // n contiguous 32-float pieces from src into S.hbuf by one bulk copy
+    auto fetch = [&](const float *src, int n, int oi) -> bool {
+        if (lane == 0) {
+            fence_proxy_async_global();
+            fence_proxy_async_shared();  // the warp's earlier reads of hbuf come first
+            mbar_arrive_expect_tx(&S.hbar, (uint32_t)n * kRChunk * 4);
+            bulk_g2s(S.hbuf[0], src, (uint32_t)n * kRChunk * 4, &S.hbar);
+        }
         ++issued;
+        bool good = true;
         while (!mbar_try_wait(&S.hbar, nred & 1u)) {
             if (S.abort_ || global_timer_ns() > deadline) {
                 if (!S.abort_) record_error(p, &S.abort_, 4u, oi);
-                ok = false;
+                good = false;
                 break;
             }
         }
-        ok = __all_sync(0xffffffffu, ok);
+        good = __all_sync(0xffffffffu, good);
+        if (good) ++nred;
+        return good;
+    };
+    for (int oi = 0; oi < p.n_ops && ok; ++oi) {
+        const int op = __ldg(p.ops + oi);
+        const int t = op_type(op), u = op_arg(op);
+        const float *slot = p.part + (size_t)(u % p.pslots) * p.n_cta * D;
+        if (t == OP_LREDUCE) {
+            // own-lane reading: this CTA's chunks c = k, k + S, ... of the
+            // lane's sum, over the lane's S CTAs in order
+            const uint64_t t_w0 = p.trace ? global_timer_ns() : 0;
+            ok = wait_count(&p.lcnt[u * p.NL + cp.lane], p.epoch * (uint32_t)cp.S, oi);
+            const uint64_t t_w1 = p.trace ? global_timer_ns() : 0;
+            float *rl = p.RL + ((size_t)(u % p.pslots) * p.NL + cp.lane) * D;
+            for (int c = cp.k; ok && c < p.nch; c += cp.S) {
+                ok = fetch(slot + ((size_t)c * p.n_cta + cp.cta0) * kRChunk, cp.S, oi);
+                if (!ok) break;
+                float s = 0.f;
+                for (int k = 0; k < cp.S; ++k) s += S.hbuf[k][lane];
+                st_hint(rl + kRChunk * c + lane, s, policy_evict_last());
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (lane == 0) {
+                __threadfence();
+                atomicAdd(&p.lready[u * p.NL + cp.lane], 1u);
+                if (p.trace) {  // the LREDUCE op's trace slot belongs to this warp
+                    unsigned long long *tr = p.trace + ((size_t)cta * p.n_ops + oi) * LF_TRACE_WORDS;
+                    tr[0] = t_w0;
+                    tr[1] = global_timer_ns();
+                    tr[2] = t_w1 - t_w0;
+                    tr[3] = 0;
+                }
+            }
+            continue;
+        }
+        if (t != OP_REDUCE || cta >= p.nch) continue;
+        // chunk `cta` of R[u]: the pieces of all CTAs lie contiguous
+        // (chunk-major partials), one bulk copy, then each lane sums one float
+        // over the CTAs in order
+        uint64_t t_w0 = 0, t_w1 = 0, t_c = 0;
+        if (p.trace && lane == 0) t_w0 = global_timer_ns();
+        ok = wait_count(&p.cnt[u], p.epoch * (uint32_t)p.n_cta, oi);
         if (!ok) break;
-        ++nred;
+        if (p.trace && lane == 0) t_w1 = global_timer_ns();
+        const float *src = slot + (size_t)cta * p.n_cta * kRChunk;
+        ok = fetch(src, p.n_cta, oi);
+        if (!ok) break;
         if (p.trace && lane == 0) t_c = global_timer_ns();
         // The pieces are dead now (the slot is rewritten only after ready[u]
         // is seen): drop them from L2 so they are never written back to HBM.
-        for (int k = lane; k < p.n_cta; k += 32) discard_l2_line(src + (size_t)k * kRChunk);
+        // In the own-lane reading the lane sums read them too: kept.
+        if (!p.own_lane)
+            for (int k = lane; k < p.n_cta; k += 32) discard_l2_line(src + (size_t)k * kRChunk);
         float s = 0.f;
         for (int k = 0; k < p.n_cta; ++k) s += S.hbuf[k][lane];
         st_hint(p.R + (size_t)u * D + kRChunk * cta + lane, s, policy_evict_last());

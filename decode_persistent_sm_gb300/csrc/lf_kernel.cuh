@@ -15,6 +15,7 @@ struct KParams {
     int hc, kt;  // attention: KV heads per chunk, keys per tile
     int pslots;  // lane-sum partial slots
     int tail_fused;  // 1: the last layer's two sub-blocks share one partial and one lane sum
+    int own_lane;    // 1: own-lane-immediate reading (lane sums RL, LREDUCE / LADD ops)
     float eps, attn_scale;
     // this step
     int pos, token;
@@ -42,6 +43,8 @@ struct KParams {
     float *R;               // [2L][D]
     uint32_t *barA, *barB;  // [L][NL]
     uint32_t *cnt, *ready;  // [2L]
+    uint32_t *lcnt, *lready;  // [2L][NL]: own-lane reading, per-lane arrivals and sums done
+    float *RL;              // [pslots][NL][D]: own-lane reading, each lane's sum of its partials
     uint32_t *fin;          // [1]
     float *cand_v;          // [n_cta]
     int *cand_i;            // [n_cta]

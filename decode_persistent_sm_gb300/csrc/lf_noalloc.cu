@@ -80,6 +80,7 @@ extern "C" lf_status lf_decode_step_static_scratch(lf_engine *e, int32_t token,
     const lf::Shape &s = P.sh;
     const Carve c = carve(e);
     if (c.total > (size_t)LF_STATIC_SCRATCH_BYTES) return LF_ERR_UNSUPPORTED;
+    if (s.own) return LF_ERR_UNSUPPORTED;  // the own-lane reading's lane sums are not carved here
     if (!e->loaded) return LF_ERR_NOT_LOADED;
     if (token < 0 || token >= s.V) return LF_ERR_INVALID_ARG;
     if (e->pos >= s.ctx) return LF_ERR_CTX_OVERFLOW;
@@ -107,7 +108,7 @@ extern "C" lf_status lf_decode_step_static_scratch(lf_engine *e, int32_t token,
     k.hc = s.HC;
     k.kt = s.KT;
     k.pslots = s.PS;
-    k.tail_fused = s.delay >= 1 ? 1 : 0;
+    k.tail_fused = s.delay >= 1 ? 1 : 0;  // (the own-lane reading is rejected above)
     k.eps = e->cfg.rms_eps;
     k.attn_scale = (float)(1.0 / std::sqrt((double)s.DH));
     k.pos = e->pos;

@@ -54,7 +54,9 @@ lf_status derive_shape(const lf_config &c, Shape *sh) {
     s.off_lm = s.off_gf + D;
     s.n_params = s.off_lm + (long long)s.V * D;
 
-    if (c.own_lane_immediate) return LF_ERR_UNSUPPORTED;
+    // With delay 0 both readings are the same function (the own partial is
+    // summed with the others at once); the own-lane path is used for d > 0.
+    s.own = c.own_lane_immediate != 0 && c.dtp_delay > 0;
     const bool kern = (s.D == 4096 && s.DH == 128) || (s.D == 256 && s.DH == 32);
     // Attention: the q heads of a lane-local KV head times head_dim must tile
     // the 256 consumer threads.
@@ -95,7 +97,7 @@ static std::vector<int> build_ops(const Shape &s) {
     // With a delay the final drain alone reads the last layer's two
     // sub-blocks: they share one partial (down_proj first, o_proj onto it)
     // and one lane sum, published as sub-block 2L - 1.
-    const int fused = d >= 1 ? 2 * L - 2 : -1;
+    const int fused = (d >= 1 && !s.own) ? 2 * L - 2 : -1;
     int next_add = 0;
     auto adds_upto = [&](int last) {
         for (; next_add <= last; ++next_add)
@@ -103,7 +105,26 @@ static std::vector<int> build_ops(const Shape &s) {
     };
     for (int l = 0; l < L; ++l) {
         const int sa = 2 * l, sf = 2 * l + 1;
-        if (d == 0) {
+        if (s.own) {
+            // Own lane immediate: every sub-block reads its own lane's partial
+            // of the previous one, so the lane runs them in dependency order;
+            // after each producer the lane's sum is formed and added at once
+            // (LREDUCE on the lane's helper warps, LADD on the streamers), and
+            // the other lanes' share joins 2d sub-blocks later (ADD).
+            adds_upto(sa - 1 - 2 * d);
+            ops.push_back(make_op(OP_NORM, l));
+            ops.push_back(make_op(OP_QKV, l));
+            ops.push_back(make_op(OP_ATTN, l));
+            ops.push_back(make_op(OP_OPROJ, l));
+            ops.push_back(make_op(OP_LREDUCE, sa));
+            ops.push_back(make_op(OP_LADD, sa));
+            adds_upto(sf - 1 - 2 * d);
+            ops.push_back(make_op(OP_NORM, L + l));
+            ops.push_back(make_op(OP_GATEUP, l));
+            ops.push_back(make_op(OP_DOWN, l));
+            ops.push_back(make_op(OP_LREDUCE, sf));
+            ops.push_back(make_op(OP_LADD, sf));
+        } else if (d == 0) {
             adds_upto(sa - 1);
             ops.push_back(make_op(OP_NORM, l));
             ops.push_back(make_op(OP_QKV, l));
@@ -145,6 +166,7 @@ static std::vector<int> build_ops(const Shape &s) {
         if (t == OP_OPROJ) prod[2 * a] = i;
         if (t == OP_DOWN) prod[2 * a + 1] = i;
         if (t == OP_ADD) cons[a] = i;
+        if (t == OP_LREDUCE) prod[a] = i;  // the global sum comes after the lane's own
     }
     if (fused >= 0) {  // the op that completes the shared partial
         if (prod[fused] < prod[fused + 1]) return {};

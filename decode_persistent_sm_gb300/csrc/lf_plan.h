@@ -21,6 +21,7 @@ struct Shape {
     int HC;     // KV heads processed together in attention (HC * GL * DH <= 512)
     int KT;     // keys per attention tile: K and V of HC heads fill one stage
     int PS;     // lane-sum partial slots (sub-block u uses slot u % PS)
+    bool own;   // own-lane-immediate reading (with a delay > 0)
     std::vector<int> kv_first;  // per lane: first global KV head it reads
     // element offsets in the FP16 blob
     long long off_E, per_layer, off_layer0, off_gf, off_lm, n_params;

@@ -222,7 +222,7 @@ lf_status lf_create(const lf_config *cfg, lf_engine **out) {
     const lf::Plan &P = e->plan;
     const lf::Shape &s = P.sh;
     const int L = s.L, NC = P.n_cta;
-    e->n_ctr = (size_t)L * s.NL * 2 + (size_t)4 * L + 1;
+    e->n_ctr = (size_t)L * s.NL * 2 + (size_t)4 * L + 1 + (size_t)4 * L * s.NL;  // + own-lane counters
     const size_t kv_elems = (size_t)s.NL * L * s.HKV_L * s.ctx * s.DH;
     const int qkv_l = (s.HQ_L + 2 * s.HKV_L) * s.DH;
     cudaError_t err = cudaSuccess;
@@ -238,6 +238,7 @@ lf_status lf_create(const lf_config *cfg, lf_engine **out) {
     ALLOC(apart, (size_t)L * NC * s.HQ_L * (s.DH + 2));
     ALLOC(part, (size_t)s.PS * NC * s.D);
     ALLOC(R, (size_t)2 * L * s.D);
+    ALLOC(RL, s.own ? (size_t)s.PS * s.NL * s.D : 1);
     ALLOC(ctr, e->n_ctr);
     ALLOC(status, 8);
     ALLOC(gen, s.ctx);
@@ -400,7 +401,9 @@ static lf_status enqueue_step(lf_engine *e, int32_t token, const int32_t *token_
     k.hc = s.HC;
     k.kt = s.KT;
     k.pslots = s.PS;
-    k.tail_fused = s.delay >= 1 ? 1 : 0;
+    k.tail_fused = (s.delay >= 1 && !s.own) ? 1 : 0;
+    k.own_lane = s.own ? 1 : 0;
+    k.RL = e->RL;
     k.eps = e->cfg.rms_eps;
     k.attn_scale = (float)(1.0 / std::sqrt((double)s.DH));
     k.pos = e->pos;
@@ -420,7 +423,9 @@ static lf_status enqueue_step(lf_engine *e, int32_t token, const int32_t *token_
     k.barB = c; c += (size_t)s.L * s.NL;
     k.cnt = c; c += 2 * s.L;
     k.ready = c; c += 2 * s.L;
-    k.fin = c;
+    k.fin = c; c += 1;
+    k.lcnt = c; c += (size_t)2 * s.L * s.NL;
+    k.lready = c;
     k.cand_v = e->cand_v; k.cand_i = e->cand_i; k.logits = e->logits;
     k.argmax = argmax_dst;
     k.err = e->status + 4;

@@ -58,7 +58,12 @@ typedef enum {
  * tensor-parallel synchronisation.  (Sections "Hiding overhead" of the blog
  * and "Architectural decisions" of the news page fix only that the
  * synchronisation is delayed by 2 layers; this exact form is the reading this
- * library implements.)
+ * library implements by default.)  own_lane_immediate = 1 selects the other
+ * reading: lane i's residual also holds its own partials P_i[u] of sub-blocks
+ * s-2d <= u <= s-1 at once (the lane's own output is local to it), the other
+ * lanes' share arriving 2*dtp_delay sub-blocks later; with dtp_delay = 0 the
+ * two readings are the same function.  The own-lane reading runs each lane's
+ * sub-blocks in dependency order with a lane-local sum after every one.
  */
 typedef struct {
     int n_layers, d_model, n_q_heads, n_kv_heads, head_dim, ffn_dim, vocab;
@@ -67,7 +72,7 @@ typedef struct {
     int ctx_cap;             /* maximum context (positions 0 .. ctx_cap-1) */
     float rms_eps, rope_theta;
     int swa_window[LF_MAX_LAYERS]; /* per layer: keys j > p - W; 0 = full causal */
-    int own_lane_immediate;  /* must be 0 (lane adds own partial at once: not built) */
+    int own_lane_immediate;  /* 0: delayed sum as above; 1: each lane adds its own partial at once */
 } lf_config;
 
 typedef struct lf_engine lf_engine;
@@ -252,7 +257,8 @@ lf_status lf_debug_read_trace(lf_engine *e, uint64_t *out, size_t n_words, int32
  * them one after another.  Synchronous: waits for the step and reports a
  * device-side timeout.  Returns LF_ERR_UNSUPPORTED when the engine's working
  * set does not fit the array (the full 2.3B lane model needs about 26 MB on
- * 152 SMs), LF_ERR_INVALID_ARG for null outputs or another current device,
+ * 152 SMs) or the config asks for the own-lane-immediate reading,
+ * LF_ERR_INVALID_ARG for null outputs or another current device,
  * and the same statuses as lf_decode_step otherwise.
  */
 #define LF_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)

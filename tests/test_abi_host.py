@@ -63,7 +63,7 @@ def test_validate_config(lib):
     assert binding.validate_config(cfg(synth.FULL, dtp_delay=-1)) == 1
     assert binding.validate_config(cfg(synth.FULL, ctx_cap=0)) == 1
     assert binding.validate_config(cfg(synth.FULL, d_model=1024)) == 7       # no kernel for it
-    assert binding.validate_config(cfg(synth.FULL, own_lane_immediate=1)) == 7
+    assert binding.validate_config(cfg(synth.FULL, own_lane_immediate=1)) == 0   # the second DTP reading
 
 
 @pytest.mark.parametrize("shape_name,lanes,delay", [("FULL", 8, 2), ("FULL", 1, 0), ("FULL", 8, 0),
@@ -110,3 +110,16 @@ def test_trace_word_count_matches_the_header():
     from decode_persistent_sm_gb300 import binding
     m = re.search(r"#define\s+LF_TRACE_WORDS\s+(\d+)", open(HEADER).read())
     assert m and int(m.group(1)) == binding.TRACE_WORDS
+
+
+@pytest.mark.parametrize("lanes,delay", [(8, 1), (8, 2), (4, 3)])
+def test_own_lane_plan_adds_a_lane_sum_per_sub_block(lib, lanes, delay):
+    from decode_persistent_sm_gb300 import binding
+    shape = synth.FULL.replace(n_lanes=lanes, dtp_delay=delay)
+    rc_a, a = binding.plan_stats(cfg(shape), 152)
+    rc_b, b = binding.plan_stats(cfg(shape, own_lane_immediate=1), 152)
+    assert rc_a == rc_b == 0 and b[4] == 1 and b[0] == a[0]
+    # one LREDUCE and one LADD per sub-block; the last layer's two sub-blocks
+    # keep separate global sums (one more REDUCE and one more ADD)
+    assert b[3] == a[3] + 2 * (2 * shape.n_layers) + 2
+
