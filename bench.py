@@ -633,23 +633,22 @@ def run_generation(args, world, rank, local):
         clocks = ClockSampler(local)
         clocks.start()
         launches = 0
-        for delay in (0, 1, 2):
-            for lanes in (1, 8):
-                shape = base.replace(n_lanes=lanes, dtp_delay=delay)
-                with Engine.from_shape(shape) as eng:
-                    eng.set_stream(stream.cuda_stream)
-                    eng.load_weights(blob)
-                    eng.load_kv(kv, SWEEP_CTX)
-                    eng.generate(first, max(args.warmup, 3))
-                    eng.set_position(SWEEP_CTX)
-                    if world > 1:
-                        torch.distributed.barrier()
-                    _, per, total = timed_generation(eng, stream, first, SWEEP_STEPS)
-                    total = worst(total)
-                    launches += SWEEP_STEPS
-                variants[f"delay{delay}_lanes{lanes}"] = {
-                    "value": world * SWEEP_STEPS / (total / 1e3), "ms_per_step": total / SWEEP_STEPS,
-                    **latency_summary(per)}
+        for delay, lanes, own in [(d, n, o) for d in (0, 1, 2) for n in (1, 8) for o in (0, 1) if d > 0 or o == 0]:
+            shape = base.replace(n_lanes=lanes, dtp_delay=delay, own_lane_immediate=own)
+            with Engine.from_shape(shape) as eng:
+                eng.set_stream(stream.cuda_stream)
+                eng.load_weights(blob)
+                eng.load_kv(kv, SWEEP_CTX)
+                eng.generate(first, max(args.warmup, 3))
+                eng.set_position(SWEEP_CTX)
+                if world > 1:
+                    torch.distributed.barrier()
+                _, per, total = timed_generation(eng, stream, first, SWEEP_STEPS)
+                total = worst(total)
+                launches += SWEEP_STEPS
+            variants[f"delay{delay}_lanes{lanes}" + ("_own" if own else "")] = {
+                "value": world * SWEEP_STEPS / (total / 1e3), "ms_per_step": total / SWEEP_STEPS,
+                **latency_summary(per)}
         clk = clocks.stop()
         main_v = variants["delay2_lanes8"]
         if rank == 0:
@@ -657,8 +656,9 @@ def run_generation(args, world, rank, local):
                     "steps": SWEEP_STEPS, "warmup": max(args.warmup, 3), "ms_per_step": main_v["ms_per_step"],
                     "data": data + ", N(0,1) KV fill",
                     "config": {"workload": f"sweep: KV pre-filled N(0,1) to {SWEEP_CTX}, then {SWEEP_STEPS} greedy "
-                                           "tokens chained on the device for delay in {0,1,2} x lanes in {1,8}; "
-                                           "value = delay 2, 8 lanes", "seed": SEED,
+                                           "tokens chained on the device for delay in {0,1,2} x lanes in {1,8}, "
+                                           "both readings of the delayed sum for delay > 0 (_own: each lane "
+                                           "adds its own partial at once); value = delay 2, 8 lanes", "seed": SEED,
                                "l2": "no flush: inputs larger than L2"},
                     "variants": variants,
                     "roofline": gen_roofline(base, SWEEP_CTX, SWEEP_STEPS, main_v["ms_per_step"]),
