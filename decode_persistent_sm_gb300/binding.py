@@ -29,6 +29,7 @@ _SIGS = {
     "lf_decode_step": (_ci, [_vp, _i32, _vp, _vp]),
     "lf_matmul_f16": (_ci, [_vp, _vp, _vp, _ci, _ci, _ci, _vp]),
     "lf_prefill_batched": (_ci, [_vp, _vp, _ci, _vp, _vp]),
+    "lf_set_prefill_attention": (_ci, [_vp, _ci]),
     "lf_generate": (_ci, [_vp, _i32, _ci, _vp, _vp]),
     "lf_generate_sampled": (_ci, [_vp, _i32, _ci, ctypes.c_float, ctypes.c_float, ctypes.c_uint64, ctypes.c_uint32,
                                   _vp, _vp]),
@@ -246,6 +247,9 @@ class Engine:
                                           out.ctypes.data if logits else None, ctypes.byref(am))
         _check("lf_prefill_batched", rc)
         return out, am.value
+
+    def set_prefill_attention(self, tensor_cores: bool):
+        _check("lf_set_prefill_attention", self._lib.lf_set_prefill_attention(self._h, 1 if tensor_cores else 0))
 
     def synchronize(self):
         _check("lf_synchronize", self._lib.lf_synchronize(self._h))

@@ -29,6 +29,7 @@ struct lf_engine {
     void *pf_mem = nullptr;      // lf_prefill_batched scratch (grow-only, owned separately)
     size_t pf_bytes = 0;
     uint32_t *pf_err = nullptr;  // device word: GEMM wait timeouts during a batched prefill
+    int pf_tc_attention = 1;     // batched prefill attention on the tensor cores (head_dim 128)
     lf::CtaPlan *d_cta = nullptr;
     lf::LayerPlan *d_lp = nullptr;
     size_t n_ctr = 0;

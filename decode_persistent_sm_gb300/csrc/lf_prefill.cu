@@ -19,6 +19,7 @@
 
 #include "laneformer.h"
 #include "lf_engine.h"
+#include "lf_pf_attn_tc.h"
 #include "lf_tc_gemm.h"
 
 namespace {
@@ -63,10 +64,10 @@ __global__ void pf_rmsnorm(const float *__restrict__ x, const __half *__restrict
 }
 
 // RoPE on q and k (pairs c, c + dh/2; table rope[p][c] = (cos, sin)), q kept
-// in fp32, k and v rounded to FP16 into the cache of every lane that reads
+// in fp32 (CUDA-core attention) and FP16 (tensor-core attention), k and v rounded to FP16 into the cache of every lane that reads
 // that KV head.  One block per position.
 __global__ void pf_rope_kv(const float *__restrict__ qkv, const float2 *__restrict__ rope, float *__restrict__ q,
-                           __half *__restrict__ kc, __half *__restrict__ vc, const int *__restrict__ kv_first,
+                           __half *__restrict__ q16, __half *__restrict__ kc, __half *__restrict__ vc, const int *__restrict__ kv_first,
                            int p0, int NQ, int NKV, int DH, int NL, int L, int l, int HKV_L, int ctx) {
     const int i = blockIdx.x, p = p0 + i, half = DH / 2;
     const float *row = qkv + (size_t)i * (NQ + 2 * NKV) * DH;
@@ -75,8 +76,11 @@ __global__ void pf_rope_kv(const float *__restrict__ qkv, const float2 *__restri
         const int hq = t / half, c = t % half;
         const float a = row[hq * DH + c], b = row[hq * DH + c + half];
         const float2 r = cs[c];
-        q[(size_t)i * NQ * DH + hq * DH + c] = a * r.x - b * r.y;
-        q[(size_t)i * NQ * DH + hq * DH + c + half] = a * r.y + b * r.x;
+        const float qa = a * r.x - b * r.y, qb = a * r.y + b * r.x;
+        q[(size_t)i * NQ * DH + hq * DH + c] = qa;
+        q[(size_t)i * NQ * DH + hq * DH + c + half] = qb;
+        q16[(size_t)i * NQ * DH + hq * DH + c] = __float2half_rn(qa);
+        q16[(size_t)i * NQ * DH + hq * DH + c + half] = __float2half_rn(qb);
     }
     for (int t = threadIdx.x; t < NL * HKV_L * half; t += blockDim.x) {
         const int lg = t / half, c = t % half, lam = lg / HKV_L, g = lg % HKV_L;
@@ -164,6 +168,12 @@ uint32_t *matmul_err_word() {
 }
 
 }  // namespace
+
+extern "C" lf_status lf_set_prefill_attention(lf_engine *e, int tensor_cores) {
+    if (!e || (tensor_cores != 0 && tensor_cores != 1)) return LF_ERR_INVALID_ARG;
+    e->pf_tc_attention = tensor_cores;
+    return LF_OK;
+}
 
 extern "C" lf_status lf_matmul_f16(const void *a_device, const void *b_device, float *c_device, int m, int n, int k,
                                    void *cuda_stream) {
@@ -336,7 +346,7 @@ size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 struct PfBufs {
     int *tok;
     float *x, *ring, *qkv, *qf, *gu;
-    __half *h, *o, *u;
+    __half *h, *o, *u, *q16;
     size_t bytes;
 };
 
@@ -359,6 +369,7 @@ PfBufs carve(uint8_t *base, const lf::Shape &s, int M) {
     b.h = reinterpret_cast<__half *>(take(M * std::max(D, F) * 2));
     b.o = reinterpret_cast<__half *>(take(M * QD * 2));
     b.u = reinterpret_cast<__half *>(take(M * F * 2));
+    b.q16 = reinterpret_cast<__half *>(take(M * QD * 2));
     b.bytes = at;
     return b;
 }
@@ -427,10 +438,14 @@ extern "C" lf_status lf_prefill_batched(lf_engine *e, const int32_t *tokens, int
             pf_rmsnorm<<<M, 256, 0, st>>>(b.x, e->gains + (size_t)l * D, b.h, D, eps);
             gs = lf::tc_gemm_f16(b.h, lw + s.o_wq, b.qkv, M, QKVN, D, QKVN, e->pf_err, kGemmTimeoutNs, st);
             if (gs != LF_OK) return gs == LF_ERR_CUDA ? pf_fail(e) : gs;
-            pf_rope_kv<<<M, 256, 0, st>>>(b.qkv, e->rope, b.qf, e->kc, e->vc, e->d_kvfirst, p0, NQ, NKV, DH, s.NL,
-                                          L, l, s.HKV_L, s.ctx);
+            pf_rope_kv<<<M, 256, 0, st>>>(b.qkv, e->rope, b.qf, b.q16, e->kc, e->vc, e->d_kvfirst, p0, NQ, NKV, DH,
+                                          s.NL, L, l, s.HKV_L, s.ctx);
             const dim3 ag((M + PF_QB - 1) / PF_QB, NQ);
-            if (DH == 128)
+            if (DH == 128 && e->pf_tc_attention) {
+                lf::TcAttnArgs ta{M, p0, NQ, s.HQ_L, s.GL, s.HKV_L, L, l, s.ctx, e->cfg.swa_window[l], scale, b.o, QD};
+                gs = lf::pf_attention_tc(b.q16, e->kc, e->vc, ta, s.NL, e->pf_err, kGemmTimeoutNs, st);
+                if (gs != LF_OK) return gs == LF_ERR_CUDA ? pf_fail(e) : gs;
+            } else if (DH == 128)
                 pf_attention<128><<<ag, 128, pf_attn_smem<128>(), st>>>(b.qf, e->kc, e->vc, b.o, M, p0, NQ, s.HQ_L,
                                                                          s.GL, s.HKV_L, L, l, s.ctx,
                                                                          e->cfg.swa_window[l], scale);

@@ -17,7 +17,7 @@
 
 #include <mutex>
 
-#include "lf_ptx.cuh"
+#include "lf_tc.cuh"
 #include "lf_tc_gemm.h"
 
 namespace lf {
@@ -36,63 +36,7 @@ struct TgShared {
     volatile int abort_;
 };
 
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-            "r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// Shared-memory matrix descriptor of a K-major operand tile with 128-byte
-// swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart (stride byte
-// offset), leading byte offset unused for this layout, descriptor version 1,
-// layout code 2 (128-byte swizzle).  The tile must be 1024-byte aligned.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
-    d |= (uint64_t)(1024u >> 4) << 32;         // stride byte offset
-    d |= (uint64_t)1 << 46;                    // version
-    d |= (uint64_t)2 << 61;                    // 128-byte swizzle
-    return d;
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulate, A and B fp16, both
-// K-major, N = 256, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, float *v) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
+constexpr uint32_t kIdesc = idesc_f16(BM, BN);
 
 // Bounded wait on an mbarrier phase; false on timeout or abort.
 __device__ __forceinline__ bool wait_phase(TgShared &S, uint64_t *bar, uint32_t parity, uint64_t deadline,
@@ -126,14 +70,11 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
         mbar_init(&S.accum, 1);
         S.abort_ = 0;
         fence_barrier_init();
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmB);
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&S.tmem_base)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        tc_alloc(&S.tmem_base, TMEM_COLS);
     }
     tc_fence_before();
     __syncthreads();
@@ -169,7 +110,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                 const uint32_t a = smem_u32(tiles + (size_t)s * STAGE_BYTES), b = a + A_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)  // 16 fp16 = 32 bytes along K per instruction
-                    tc_mma(tmem, smem_desc_sw128(a + 32 * kk), smem_desc_sw128(b + 32 * kk), (kb | kk) != 0);
+                    tc_mma(tmem, smem_desc_sw128(a + 32 * kk), smem_desc_sw128(b + 32 * kk), kIdesc, (kb | kk) != 0);
                 tc_commit(&S.empty[s]);  // the stage is free once these MMAs have read it
             }
             tc_commit(&S.accum);  // all MMAs issued above are complete when this arrives
@@ -208,7 +149,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
         }
         __syncwarp();
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+        tc_dealloc(tmem, TMEM_COLS);
     }
 }
 

@@ -286,6 +286,13 @@ lf_status lf_decode_step_static_scratch(lf_engine *e, int32_t token, float *logi
  * wait ran out (engine poisoned). */
 lf_status lf_prefill_batched(lf_engine *e, const int32_t *tokens, int n, float *logits, int32_t *argmax);
 
+/* Which attention lf_prefill_batched uses: tensor_cores = 1 (default) runs
+ * S = Q K^T and O = P V as tcgen05 MMAs (head_dim 128; other head sizes use
+ * the CUDA-core kernel anyway), 0 the CUDA-core kernel.  Same function up to
+ * rounding (P and q are FP16 operands on the tensor-core path).
+ * LF_ERR_INVALID_ARG for other values. */
+lf_status lf_set_prefill_attention(lf_engine *e, int tensor_cores);
+
 /* Tensor-core matrix product of the batched prefill (lf_prefill_batched),
  * exported for tests and for callers that build their own batched passes:
  * c[m][n] = sum_k a[m][k] * b[n][k], with a (m x k) and b (n x k) row-major

@@ -112,3 +112,36 @@ def test_full_shape_prompt_128():
     _, _, pre_rel, pre_agree, rels, agree = prefill_then_steps(shape, 1, 128, 2, gain_std=0.0)
     assert pre_rel <= REL_L2 and pre_agree
     assert_gates(rels, agree, "full shape after a 128-token batched prefill")
+
+
+@pytest.mark.slow
+def test_full_shape_prompt_260_tensor_core_attention():
+    # three 128-query tiles and three 128-key tiles on the tensor-core path
+    shape = synth.FULL
+    _, _, pre_rel, pre_agree, rels, agree = prefill_then_steps(shape, 3, 260, 2, gain_std=0.0)
+    assert pre_rel <= REL_L2 and pre_agree
+    assert_gates(rels, agree, "full shape after a 260-token batched prefill")
+
+
+@pytest.mark.slow
+def test_tensor_core_and_cuda_core_attention_agree_past_the_window():
+    # 1500 positions: the sliding-window layers' 1024-key window is crossed;
+    # both prefill attentions must give the same function (the oracle checks
+    # each of them on shorter prompts)
+    from decode_persistent_sm_gb300 import Engine
+    shape = synth.FULL
+    blob = synth.make_weights(shape, 4)
+    tokens = synth.make_tokens(4, 1503, shape.vocab)
+    out = {}
+    with Engine.from_shape(shape) as eng:
+        eng.load_weights(blob)
+        for tc in (True, False):
+            eng.reset()
+            eng.set_prefill_attention(tc)
+            got, am = eng.prefill_batched(tokens[:1500])
+            steps = [eng.decode_step(int(t)) for t in tokens[1500:]]
+            out[tc] = (got, am, steps)
+    (g1, a1, s1), (g0, a0, s0) = out[True], out[False]
+    assert rel_l2(g1, g0) <= REL_L2 and a1 == a0
+    for (l1, m1), (l0, m0) in zip(s1, s0):
+        assert rel_l2(l1, l0) <= REL_L2 and m1 == m0
