@@ -3,13 +3,17 @@
 //
 // One CTA = 128 queries of one q head (one TMEM lane per query).  Keys of the
 // head's FP16 cache come in tiles of 128.  Two passes over the key tiles:
-//   pass 1: S = Q K^T (tcgen05.mma into TMEM columns 0..127); each of the
+//   pass 1: S = Q K^T (tcgen05.mma into TMEM, 128 columns); each of the
 //           four softmax warps reads its 32 rows (tcgen05.ld, one query row
 //           per thread) and keeps the row's running max and sum;
 //   pass 2: S again; P = exp(S - max) in FP16 written to shared memory in the
 //           128-byte-swizzled K-major operand layout; the V tile transposed
 //           into the same layout; O += P V^T (tcgen05.mma into TMEM columns
-//           128..255), so O never needs rescaling.
+//           256..383), so O never needs rescaling.
+// K tiles and S are double-buffered (two shared-memory K buffers, two sets
+// of TMEM columns), so S of the next step is computed while the softmax
+// warps work on this one, and the P.V MMAs of a step overlap the next
+// step's softmax.
 // Finally O / sum is stored per row.  Warp 0 issues the TMA copies, one
 // thread of warp 1 issues the MMAs (and owns the TMEM allocation), warps 2-5
 // do the softmax.  Every wait is bounded; a timed-out CTA records the error,
@@ -28,18 +32,28 @@ namespace {
 
 constexpr int AQ = 128, AK = 128, ADH = 128;  // queries per CTA, keys per tile, head dimension
 constexpr int A_THREADS = 192;
-constexpr uint32_t A_TMEM_COLS = 256;  // S in columns [0, 128), O in [128, 256)
+constexpr uint32_t A_TMEM_COLS = 512;  // S buffers in columns [0, 128) and [128, 256), O in [256, 384)
+constexpr uint32_t TM_O = 256;
 constexpr int HALF_TILE = AQ * 64 * 2;  // one [128 rows][64] FP16 swizzled tile, 16 KB
-constexpr int OFF_Q = 0, OFF_K = 2 * HALF_TILE, OFF_V = 4 * HALF_TILE, OFF_VT = 6 * HALF_TILE,
-              OFF_P = 8 * HALF_TILE, A_TILES = 10 * HALF_TILE;
+constexpr int OFF_Q = 0, OFF_K = 2 * HALF_TILE /* two K buffers */, OFF_V = 6 * HALF_TILE, OFF_VT = 8 * HALF_TILE,
+              OFF_P = 10 * HALF_TILE, A_TILES = 12 * HALF_TILE;
 constexpr size_t A_SMEM = (size_t)A_TILES + 1024 + 256;
 constexpr uint32_t kIdescA = idesc_f16(AQ, AK);  // S: N = keys; O: N = head dimension (also 128)
+constexpr float kLog2e = 1.4426950408889634f;
 
+// Every barrier completes once per use of what it guards, and no waiter can
+// fall two phases behind, so parity waits are unambiguous.
 struct AttnShared {
-    uint64_t bq, bk, bv, bs, bp, bo;  // Q loaded, K loaded, V loaded, S done, softmax step done, P.V done
+    uint64_t bq;      // Q loaded
+    uint64_t bk[2];   // K buffer b loaded (steps b, b + 2, ...)
+    uint64_t bs[2];   // S buffer b computed
+    uint64_t bp[2];   // S buffer b read by the softmax warps (128 arrivals)
+    uint64_t bpw;     // pass 2: P and V^T written (128 arrivals)
+    uint64_t bv;      // V tile loaded
+    uint64_t bo;      // P.V MMAs done
     uint32_t tmem;
     volatile int abort_;
-    volatile int ns_, no_;  // commits issued on bs / bo (for the drain after an error)
+    volatile int nbs_[2], nbo_;  // commits issued (for the drain after an error)
 };
 
 __device__ __forceinline__ bool await_phase(AttnShared &S, uint64_t *bar, uint32_t parity, uint64_t deadline,
@@ -67,20 +81,23 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     const int rows = min(AQ, a.M - i0);
     const int p_first = a.p0 + i0, p_last = a.p0 + i0 + rows - 1;
     const int lo = a.window > 0 ? max(0, p_first - a.window + 1) : 0, hi = p_last;
-    const int kt0 = lo / AK, ntiles = hi / AK - kt0 + 1;
+    const int kt0 = lo / AK, ntiles = hi / AK - kt0 + 1, nsteps = 2 * ntiles;
     const int lam = h / a.HQ_L, g = (h % a.HQ_L) / a.GL, z = (lam * a.L + a.l) * a.HKV_L + g;
     const uint64_t deadline = global_timer_ns() + timeout_ns;
 
     if (threadIdx.x == 0) {
         mbar_init(&S.bq, 1);
-        mbar_init(&S.bk, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&S.bk[b], 1);
+            mbar_init(&S.bs[b], 1);
+            mbar_init(&S.bp[b], 128);
+            S.nbs_[b] = 0;
+        }
+        mbar_init(&S.bpw, 128);
         mbar_init(&S.bv, 1);
-        mbar_init(&S.bs, 1);
-        mbar_init(&S.bp, 128);
         mbar_init(&S.bo, 1);
         S.abort_ = 0;
-        S.ns_ = 0;
-        S.no_ = 0;
+        S.nbo_ = 0;
         fence_barrier_init();
         tma_prefetch_map(&tmQ);
         tma_prefetch_map(&tmK);
@@ -94,20 +111,21 @@ __global__ void __launch_bounds__(A_THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0) {  // copies
-            int nk = 0, nv = 0;  // K / V tiles issued
+            int nk[2] = {0, 0}, nv = 0;
             mbar_arrive_expect_tx(&S.bq, 2 * HALF_TILE);
             tma_load_2d(t + OFF_Q, &tmQ, h * ADH, i0, &S.bq);
             tma_load_2d(t + OFF_Q + HALF_TILE, &tmQ, h * ADH + 64, i0, &S.bq);
-            for (int step = 0; step < 2 * ntiles; ++step) {
-                const int kt = kt0 + step % ntiles, j = step - ntiles;
-                // the K tile is free once the previous step's S MMAs completed
-                if (step > 0 && !await_phase(S, &S.bs, (step - 1) & 1u, deadline, err)) break;
-                mbar_arrive_expect_tx(&S.bk, 2 * HALF_TILE);
-                tma_load_3d(t + OFF_K, &tmK, 0, kt * AK, z, &S.bk);
-                tma_load_3d(t + OFF_K + HALF_TILE, &tmK, 64, kt * AK, z, &S.bk);
-                ++nk;
-                if (j >= 0) {  // the V staging tile is free once the previous step's transpose is done
-                    if (j > 0 && !await_phase(S, &S.bp, (step - 1) & 1u, deadline, err)) break;
+            for (int step = 0; step < nsteps; ++step) {
+                const int b = step & 1, kt = kt0 + step % ntiles, j = step - ntiles;
+                // K buffer b is free once S of step - 2 is computed
+                if (step >= 2 && !await_phase(S, &S.bs[b], ((step - 2) >> 1) & 1u, deadline, err)) break;
+                uint8_t *kb = t + OFF_K + b * 2 * HALF_TILE;
+                mbar_arrive_expect_tx(&S.bk[b], 2 * HALF_TILE);
+                tma_load_3d(kb, &tmK, 0, kt * AK, z, &S.bk[b]);
+                tma_load_3d(kb + HALF_TILE, &tmK, 64, kt * AK, z, &S.bk[b]);
+                ++nk[b];
+                if (j >= 0) {  // the V staging tile is free once the previous transpose is written
+                    if (j > 0 && !await_phase(S, &S.bpw, (j - 1) & 1u, deadline, err)) break;
                     mbar_arrive_expect_tx(&S.bv, 2 * HALF_TILE);
                     tma_load_3d(t + OFF_V, &tmV, 0, kt * AK, z, &S.bv);
                     ++nv;
@@ -117,9 +135,10 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                 const uint64_t dl = global_timer_ns() + 1000000000ull;
                 while (!mbar_try_wait(&S.bq, 0) && global_timer_ns() < dl) {
                 }
-                if (nk > 0)
-                    while (!mbar_try_wait(&S.bk, (nk - 1) & 1u) && global_timer_ns() < dl) {
-                    }
+                for (int b = 0; b < 2; ++b)
+                    if (nk[b] > 0)
+                        while (!mbar_try_wait(&S.bk[b], (nk[b] - 1) & 1u) && global_timer_ns() < dl) {
+                        }
                 if (nv > 0)
                     while (!mbar_try_wait(&S.bv, (nv - 1) & 1u) && global_timer_ns() < dl) {
                     }
@@ -127,97 +146,112 @@ __global__ void __launch_bounds__(A_THREADS, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {  // MMAs
+            const uint32_t q = smem_u32(t + OFF_Q), p = smem_u32(t + OFF_P), vt = smem_u32(t + OFF_VT);
+            // O += P V^T of pass-2 step s, once the softmax warps wrote P and V^T
+            auto pv = [&](int s) -> bool {
+                const int j = s - ntiles;
+                if (!await_phase(S, &S.bpw, j & 1u, deadline, err)) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < AK / 16; ++kk) {
+                    const uint32_t off = (uint32_t)(kk >> 2) * HALF_TILE + (uint32_t)(kk & 3) * 32;
+                    tc_mma(tmem + TM_O, smem_desc_sw128(p + off), smem_desc_sw128(vt + off), kIdescA,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(&S.bo);
+                S.nbo_ = j + 1;
+                return true;
+            };
             bool ok = await_phase(S, &S.bq, 0, deadline, err);
-            const uint32_t q = smem_u32(t + OFF_Q), k = smem_u32(t + OFF_K), p = smem_u32(t + OFF_P),
-                           vt = smem_u32(t + OFF_VT);
-            for (int step = 0; ok && step < 2 * ntiles; ++step) {
-                const int j = step - ntiles;
-                if (!await_phase(S, &S.bk, step & 1u, deadline, err)) break;
-                // S in TMEM is free once the softmax warps have read the previous step's
-                if (step > 0 && !await_phase(S, &S.bp, (step - 1) & 1u, deadline, err)) break;
+            for (int step = 0; ok && step < nsteps; ++step) {
+                const int b = step & 1;
+                const uint32_t k = smem_u32(t + OFF_K + b * 2 * HALF_TILE);
+                ok = await_phase(S, &S.bk[b], (step >> 1) & 1u, deadline, err);
+                // S buffer b is free once the softmax warps read S of step - 2
+                if (ok && step >= 2) ok = await_phase(S, &S.bp[b], ((step - 2) >> 1) & 1u, deadline, err);
+                if (!ok) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < ADH / 16; ++kk) {
                     const uint32_t off = (uint32_t)(kk >> 2) * HALF_TILE + (uint32_t)(kk & 3) * 32;
-                    tc_mma(tmem, smem_desc_sw128(q + off), smem_desc_sw128(k + off), kIdescA, kk > 0);
+                    tc_mma(tmem + (uint32_t)b * AK, smem_desc_sw128(q + off), smem_desc_sw128(k + off), kIdescA,
+                           kk > 0);
                 }
-                tc_commit(&S.bs);
-                S.ns_ = step + 1;
-                if (j >= 0) {  // P and V^T of this step are written once the softmax warps arrive
-                    if (!await_phase(S, &S.bp, step & 1u, deadline, err)) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < AK / 16; ++kk) {
-                        const uint32_t off = (uint32_t)(kk >> 2) * HALF_TILE + (uint32_t)(kk & 3) * 32;
-                        tc_mma(tmem + 128, smem_desc_sw128(p + off), smem_desc_sw128(vt + off), kIdescA,
-                               (j > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    tc_commit(&S.bo);
-                    S.no_ = j + 1;
-                }
+                tc_commit(&S.bs[b]);
+                S.nbs_[b] = (step >> 1) + 1;
+                if (step >= 1 && step - 1 >= ntiles) ok = pv(step - 1);  // overlaps the softmax of this step
             }
+            if (ok) pv(nsteps - 1);
         }
     } else {  // softmax warps: warp w owns TMEM lanes (rows) 32 * (w % 4) .. + 31
         const int quarter = warp & 3, row = 32 * quarter + lane, st = threadIdx.x - 64;
         const int pos = a.p0 + i0 + row;
+        const int klo = a.window > 0 ? max(pos - a.window + 1, 0) : 0, khi = min(pos, hi);  // this row's keys
         const uint32_t trow = tmem + ((uint32_t)(32 * quarter) << 16);
-        float m = -INFINITY, l = 0.f;
+        const float sc2 = a.scale * kLog2e;  // scores in the log2 domain
+        float m2 = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int step = 0; step < 2 * ntiles; ++step) {
-            const int kt = kt0 + step % ntiles, j = step - ntiles;
-            ok = __all_sync(0xffffffffu, ok && await_phase(S, &S.bs, step & 1u, deadline, err));
+        for (int step = 0; step < nsteps; ++step) {
+            const int b = step & 1, kt = kt0 + step % ntiles, j = step - ntiles;
+            const int vlo = klo - kt * AK, vhi = khi - kt * AK;  // valid columns of the tile
+            ok = __all_sync(0xffffffffu, ok && await_phase(S, &S.bs[b], (step >> 1) & 1u, deadline, err));
             if (!ok) break;
             tc_fence_after();
+            const uint32_t sb = trow + (uint32_t)b * AK;
             if (j < 0) {  // pass 1: running max and sum of the row
 #pragma unroll 1
                 for (int c0 = 0; c0 < AK; c0 += 32) {
                     float v[32];
-                    tc_ld32(trow + (uint32_t)c0, v);
+                    tc_ld32(sb + (uint32_t)c0, v);
                     float mt = -INFINITY;
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const int key = kt * AK + c0 + i;
-                        const bool valid = key <= pos && key <= hi && (a.window == 0 || key > pos - a.window);
-                        v[i] = valid ? v[i] * a.scale : -INFINITY;
+                        const int col = c0 + i;
+                        v[i] = (col >= vlo && col <= vhi) ? v[i] * sc2 : -INFINITY;
                         mt = fmaxf(mt, v[i]);
                     }
                     if (mt != -INFINITY) {
-                        const float mn = fmaxf(m, mt);
+                        const float mn = fmaxf(m2, mt);
                         float sum = 0.f;
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) sum += (v[i] == -INFINITY) ? 0.f : expf(v[i] - mn);
-                        l = (m == -INFINITY ? 0.f : l * expf(m - mn)) + sum;
-                        m = mn;
+                        for (int i = 0; i < 32; ++i) sum += exp2f(v[i] - mn);  // exp2f(-inf) = 0
+                        l = (m2 == -INFINITY ? 0.f : l * exp2f(m2 - mn)) + sum;
+                        m2 = mn;
                     }
                 }
-            } else {  // pass 2: P into shared memory, V transposed next to it
+                tc_fence_before();
+                mbar_arrive(&S.bp[b]);
+            } else {  // pass 2: P of the row in registers, then into shared memory
+                uint4 pk[AK / 8];
+#pragma unroll
+                for (int c0 = 0; c0 < AK; c0 += 32) {
+                    float v[32];
+                    tc_ld32(sb + (uint32_t)c0, v);
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        __align__(16) __half hv[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int col = c0 + 8 * c8 + i;
+                            hv[i] = __float2half_rn((col >= vlo && col <= vhi) ? exp2f(v[8 * c8 + i] * sc2 - m2) : 0.f);
+                        }
+                        pk[c0 / 8 + c8] = *reinterpret_cast<const uint4 *>(hv);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&S.bp[b]);  // S buffer b may be recomputed
                 if (j > 0) {  // the previous P.V MMAs must have read P and V^T
                     ok = __all_sync(0xffffffffu, await_phase(S, &S.bo, (j - 1) & 1u, deadline, err));
                     if (!ok) break;
                 }
-#pragma unroll 1
-                for (int c0 = 0; c0 < AK; c0 += 32) {
-                    float v[32];
-                    tc_ld32(trow + (uint32_t)c0, v);
 #pragma unroll
-                    for (int c8 = 0; c8 < 32; c8 += 8) {
-                        __align__(16) __half hv[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const int key = kt * AK + c0 + c8 + i;
-                            const bool valid = key <= pos && key <= hi && (a.window == 0 || key > pos - a.window);
-                            hv[i] = __float2half_rn(valid ? expf(v[c8 + i] * a.scale - m) : 0.f);
-                        }
-                        const int col = c0 + c8;  // key within the tile
-                        *reinterpret_cast<uint4 *>(t + OFF_P + (col >> 6) * HALF_TILE + sw128_offset(row, col & 63)) =
-                            *reinterpret_cast<const uint4 *>(hv);
-                    }
-                }
+                for (int c = 0; c < AK / 8; ++c)
+                    *reinterpret_cast<uint4 *>(t + OFF_P + (c >> 3) * HALF_TILE + sw128_offset(row, (8 * c) & 63)) = pk[c];
                 ok = __all_sync(0xffffffffu, await_phase(S, &S.bv, j & 1u, deadline, err));
                 if (!ok) break;
                 // V^T row d = st: 8 keys at a time, gathered from the staged [key][d] tile
                 const __half *vst = reinterpret_cast<const __half *>(t + OFF_V);
-#pragma unroll 1
+#pragma unroll 2
                 for (int c = 0; c < AK / 8; ++c) {
                     __align__(16) __half hv[8];
 #pragma unroll
@@ -226,9 +260,9 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                         *reinterpret_cast<const uint4 *>(hv);
                 }
                 fence_proxy_async_shared();  // the tensor core reads what these threads wrote
+                tc_fence_before();
+                mbar_arrive(&S.bpw);
             }
-            tc_fence_before();
-            mbar_arrive(&S.bp);
         }
         // epilogue: O / l of this row
         if (ok) ok = __all_sync(0xffffffffu, await_phase(S, &S.bo, (ntiles - 1) & 1u, deadline, err));
@@ -238,7 +272,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
 #pragma unroll 1
             for (int c0 = 0; c0 < ADH; c0 += 32) {
                 float v[32];
-                tc_ld32(trow + 128u + (uint32_t)c0, v);
+                tc_ld32(trow + TM_O + (uint32_t)c0, v);
                 if (row < rows) {
                     __half *dst = a.o + (size_t)(i0 + row) * a.ld_o + (size_t)h * ADH + c0;
 #pragma unroll
@@ -255,13 +289,14 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
-        if (S.abort_ && lane == 0) {  // MMAs may still run: wait (bounded) for their commits
+        if (S.abort_ && lane == 0) {  // MMAs may still run: wait (bounded) for their last commits
             const uint64_t dl = global_timer_ns() + 1000000000ull;
-            if (S.ns_ > 0)
-                while (!mbar_try_wait(&S.bs, (S.ns_ - 1) & 1u) && global_timer_ns() < dl) {
-                }
-            if (S.no_ > 0)
-                while (!mbar_try_wait(&S.bo, (S.no_ - 1) & 1u) && global_timer_ns() < dl) {
+            for (int b = 0; b < 2; ++b)
+                if (S.nbs_[b] > 0)
+                    while (!mbar_try_wait(&S.bs[b], (S.nbs_[b] - 1) & 1u) && global_timer_ns() < dl) {
+                    }
+            if (S.nbo_ > 0)
+                while (!mbar_try_wait(&S.bo, (S.nbo_ - 1) & 1u) && global_timer_ns() < dl) {
                 }
         }
         __syncwarp();
