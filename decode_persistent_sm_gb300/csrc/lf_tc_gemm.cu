@@ -3,13 +3,13 @@
 // A holds the activations of M positions, B a weight matrix in its natural
 // [out][in] layout, so both operands are K-major.
 //
-// One CTA computes one 128 x 256 tile of C: a copy warp streams 128 x 64 and
-// 256 x 64 tiles of A and B into a 4-stage shared-memory ring with TMA
-// (128-byte swizzle), one elected thread of the MMA warp issues
-// tcgen05.mma (kind::f16, fp32 accumulators in 256 TMEM columns) and
-// releases each stage with tcgen05.commit, and four epilogue warps read the
-// accumulators back with tcgen05.ld (each warp its 32 TMEM lanes = rows) and
-// store them.  Every wait is bounded: on a timeout the CTA records an error,
+// A persistent CTA per SM walks 128 x 256 tiles of C in a grouped order: a
+// copy warp streams 128 x 64 and 256 x 64 tiles of A and B into a 4-stage
+// shared-memory ring with TMA (128-byte swizzle), one elected thread of the
+// MMA warp issues tcgen05.mma (kind::f16, fp32 accumulators in one of two
+// 256-column TMEM buffers) and releases each stage with tcgen05.commit, and
+// four epilogue warps read a finished accumulator back with tcgen05.ld (each
+// warp its 32 TMEM lanes = rows) and store it while the next tile's MMAs run.  Every wait is bounded: on a timeout the CTA records an error,
 // lets its copies and MMAs in flight finish (bounded), frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -27,13 +27,16 @@ constexpr int BM = 128, BN = 256, BK = 64;  // BK fp16 = 128 bytes = one swizzle
 constexpr int TG_STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TG_THREADS = 192;  // warp 0 copies, warp 1 MMA + TMEM owner, warps 2-5 epilogue
-constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t TMEM_COLS = 512;  // two 256-column accumulators
+constexpr int GROUP_M = 8;  // tile order: 8 M-tiles share each B tile while it is in L2
 constexpr size_t TG_SMEM = (size_t)TG_STAGES * STAGE_BYTES + 1024 + 256;
 
 struct TgShared {
-    uint64_t full[TG_STAGES], empty[TG_STAGES], accum;
+    uint64_t full[TG_STAGES], empty[TG_STAGES];  // stage ring
+    uint64_t acc_full[2], acc_empty[2];           // accumulator b computed / read back (128 arrivals)
     uint32_t tmem_base;
     volatile int abort_;
+    volatile int n_acc_[2];  // commits issued on acc_full[b] (for the drain after an error)
 };
 
 constexpr uint32_t kIdesc = idesc_f16(BM, BN);
@@ -52,6 +55,17 @@ __device__ __forceinline__ bool wait_phase(TgShared &S, uint64_t *bar, uint32_t 
     return true;
 }
 
+// Tile t of the grouped order: groups of GROUP_M M-tiles walk every N-tile.
+__device__ __forceinline__ void tile_of(int t, int mt, int nt, int &m, int &n) {
+    const int per_group = GROUP_M * nt, group = t / per_group, first = group * GROUP_M;
+    const int gm = min(GROUP_M, mt - first), r = t - group * per_group;
+    m = first + r % gm;
+    n = r / gm;
+}
+
+// Persistent: CTA c computes tiles c, c + gridDim.x, ...; the stage ring and
+// the two TMEM accumulators run across tiles, so copies and MMAs of one tile
+// overlap the epilogue of the previous one.
 __global__ void __launch_bounds__(TG_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, float *C,
                    int M, int N, int K, int ldc, uint32_t *err, unsigned long long timeout_ns) {
@@ -59,7 +73,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
     uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(tg_raw) + 1023) & ~uintptr_t(1023));
     TgShared &S = *reinterpret_cast<TgShared *>(tiles + (size_t)TG_STAGES * STAGE_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN, nk = K / BK;
+    const int mt = (M + BM - 1) / BM, nt = (N + BN - 1) / BN, ntiles = mt * nt, nk = K / BK;
     const uint64_t deadline = global_timer_ns() + timeout_ns;
 
     if (threadIdx.x == 0) {
@@ -67,15 +81,17 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
             mbar_init(&S.full[s], 1);
             mbar_init(&S.empty[s], 1);
         }
-        mbar_init(&S.accum, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&S.acc_full[b], 1);
+            mbar_init(&S.acc_empty[b], 128);
+            S.n_acc_[b] = 0;
+        }
         S.abort_ = 0;
         fence_barrier_init();
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
     }
-    if (warp == 1) {
-        tc_alloc(&S.tmem_base, TMEM_COLS);
-    }
+    if (warp == 1) tc_alloc(&S.tmem_base, TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -83,49 +99,72 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0) {  // copies
-            int issued = 0;
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % TG_STAGES;
-                if (kb >= TG_STAGES && !wait_phase(S, &S.empty[s], ((kb / TG_STAGES) - 1) & 1u, deadline, err))
-                    break;
-                uint8_t *a = tiles + (size_t)s * STAGE_BYTES;
-                mbar_arrive_expect_tx(&S.full[s], STAGE_BYTES);
-                tma_load_2d(a, &tmA, kb * BK, m0, &S.full[s]);
-                tma_load_2d(a + A_BYTES, &tmB, kb * BK, n0, &S.full[s]);
-                ++issued;
+            int kbg = 0;  // k-blocks issued so far (all tiles)
+            for (int t = blockIdx.x; t < ntiles && !S.abort_; t += gridDim.x) {
+                int m, n;
+                tile_of(t, mt, nt, m, n);
+                for (int kb = 0; kb < nk; ++kb, ++kbg) {
+                    const int s = kbg % TG_STAGES;
+                    if (kbg >= TG_STAGES &&
+                        !wait_phase(S, &S.empty[s], ((kbg / TG_STAGES) - 1) & 1u, deadline, err))
+                        break;
+                    uint8_t *a = tiles + (size_t)s * STAGE_BYTES;
+                    mbar_arrive_expect_tx(&S.full[s], STAGE_BYTES);
+                    tma_load_2d(a, &tmA, kb * BK, m * BM, &S.full[s]);
+                    tma_load_2d(a + A_BYTES, &tmB, kb * BK, n * BN, &S.full[s]);
+                }
             }
             if (S.abort_) {  // let the copies in flight land before the CTA exits
                 const uint64_t dl = global_timer_ns() + 1000000000ull;
-                for (int kb = (issued > TG_STAGES ? issued - TG_STAGES : 0); kb < issued; ++kb)
-                    while (!mbar_try_wait(&S.full[kb % TG_STAGES], (kb / TG_STAGES) & 1u) && global_timer_ns() < dl) {
+                for (int k = (kbg > TG_STAGES ? kbg - TG_STAGES : 0); k < kbg; ++k)
+                    while (!mbar_try_wait(&S.full[k % TG_STAGES], (k / TG_STAGES) & 1u) && global_timer_ns() < dl) {
                     }
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {  // MMA issue
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % TG_STAGES;
-                if (!wait_phase(S, &S.full[s], (kb / TG_STAGES) & 1u, deadline, err)) break;
+            int kbg = 0, lt = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++lt) {
+                const int b = lt & 1;
+                const uint32_t acc = tmem + (uint32_t)b * BN;
+                // accumulator b is free once the epilogue read tile lt - 2 out of it
+                if (lt >= 2 && !wait_phase(S, &S.acc_empty[b], ((lt >> 1) - 1) & 1u, deadline, err)) break;
                 tc_fence_after();
-                const uint32_t a = smem_u32(tiles + (size_t)s * STAGE_BYTES), b = a + A_BYTES;
+                for (int kb = 0; kb < nk; ++kb, ++kbg) {
+                    const int s = kbg % TG_STAGES;
+                    if (!wait_phase(S, &S.full[s], (kbg / TG_STAGES) & 1u, deadline, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a = smem_u32(tiles + (size_t)s * STAGE_BYTES), bb = a + A_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk)  // 16 fp16 = 32 bytes along K per instruction
-                    tc_mma(tmem, smem_desc_sw128(a + 32 * kk), smem_desc_sw128(b + 32 * kk), kIdesc, (kb | kk) != 0);
-                tc_commit(&S.empty[s]);  // the stage is free once these MMAs have read it
+                    for (int kk = 0; kk < BK / 16; ++kk)  // 16 fp16 = 32 bytes along K per instruction
+                        tc_mma(acc, smem_desc_sw128(a + 32 * kk), smem_desc_sw128(bb + 32 * kk), kIdesc,
+                               (kb | kk) != 0);
+                    tc_commit(&S.empty[s]);  // the stage is free once these MMAs have read it
+                }
+                tc_commit(&S.acc_full[b]);  // all MMAs of the tile are complete when this arrives
+                S.n_acc_[b] = (lt >> 1) + 1;
             }
-            tc_commit(&S.accum);  // all MMAs issued above are complete when this arrives
         }
     } else {  // epilogue: warp w reads TMEM lanes 32 * (w % 4) .. + 31
-        const int q = warp & 3, row = m0 + 32 * q + lane;
-        // warp-uniform: tcgen05.ld is executed by whole warps
-        const bool ok = __all_sync(0xffffffffu, wait_phase(S, &S.accum, 0, deadline, err));
-        tc_fence_after();
-        if (ok) {
+        const int q = warp & 3;
+        int lt = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
+            int m, n;
+            tile_of(t, mt, nt, m, n);
+            const int b = lt & 1, row = m * BM + 32 * q + lane;
+            // warp-uniform: tcgen05.ld is executed by whole warps
+            const bool ok = __all_sync(0xffffffffu, wait_phase(S, &S.acc_full[b], (lt >> 1) & 1u, deadline, err));
+            if (!ok) break;
+            tc_fence_after();
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 float v[32];
-                tc_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
-                const int col = n0 + c0;
+                tc_ld32(tmem + (uint32_t)b * BN + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
+                const int col = n * BN + c0;
                 if (row < M && col < N) {
                     float *dst = C + (size_t)row * ldc + col;
                     if (col + 32 <= N && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
@@ -133,19 +172,25 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                         for (int i = 0; i < 32; i += 4)
                             *reinterpret_cast<float4 *>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
                     } else {
-                        for (int i = 0; i < 32 && col + i < N; ++i) dst[i] = v[i];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (col + i < N) dst[i] = v[i];
                     }
                 }
             }
+            tc_fence_before();
+            mbar_arrive(&S.acc_empty[b]);
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
-        if (S.abort_ && lane == 0) {  // MMAs may still run: wait (bounded) for the last commit
+        if (S.abort_ && lane == 0) {  // MMAs may still run: wait (bounded) for their last commits
             const uint64_t dl = global_timer_ns() + 1000000000ull;
-            while (!mbar_try_wait(&S.accum, 0) && global_timer_ns() < dl) {
-            }
+            for (int b = 0; b < 2; ++b)
+                if (S.n_acc_[b] > 0)
+                    while (!mbar_try_wait(&S.acc_full[b], (S.n_acc_[b] - 1) & 1u) && global_timer_ns() < dl) {
+                    }
         }
         __syncwarp();
         tc_fence_after();
@@ -201,8 +246,16 @@ lf_status tc_gemm_f16(const __half *A, const __half *B, float *C, int M, int N, 
         attr_err = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TG_SMEM);
     });
     if (attr_err != cudaSuccess) return LF_ERR_CUDA;
-    const dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
-    tc_gemm_kernel<<<grid, TG_THREADS, TG_SMEM, stream>>>(ma, mb, C, M, N, K, ldc, err, timeout_ns);
+    static int n_sm = 0;
+    if (n_sm == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1)
+            return LF_ERR_CUDA;
+    }
+    const int ntiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    tc_gemm_kernel<<<ntiles < n_sm ? ntiles : n_sm, TG_THREADS, TG_SMEM, stream>>>(ma, mb, C, M, N, K, ldc, err,
+                                                                                 timeout_ns);
     return cudaGetLastError() == cudaSuccess ? LF_OK : LF_ERR_CUDA;
 }
 
