@@ -12,8 +12,10 @@
 //
 // One CTA of 1024 threads: the probabilities live in shared memory; tau is
 // found by bisection on the fp32 bit pattern (the mass above a threshold only
-// changes at the p values, and positive floats order like their bits); the
-// crossing is found with a block scan over contiguous index chunks.
+// changes at the p values, and positive floats order like their bits), each
+// step one pass over the vocabulary and a block sum by a fixed tree (the same
+// order every time); the crossing is found by the warp that owns it, walking
+// its contiguous index range 32 tokens at a time with a warp scan.
 #include <cuda_runtime.h>
 
 #include <cfloat>
@@ -44,18 +46,7 @@ __device__ __forceinline__ void philox4x32_10(uint32_t c[4], uint32_t k0, uint32
     }
 }
 
-// Block-wide reductions; every thread gets the result.
-__device__ float bsum(float v, float *red) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    float t = 0.f;
-#pragma unroll 1
-    for (int w = 0; w < SMP_THREADS / 32; ++w) t += red[w];
-    return t;
-}
+// Block-wide maximum; every thread gets the result.
 __device__ float bmax(float v, float *red) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -68,15 +59,33 @@ __device__ float bmax(float v, float *red) {
     return t;
 }
 
+// Block-wide sum by a fixed tree (warp shuffles, then warp 0 over the warp
+// partials): the same order every time; every thread gets the result.
+__device__ float bsum(float v, float *red, float *bcast) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float t = red[threadIdx.x];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (threadIdx.x == 0) *bcast = t;
+    }
+    __syncthreads();
+    return *bcast;
+}
+
 __global__ void __launch_bounds__(SMP_THREADS, 1)
     sample_kernel(const float *__restrict__ logits, int V, float temperature, float top_p, uint32_t key0,
                   uint32_t key1, uint32_t position, uint32_t sample, int *__restrict__ out) {
     extern __shared__ float pv[];  // [V] unnormalised probabilities
     __shared__ float red[SMP_THREADS / 32];
-    __shared__ float wsum[SMP_THREADS / 32];
+    __shared__ float wtot[SMP_THREADS / 32];
+    __shared__ float bc[2];
     __shared__ int tok;
     __shared__ float u_sh;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     if (tid == 0) tok = INT_MAX;
 
     if (temperature <= 0.f) {  // greedy
@@ -101,64 +110,77 @@ __global__ void __launch_bounds__(SMP_THREADS, 1)
         pv[i] = p;
         z += p;
     }
-    const float total = bsum(z, red);
-    const float target = top_p * total;
+    const float target = top_p * bsum(z, red, &bc[0]);
     // largest bit pattern b with mass(b) >= target; mass(0) = total >= target
     uint32_t lo = 0, hi = __float_as_uint(1.0f);
-    float kept = total;
+    float kept = 0.f;
+    bool have = false;
     while (lo < hi) {
         const uint32_t mid = lo + (hi - lo + 1) / 2;
         float s = 0.f;
-        for (int i = tid; i < V; i += SMP_THREADS)
-            if (__float_as_uint(pv[i]) >= mid) s += pv[i];
-        const float mass = bsum(s, red);
+        for (int i = tid; i < V; i += SMP_THREADS) {
+            const float p = pv[i];
+            s += __float_as_uint(p) >= mid ? p : 0.f;
+        }
+        const float mass = bsum(s, red, &bc[(lo ^ hi) & 1]);
         if (mass >= target) {
             lo = mid;
             kept = mass;
+            have = true;
         } else {
             hi = mid - 1;
         }
+    }
+    if (!have) {  // lo never moved: every token is kept
+        float s = 0.f;
+        for (int i = tid; i < V; i += SMP_THREADS) s += pv[i];
+        kept = bsum(s, red, &bc[0]);
     }
     if (tid == 0) {
         uint32_t c[4] = {position, sample, 0u, 0u};
         philox4x32_10(c, key0, key1);
         u_sh = (float)(c[0] >> 8) * (1.0f / 16777216.0f);
     }
+    // warp w owns the contiguous index range [w R, (w + 1) R): its kept mass,
+    // an exclusive scan over the warps, then the owning warp walks its range
+    const int R = (V + SMP_THREADS / 32 - 1) / (SMP_THREADS / 32), r0 = w * R, r1 = min(V, r0 + R);
+    float ws = 0.f;
+    for (int i = r0 + lane; i < r1; i += 32) {
+        const float p = pv[i];
+        ws += __float_as_uint(p) >= lo ? p : 0.f;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+    if (lane == 0) wtot[w] = ws;
     __syncthreads();
     const float t = u_sh * kept;
-    // contiguous chunks in index order, exclusive scan of their kept mass
-    const int chunk = (V + SMP_THREADS - 1) / SMP_THREADS, b0 = tid * chunk, b1 = min(V, b0 + chunk);
-    float s = 0.f;
-    for (int i = b0; i < b1; ++i)
-        if (__float_as_uint(pv[i]) >= lo) s += pv[i];
-    float inc = s;
-    const int lane = tid & 31, w = tid >> 5;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += y;
-    }
-    if (lane == 31) wsum[w] = inc;
-    __syncthreads();
     float before = 0.f;
-    for (int k = 0; k < w; ++k) before += wsum[k];
-    const float excl = before + inc - s;
-    if (s > 0.f && excl <= t && t < excl + s) {
-        float run = excl;
-        for (int i = b0; i < b1; ++i) {
-            if (__float_as_uint(pv[i]) < lo) continue;
-            run += pv[i];
-            if (run > t) {
-                atomicMin(&tok, i);
+    for (int k = 0; k < w; ++k) before += wtot[k];
+    if (ws > 0.f && before <= t && t < before + ws) {
+        float run = before;
+        for (int i0 = r0; i0 < r1; i0 += 32) {
+            const int i = i0 + lane;
+            const float p = i < r1 ? pv[i] : 0.f;
+            float inc = __float_as_uint(p) >= lo && i < r1 ? p : 0.f;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += y;
+            }
+            const unsigned int hit = __ballot_sync(0xffffffffu, inc > 0.f && run + inc > t &&
+                                                                  __float_as_uint(p) >= lo && p > 0.f);
+            if (hit) {
+                if (lane == __ffs(hit) - 1) tok = i;
                 break;
             }
+            run += __shfl_sync(0xffffffffu, inc, 31);
         }
     }
     __syncthreads();
     if (tok == INT_MAX) {  // rounding put t at or past the scanned total: the last kept index
         int last = -1;
-        for (int i = b0; i < b1; ++i)
-            if (__float_as_uint(pv[i]) >= lo) last = i;
+        for (int i = tid; i < V; i += SMP_THREADS)
+            if (__float_as_uint(pv[i]) >= lo && pv[i] > 0.f) last = max(last, i);
         const float lm = bmax((float)last, red);
         if (tid == 0) tok = (int)lm;
         __syncthreads();
