@@ -9,7 +9,7 @@ delayed lane sum, LM head, argmax); the position is set back to 512 before
 every step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-  python bench.py --workload e2e|long|sweep|prefill|passn   # further workloads, one line each
+  python bench.py --workload e2e|long|sweep|prefill|passn|passn_batch|batch   # further workloads, one line each
 
 Under torchrun (N > 1) every rank decodes its own replica on its own GPU (the
 path needs no exchange between GPUs); rank 0 prints one JSON line.
@@ -409,6 +409,7 @@ GEN_WORKLOADS = {
 SWEEP_CTX, SWEEP_STEPS = 2048, 256
 PREFILL_N = 3584
 PASSN = (128, 8, 256, 0.8, 0.95)  # prompt, samples, tokens per sample, temperature, top_p
+BATCH_SWEEP = (512, 64, (1, 2, 4, 8, 16))  # KV fill, greedy steps per batch size, batch sizes
 
 
 def timed_generation(eng, stream, first_token: int, n: int):
@@ -436,8 +437,11 @@ def latency_summary(per_ms):
             "max_ms": float(a[-1]), "mean_ms": float(a.mean())}
 
 
-def gen_roofline(shape, pos0: int, n: int, ms_per_step: float):
-    nbytes = sum(algorithmic_bytes(shape, p) for p in range(pos0, pos0 + n)) / n
+def gen_roofline(shape, pos0: int, n: int, ms_per_step: float, batch: int = 1):
+    """Roofline of n steps from pos0 at ms_per_step; a batch of B samples
+    streams the weights once per step and reads B live KV caches."""
+    kv = lambda p: algorithmic_bytes(shape, p) - algorithmic_bytes(shape, -1)
+    nbytes = sum(algorithmic_bytes(shape, p) + (batch - 1) * kv(p) for p in range(pos0, pos0 + n)) / n
     peak, peak_kind = peak_hbm()
     achieved = nbytes / (ms_per_step / 1e3) / 1e9
     return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -626,6 +630,102 @@ def run_generation(args, world, rank, local):
             torch.distributed.destroy_process_group()
         return
 
+    if args.workload == "passn_batch":
+        n_prompt, n_samp, n_tok, temp, top_p = PASSN
+        shape = base
+        prompt = synth.make_tokens(SEED + rank, n_prompt, shape.vocab)
+        with Engine.from_shape(shape) as eng:
+            eng.set_stream(stream.cuda_stream)
+            eng.load_weights(blob)
+            eng.prefill_batched(prompt[:-1], logits=False)
+            eng.batch_begin(n_samp)
+            eng.batch_generate([int(prompt[-1])] * n_samp, max(args.warmup, 3), temp, top_p, SEED + 999)
+            clocks = ClockSampler(local)
+            clocks.start()
+            eng.batch_begin(n_samp)  # back to the prompt's end
+            if world > 1:
+                torch.distributed.barrier()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            toks = eng.batch_generate([int(prompt[-1])] * n_samp, n_tok, temp, top_p, SEED)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            clk = clocks.stop()
+            total = worst(e0.elapsed_time(e1))
+        ms = total / n_tok  # one batch step: every sample advances one token
+        distinct = len({tuple(o) for o in toks})
+        if rank == 0:
+            rate = world * n_samp * n_tok / (total / 1e3)
+            line = {"metric": "sampled decode tokens/s for pass@N, N samples decoded as one batch (2.3B lane model, "
+                              "FP16)",
+                    "value": rate, "steps": n_tok, "warmup": max(args.warmup, 3), "ms_per_step": ms, "data": data,
+                    "config": {"workload": f"pass@{n_samp}: prompt of {n_prompt} random ids (batched prefill), then "
+                                           f"{n_samp} samples of {n_tok} tokens decoded together (lf_batch_generate: "
+                                           f"one weight stream per step for all samples), temperature {temp}, "
+                                           f"top-p {top_p}", "batch": n_samp, "seed": SEED,
+                               "l2": "no flush: inputs larger than L2"},
+                    "distinct_samples": distinct,
+                    "roofline": gen_roofline(shape, n_prompt - 1, n_tok, ms, batch=n_samp), "cpu_baseline": None,
+                    "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 4 * n_samp / n_tok,
+                            "d2h_bytes_per_step": 4 * n_samp + 4 / n_tok,
+                            "call": "lf_batch_generate (first tokens in, all tokens and the status word out once)"},
+                    "gpu_launches": n_tok * (7 * shape.n_layers + 6), "clocks": clk, **common}
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    if args.workload == "batch":
+        fill, n_tok, sizes = BATCH_SWEEP
+        shape = base
+        kv = synth.make_kv(shape, SEED, fill)
+        first = synth.make_tokens(SEED + rank, 16, shape.vocab)
+        variants = {}
+        clocks = ClockSampler(local)
+        clocks.start()
+        with Engine.from_shape(shape) as eng:
+            eng.set_stream(stream.cuda_stream)
+            eng.load_weights(blob)
+            eng.load_kv(kv, fill)
+            for B in sizes:
+                eng.batch_begin(B)
+                eng.batch_generate([int(t) for t in first[:B]], max(args.warmup, 3), 0.0, 1.0, 0)
+                eng.batch_begin(B)
+                if world > 1:
+                    torch.distributed.barrier()
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                eng.batch_generate([int(t) for t in first[:B]], n_tok, 0.0, 1.0, 0)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                total = worst(e0.elapsed_time(e1))
+                ms = total / n_tok
+                variants[f"B{B}"] = {"value": world * B * n_tok / (total / 1e3), "ms_per_step": ms,
+                                     "roofline_frac": gen_roofline(shape, fill, n_tok, ms, batch=B)["frac"]}
+            eng.batch_end()
+        clk = clocks.stop()
+        main_v = variants["B8"]
+        if rank == 0:
+            line = {"metric": "batched greedy decode tokens/s (all samples) per batch size", "value": main_v["value"],
+                    "steps": n_tok, "warmup": max(args.warmup, 3), "ms_per_step": main_v["ms_per_step"],
+                    "data": data + ", N(0,1) KV fill",
+                    "config": {"workload": f"batched decode: KV pre-filled N(0,1) to {fill} and shared by every "
+                                           f"sample, then {n_tok} greedy steps of B samples together "
+                                           f"(lf_batch_generate) for B in {list(sizes)}; value at B = 8",
+                               "seed": SEED, "l2": "no flush: inputs larger than L2"},
+                    "variants": variants,
+                    "roofline": gen_roofline(shape, fill, n_tok, main_v["ms_per_step"], batch=8),
+                    "cpu_baseline": None, "e2e": None,
+                    "gpu_launches": len(sizes) * n_tok * (7 * shape.n_layers + 6), "clocks": clk, **common}
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
     if args.workload == "sweep":
         variants = {}
         kv = synth.make_kv(base, SEED, SWEEP_CTX)
@@ -744,7 +844,8 @@ def main():
     ap.add_argument("--trace", default="", help="write a one-step op trace (JSON) to this path")
     ap.add_argument("--position", type=int, default=POS,
                     help="step workload: decode position (KV pre-filled up to it); 512 is the default line")
-    ap.add_argument("--workload", choices=["step", "e2e", "long", "sweep", "prefill", "passn", "gemm"],
+    ap.add_argument("--workload", choices=["step", "e2e", "long", "sweep", "prefill", "passn", "passn_batch", "batch",
+                                           "gemm"],
                     default="step",
                     help="step: the single-step microbench (default line); e2e / long / sweep: the "
                          "generation workloads")

@@ -54,6 +54,12 @@ _SIGS = {
     "lf_debug_trace": (_ci, [_vp, _ci]),
     "lf_set_l2_prefetch": (_ci, [_vp, ctypes.c_uint32, ctypes.c_uint32]),
     "lf_debug_read_trace": (_ci, [_vp, _vp, ctypes.c_size_t, _vp]),
+    "lf_batch_begin": (_ci, [_vp, _ci]),
+    "lf_batch_end": (_ci, [_vp]),
+    "lf_batch_info": (_ci, [_vp, ctypes.POINTER(_ci), ctypes.POINTER(_ci)]),
+    "lf_batch_step": (_ci, [_vp, _vp, _vp, _vp]),
+    "lf_batch_generate": (_ci, [_vp, _vp, _ci, ctypes.c_float, ctypes.c_float, ctypes.c_uint64, _vp]),
+    "lf_gemv_f16": (_ci, [_vp, _vp, _vp, _ci, _ci, _ci, _vp]),
 }
 
 
@@ -121,6 +127,13 @@ def matmul_f16(a_ptr: int, b_ptr: int, c_ptr: int, m: int, n: int, k: int, strea
     FP16 a, b row-major, fp32 c); waits for the stream."""
     lib = load_library()
     _check("lf_matmul_f16", lib.lf_matmul_f16(a_ptr, b_ptr, c_ptr, int(m), int(n), int(k), stream))
+
+
+def gemv_f16(w_ptr: int, x_ptr: int, y_ptr: int, n: int, k: int, batch: int, stream: Optional[int] = None):
+    """y[b][n] = w[n][k] . x[b][k] for b < batch (1..16) on the tensor cores
+    (device pointers: FP16 w, x row-major, fp32 y); waits for the stream."""
+    lib = load_library()
+    _check("lf_gemv_f16", lib.lf_gemv_f16(w_ptr, x_ptr, y_ptr, int(n), int(k), int(batch), stream))
 
 
 def sample_token(logits_ptr: int, vocab: int, temperature: float, top_p: float, seed: int, position: int,
@@ -221,6 +234,40 @@ class Engine:
                                            out.ctypes.data if logits else None)
         _check("lf_generate_sampled", rc)
         return toks, out
+
+    def batch_begin(self, n_batch: int):
+        """lf_batch_begin: n_batch samples continue the current sequence
+        together (each with a copy of its KV cache so far)."""
+        _check("lf_batch_begin", self._lib.lf_batch_begin(self._h, int(n_batch)))
+
+    def batch_end(self):
+        _check("lf_batch_end", self._lib.lf_batch_end(self._h))
+
+    def batch_info(self):
+        """(n_batch, batch position); (0, 0) without a batch."""
+        nb, pos = ctypes.c_int(0), ctypes.c_int(0)
+        _check("lf_batch_info", self._lib.lf_batch_info(self._h, ctypes.byref(nb), ctypes.byref(pos)))
+        return nb.value, pos.value
+
+    def batch_step(self, tokens: Sequence[int], logits: bool = True):
+        """lf_batch_step: one step of every sample; returns (logits [B][vocab]
+        or None, argmax [B])."""
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        am = np.full(t.size, -1, dtype=np.int32)
+        out = np.empty((t.size, self.vocab), dtype=np.float32) if logits else None
+        rc = self._lib.lf_batch_step(self._h, t.ctypes.data, out.ctypes.data if logits else None, am.ctypes.data)
+        _check("lf_batch_step", rc)
+        return out, am
+
+    def batch_generate(self, first_tokens: Sequence[int], n: int, temperature: float, top_p: float, seed: int):
+        """lf_batch_generate: n sampled steps of every sample (sample b draws
+        from Philox stream (seed, position, b)); returns tokens [B][n]."""
+        t = np.ascontiguousarray(np.asarray(first_tokens, dtype=np.int32))
+        out = np.zeros((t.size, int(n)), dtype=np.int32)
+        rc = self._lib.lf_batch_generate(self._h, t.ctypes.data, int(n), float(temperature), float(top_p),
+                                         int(seed) & (2 ** 64 - 1), out.ctypes.data)
+        _check("lf_batch_generate", rc)
+        return out
 
     def decode_step_chained(self, token_device_ptr: int, argmax_device_ptr: int):
         """Enqueues one step whose token is read from, and whose argmax goes to,

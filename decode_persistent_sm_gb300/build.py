@@ -19,8 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblaneformer.so")
 SOURCES = ["lf_plan.cpp", "lf_kernel.cu", "lf_runtime.cu", "lf_noalloc.cu", "lf_tc_gemm.cu", "lf_prefill.cu",
-           "lf_pf_attn_tc.cu",
-           "lf_sample.cu"]
+           "lf_pf_attn_tc.cu", "lf_sample.cu", "lf_gemv_tc.cu", "lf_batch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,0 +1,566 @@
+// Batched decode: B independent samples (1..16) of the same model advance
+// one position per step together, so each weight byte streamed from HBM
+// serves all of them (pass@N: N continuations of one prompt).
+//
+// Each sample computes exactly the single-sequence forward under the delayed
+// lane sum (DTP-A): x(s) = e + sum_{u <= s-1-2d} P_u, the drained partials
+// added before the final norm.  That function does not depend on how the
+// partials are split over lanes (lanes are a partition of the same dense
+// weights), so the batch computes each P_u whole; only the fp32 summation
+// order differs from the lane-ordered sum.  The own-lane reading, whose value
+// does depend on the lanes, is not offered here.
+//
+// One step, for all samples at once: embedding; per sub-block the delayed
+// add fused with the RMSNorm, then the tensor-core GEMVs of lf_gemv_tc.cu
+// (QKV with RoPE and the KV append in its epilogue, the gate/up projection
+// with SwiGLU in its epilogue, o_proj and down writing the partial ring) and,
+// for attention, a split-key kernel whose last CTA per (sample, KV head)
+// merges the splits in split order; drain + final norm; LM head; argmax.
+// The step is captured once as a CUDA graph; the kernels read the position
+// from a device word, so the same graph serves every step.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cfloat>
+#include <climits>
+#include <cmath>
+#include <mutex>
+#include <vector>
+
+#include "laneformer.h"
+#include "lf_engine.h"
+#include "lf_gemv_tc.h"
+#include "lf_rows.cuh"
+#include "lf_sample.h"
+
+namespace lf {
+
+constexpr int kBatchAttnSplits = 16;  // key splits per (sample, KV head)
+constexpr int kBatchAttnThreads = 128;
+constexpr unsigned long long kBatchTimeoutNs = 2000000000ull;
+
+struct BatchState {
+    int B = 0, pos = 0;
+    bool ready = false;
+    void *mem = nullptr;
+    size_t bytes = 0;
+    cudaStream_t cap = nullptr;
+    cudaGraphExec_t graph = nullptr;
+    // device buffers (carved from mem)
+    int *tok = nullptr, *gen = nullptr, *am = nullptr, *d_pos = nullptr;
+    int2 *kvsrc = nullptr;  // per KV head: (lane, head within the lane) of the engine cache that holds it
+    uint32_t *err = nullptr, *cnt = nullptr, *att_cnt = nullptr;
+    float *x = nullptr, *ring = nullptr, *q = nullptr, *logits = nullptr, *ws = nullptr, *att_ws = nullptr;
+    __half *h16 = nullptr, *o16 = nullptr, *u16 = nullptr, *kc = nullptr, *vc = nullptr;
+    size_t ws_floats = 0;
+    int n_cnt = 0;
+};
+
+}  // namespace lf
+
+namespace {
+
+using lf::BatchState;
+using lf::kBatchAttnThreads;
+using lf::kBatchTimeoutNs;
+
+// x[b] = E[tok[b]] (fp32); a token outside the vocabulary sets error code 6.
+__global__ void ba_embed(const __half *__restrict__ emb, const int *__restrict__ tok, float *__restrict__ x, int D,
+                         int V, uint32_t *err) {
+    const int t = tok[blockIdx.x];
+    if (t < 0 || t >= V) {
+        if (threadIdx.x == 0) atomicCAS(err, 0u, 6u);
+        return;
+    }
+    const __half *e = emb + (size_t)t * D;
+    for (int c = threadIdx.x; c < D; c += blockDim.x) x[(size_t)blockIdx.x * D + c] = __half2float(e[c]);
+}
+
+// Decode attention of one sample, one KV head and one split of its keys:
+// keys j in [max(0, p - W + 1), p] (W = 0: all) are cut into
+// kBatchAttnSplits near-equal ranges; the CTA scores its range for the GL
+// query heads of the KV head, keeps the unnormalised P V with the running
+// max and sum, and the last CTA of the (sample, KV head) to finish merges
+// the splits in split order into FP16 o.
+__global__ void __launch_bounds__(kBatchAttnThreads)
+    ba_attn(const float *__restrict__ q, const __half *__restrict__ kc, const __half *__restrict__ vc,
+            const int *__restrict__ pos_word, int L, int l, int NKV, int GL, int DH, int ctx, int window, float scale,
+            float *__restrict__ ws, uint32_t *__restrict__ cnt, __half *__restrict__ o) {
+    extern __shared__ float asm_[];  // qs [GL][DH], then sc [GL][per_max]
+    __shared__ float mh[8], lh[8];
+    __shared__ int last;
+    const int g = blockIdx.x, b = blockIdx.y, split = blockIdx.z, S = gridDim.z;
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, NQ = NKV * GL;
+    const int per_max = (ctx + S - 1) / S;
+    float *qs = asm_, *sc = asm_ + GL * DH;
+    const int p = *pos_word;
+    const int jlo = window > 0 ? max(0, p - window + 1) : 0, n = p - jlo + 1, per = (n + S - 1) / S;
+    const int j0 = jlo + split * per, nk = max(0, min(j0 + per, p + 1) - j0);
+
+    const float *qb = q + (size_t)b * NQ * DH + (size_t)g * GL * DH;
+    for (int i = tid; i < GL * DH; i += blockDim.x) qs[i] = qb[i];
+    __syncthreads();
+    const size_t head = (((size_t)b * L + l) * NKV + g) * ctx;
+    const __half *kh = kc + head * DH, *vh = vc + head * DH;
+    for (int jj = tid; jj < nk; jj += blockDim.x) {
+        const uint4 *kr = reinterpret_cast<const uint4 *>(kh + (size_t)(j0 + jj) * DH);
+        float acc[8];
+        for (int h = 0; h < GL; ++h) acc[h] = 0.f;
+        for (int c8 = 0; c8 < DH / 8; ++c8) {
+            const uint4 u = kr[c8];
+            const __half2 *hp = reinterpret_cast<const __half2 *>(&u);
+            float kf[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __half22float2(hp[i]);
+                kf[2 * i] = f.x;
+                kf[2 * i + 1] = f.y;
+            }
+            for (int h = 0; h < GL; ++h) {
+                const float *qh = qs + h * DH + c8 * 8;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[h] += kf[i] * qh[i];
+            }
+        }
+        for (int h = 0; h < GL; ++h) sc[h * per_max + jj] = acc[h] * scale;
+    }
+    __syncthreads();
+    for (int h = w; h < GL; h += blockDim.x / 32) {  // one warp per head: max, exponentials, sum
+        float m = -INFINITY;
+        for (int jj = lane; jj < nk; jj += 32) m = fmaxf(m, sc[h * per_max + jj]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        float s = 0.f;
+        for (int jj = lane; jj < nk; jj += 32) {
+            const float e = expf(sc[h * per_max + jj] - m);
+            sc[h * per_max + jj] = e;
+            s += e;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        if (lane == 0) {
+            mh[h] = m;
+            lh[h] = s;
+        }
+    }
+    __syncthreads();
+    const int half = DH / 2;
+    float *part = ws + (((size_t)b * NKV + g) * S + split) * GL * (DH + 2);
+    for (int i = tid; i < GL * half; i += blockDim.x) {
+        const int h = i / half, c2 = i % half;
+        float ox = 0.f, oy = 0.f;
+        const float *ph = sc + h * per_max;
+        for (int jj = 0; jj < nk; ++jj) {
+            const float2 v = __half22float2(reinterpret_cast<const __half2 *>(vh + (size_t)(j0 + jj) * DH)[c2]);
+            ox += ph[jj] * v.x;
+            oy += ph[jj] * v.y;
+        }
+        part[h * (DH + 2) + 2 * c2] = ox;
+        part[h * (DH + 2) + 2 * c2 + 1] = oy;
+        if (c2 == 0) {
+            part[h * (DH + 2) + DH] = nk > 0 ? mh[h] : -INFINITY;
+            part[h * (DH + 2) + DH + 1] = nk > 0 ? lh[h] : 0.f;
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const uint32_t old = atomicAdd(&cnt[b * NKV + g], 1u);
+        last = old == (uint32_t)(S - 1);
+        if (last) cnt[b * NKV + g] = 0;
+        __threadfence();
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    const float *all = ws + ((size_t)b * NKV + g) * S * GL * (DH + 2);
+    for (int i = tid; i < GL * DH; i += blockDim.x) {
+        const int h = i / DH, c = i % DH;
+        float M = -INFINITY;
+        for (int s = 0; s < S; ++s) {
+            const float *ps = all + ((size_t)s * GL + h) * (DH + 2);
+            if (__ldcg(ps + DH + 1) > 0.f) M = fmaxf(M, __ldcg(ps + DH));
+        }
+        float num = 0.f, den = 0.f;
+        for (int s = 0; s < S; ++s) {
+            const float *ps = all + ((size_t)s * GL + h) * (DH + 2);
+            const float ls = __ldcg(ps + DH + 1);
+            if (ls > 0.f) {
+                const float f = expf(__ldcg(ps + DH) - M);
+                num += f * __ldcg(ps + c);
+                den += f * ls;
+            }
+        }
+        o[(size_t)b * NQ * DH + (size_t)(g * GL + h) * DH + c] = __float2half_rn(num / den);
+    }
+}
+
+// am[b] = lowest index among the maxima of logits[b] (one block per sample).
+__global__ void __launch_bounds__(1024) ba_argmax(const float *__restrict__ logits, int V, int *__restrict__ am) {
+    __shared__ float bv[32];
+    __shared__ int bi[32];
+    const float *z = logits + (size_t)blockIdx.x * V;
+    float best = -INFINITY;
+    int idx = INT_MAX;
+    for (int i = threadIdx.x; i < V; i += blockDim.x)
+        if (z[i] > best) {
+            best = z[i];
+            idx = i;
+        }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, best, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, idx, off);
+        if (ov > best || (ov == best && oi < idx)) {
+            best = ov;
+            idx = oi;
+        }
+    }
+    if ((threadIdx.x & 31) == 0) {
+        bv[threadIdx.x >> 5] = best;
+        bi[threadIdx.x >> 5] = idx;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < (int)(blockDim.x >> 5); ++w)
+            if (bv[w] > best || (bv[w] == best && bi[w] < idx)) {
+                best = bv[w];
+                idx = bi[w];
+            }
+        am[blockIdx.x] = idx == INT_MAX ? 0 : idx;
+    }
+}
+
+__global__ void ba_bump(int *pos_word) { *pos_word += 1; }
+
+// Sample b's cache gets positions [0, P) of the engine's cache for layer l
+// (blockIdx.x = l * NKV + kv head); the engine keeps each KV head in the
+// cache of the lane that computes it.
+__global__ void ba_copy_prefix(const __half *__restrict__ ekc, const __half *__restrict__ evc,
+                               __half *__restrict__ bkc, __half *__restrict__ bvc, const int2 *__restrict__ kvsrc,
+                               int P, int L, int NKV, int HKV_L, int DH, int ctx) {
+    const int l = blockIdx.x / NKV, kh = blockIdx.x % NKV, b = blockIdx.y;
+    const int2 src = kvsrc[kh];
+    const size_t from = ((((size_t)src.x * L + l) * HKV_L + src.y) * ctx) * DH;
+    const size_t to = ((((size_t)b * L + l) * NKV + kh) * ctx) * DH;
+    const size_t n16 = (size_t)P * DH / 8;
+    const uint4 *sk = reinterpret_cast<const uint4 *>(ekc + from), *sv = reinterpret_cast<const uint4 *>(evc + from);
+    uint4 *dk = reinterpret_cast<uint4 *>(bkc + to), *dv = reinterpret_cast<uint4 *>(bvc + to);
+    for (size_t i = threadIdx.x; i < n16; i += blockDim.x) {
+        dk[i] = sk[i];
+        dv[i] = sv[i];
+    }
+}
+
+size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
+
+size_t attn_smem(const lf::Shape &s) {
+    const int GL = s.NQ / s.NKV, per_max = (s.ctx + lf::kBatchAttnSplits - 1) / lf::kBatchAttnSplits;
+    return (size_t)GL * (s.DH + per_max) * sizeof(float);
+}
+
+// The buffers of a batch of B, carved from one allocation (base null: sizes only).
+void carve(BatchState &b, uint8_t *base, const lf::Shape &s, int B) {
+    size_t at = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t *p = base ? base + at : nullptr;
+        at += al256(bytes);
+        return p;
+    };
+    const size_t D = s.D, QD = (size_t)s.NQ * s.DH, F = s.F, V = s.V, R = 2 * (size_t)s.delay + 1;
+    const size_t kv = (size_t)B * s.L * s.NKV * s.ctx * s.DH;
+    const int GL = s.NQ / s.NKV;
+    b.tok = reinterpret_cast<int *>(take(B * sizeof(int)));
+    b.gen = reinterpret_cast<int *>(take((size_t)B * s.ctx * sizeof(int)));
+    b.am = reinterpret_cast<int *>(take(B * sizeof(int)));
+    b.d_pos = reinterpret_cast<int *>(take(sizeof(int)));
+    b.kvsrc = reinterpret_cast<int2 *>(take(s.NKV * sizeof(int2)));
+    b.err = reinterpret_cast<uint32_t *>(take(sizeof(uint32_t)));
+    b.cnt = reinterpret_cast<uint32_t *>(take((size_t)b.n_cnt * sizeof(uint32_t)));
+    b.att_cnt = reinterpret_cast<uint32_t *>(take((size_t)B * s.NKV * sizeof(uint32_t)));
+    b.x = reinterpret_cast<float *>(take(B * D * 4));
+    b.ring = reinterpret_cast<float *>(take(R * B * D * 4));
+    b.q = reinterpret_cast<float *>(take(B * QD * 4));
+    b.logits = reinterpret_cast<float *>(take(B * V * 4));
+    b.ws = reinterpret_cast<float *>(take(std::max<size_t>(b.ws_floats, 1) * 4));
+    b.att_ws = reinterpret_cast<float *>(take((size_t)B * s.NKV * lf::kBatchAttnSplits * GL * (s.DH + 2) * 4));
+    b.h16 = reinterpret_cast<__half *>(take(B * D * 2));
+    b.o16 = reinterpret_cast<__half *>(take(B * QD * 2));
+    b.u16 = reinterpret_cast<__half *>(take(B * F * 2));
+    b.kc = reinterpret_cast<__half *>(take(kv * 2));
+    b.vc = reinterpret_cast<__half *>(take(kv * 2));
+    b.bytes = at;
+}
+
+void batch_release(BatchState *b) {
+    if (!b) return;
+    if (b->graph) cudaGraphExecDestroy(b->graph);
+    if (b->cap) cudaStreamDestroy(b->cap);
+    if (b->mem) cudaFree(b->mem);
+    delete b;
+}
+
+// Every kernel of one step, in order, on `st` (captured into the graph).
+lf_status enqueue_batch_step(lf_engine *e, BatchState &b, cudaStream_t st) {
+    const lf::Shape &s = e->plan.sh;
+    const int B = b.B, D = s.D, L = s.L, R = 2 * s.delay + 1, QD = s.NQ * s.DH, QKVN = (s.NQ + 2 * s.NKV) * s.DH;
+    const float eps = e->cfg.rms_eps, scale = (float)(1.0 / std::sqrt((double)s.DH));
+    const size_t BD = (size_t)B * D;
+    lf::GemvArgs base;
+    base.B = B;
+    base.ws = b.ws;
+    base.ws_floats = b.ws_floats;
+    base.cnt = b.cnt;
+    base.n_cnt = b.n_cnt;
+    base.err = b.err;
+    base.timeout_ns = kBatchTimeoutNs;
+
+    ba_embed<<<B, 256, 0, st>>>(e->emb, b.tok, b.x, D, s.V, b.err);
+    for (int sb = 0; sb < 2 * L; ++sb) {
+        const int l = sb / 2, ua = sb - 1 - 2 * s.delay;
+        const __half *lw = e->blob + s.off_layer0 + (long long)l * s.per_layer;
+        float *P = b.ring + (size_t)(sb % R) * BD;
+        const __half *gain = e->gains + (size_t)(sb % 2 == 0 ? l : L + l) * D;
+        pf_addnorm<<<B, kNormThreads, 0, st>>>(b.x, b.ring, BD, ua, ua >= 0 ? 1 : 0, R, gain, b.h16, D, eps);
+        lf_status gs;
+        if (sb % 2 == 0) {
+            lf::GemvArgs a = base;
+            a.N = QKVN;
+            a.K = D;
+            a.mode = lf::GEMV_QKV;
+            a.q = b.q;
+            a.rope = e->rope;
+            a.kc = b.kc;
+            a.vc = b.vc;
+            a.pos = b.d_pos;
+            a.NQ = s.NQ;
+            a.NKV = s.NKV;
+            a.DH = s.DH;
+            a.L = L;
+            a.l = l;
+            a.ctx = s.ctx;
+            if ((gs = lf::gemv_tc(lw + s.o_wq, b.h16, a, st)) != LF_OK) return gs;
+            const dim3 ag(s.NKV, B, lf::kBatchAttnSplits);
+            ba_attn<<<ag, lf::kBatchAttnThreads, attn_smem(s), st>>>(b.q, b.kc, b.vc, b.d_pos, L, l, s.NKV,
+                                                                    s.NQ / s.NKV, s.DH, s.ctx, e->cfg.swa_window[l],
+                                                                    scale, b.att_ws, b.att_cnt, b.o16);
+            a = base;
+            a.N = D;
+            a.K = QD;
+            a.y = P;
+            a.ldy = D;
+            if ((gs = lf::gemv_tc(lw + s.o_wo, b.o16, a, st)) != LF_OK) return gs;
+        } else {
+            lf::GemvArgs a = base;
+            a.N = 2 * s.F;
+            a.K = D;
+            a.mode = lf::GEMV_SWIGLU;
+            a.u = b.u16;
+            a.ldu = s.F;
+            if ((gs = lf::gemv_tc(lw + s.o_wg, b.h16, a, st)) != LF_OK) return gs;
+            a = base;
+            a.N = D;
+            a.K = s.F;
+            a.y = P;
+            a.ldy = D;
+            if ((gs = lf::gemv_tc(lw + s.o_wd, b.u16, a, st)) != LF_OK) return gs;
+        }
+    }
+    const int u0 = std::max(0, 2 * L - 1 - 2 * s.delay);
+    pf_addnorm<<<B, kNormThreads, 0, st>>>(b.x, b.ring, BD, u0, 2 * L - u0, R, e->gains + (size_t)2 * L * D, b.h16,
+                                           D, eps);
+    lf::GemvArgs a = base;
+    a.N = s.V;
+    a.K = D;
+    a.y = b.logits;
+    a.ldy = s.V;
+    lf_status gs = lf::gemv_tc(e->blob + s.off_lm, b.h16, a, st);
+    if (gs != LF_OK) return gs;
+    ba_argmax<<<B, 1024, 0, st>>>(b.logits, s.V, b.am);
+    ba_bump<<<1, 1, 0, st>>>(b.d_pos);
+    return cudaGetLastError() == cudaSuccess ? LF_OK : LF_ERR_CUDA;
+}
+
+lf_status batch_fail(lf_engine *e, lf_status st) {
+    if (e->batch) e->batch->ready = false;
+    if (st == LF_ERR_CUDA || st == LF_ERR_TIMEOUT) e->poisoned = st;
+    return st;
+}
+
+// Reads the error word after the work queued on the engine stream; the
+// stream is synchronised.
+lf_status batch_finish(lf_engine *e, BatchState &b) {
+    uint32_t werr = 0;
+    cudaError_t err = cudaMemcpyAsync(&werr, b.err, sizeof(werr), cudaMemcpyDeviceToHost, e->stream);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(e->stream);
+    if (err != cudaSuccess) {
+        (void)cudaGetLastError();
+        return batch_fail(e, LF_ERR_CUDA);
+    }
+    if (werr == 6) return batch_fail(e, LF_ERR_INVALID_ARG);
+    if (werr) return batch_fail(e, LF_ERR_TIMEOUT);
+    return LF_OK;
+}
+
+}  // namespace
+
+void lf_batch_free(lf_engine *e) {
+    if (!e) return;
+    batch_release(e->batch);
+    e->batch = nullptr;
+}
+
+extern "C" lf_status lf_batch_begin(lf_engine *e, int n_batch) {
+    if (!e || n_batch < 1 || n_batch > lf::kGemvMaxBatch) return LF_ERR_INVALID_ARG;
+    if (e->poisoned != LF_OK) return e->poisoned;
+    if (!e->loaded) return LF_ERR_NOT_LOADED;
+    if (!e->blob) return LF_ERR_OOM;
+    const lf::Shape &s = e->plan.sh;
+    if (s.own || s.D % 64 || (s.NQ * s.DH) % 64 || s.F % 64 || 128 % s.DH || ((s.NQ + 2 * s.NKV) * s.DH) % 128 ||
+        s.D > 4 * kNormV * kNormThreads || s.NQ / s.NKV > 8 || s.NQ % s.NKV || attn_smem(s) > 200 * 1024)
+        return LF_ERR_UNSUPPORTED;
+    if (e->pos >= s.ctx) return LF_ERR_CTX_OVERFLOW;
+    lf_batch_free(e);
+    BatchState *b = new BatchState();
+    b->B = n_batch;
+    // split-K workspace: the largest need over the step's GEMVs
+    const int QD = s.NQ * s.DH, QKVN = (s.NQ + 2 * s.NKV) * s.DH;
+    const int shapes[5][3] = {{QKVN, s.D, lf::GEMV_QKV},
+                              {s.D, QD, lf::GEMV_F32},
+                              {2 * s.F, s.D, lf::GEMV_SWIGLU},
+                              {s.D, s.F, lf::GEMV_F32},
+                              {s.V, s.D, lf::GEMV_F32}};
+    for (auto &sh : shapes) {
+        size_t wf = 0;
+        int nc = 0;
+        lf::gemv_tc_needs(sh[0], sh[1], sh[2], &wf, &nc);
+        b->ws_floats = std::max(b->ws_floats, wf);
+        b->n_cnt = std::max(b->n_cnt, nc);
+    }
+    carve(*b, nullptr, s, n_batch);
+    if (cudaMalloc(&b->mem, b->bytes) != cudaSuccess) {
+        (void)cudaGetLastError();
+        b->mem = nullptr;
+        batch_release(b);
+        return LF_ERR_OOM;
+    }
+    carve(*b, static_cast<uint8_t *>(b->mem), s, n_batch);
+    e->batch = b;
+
+    std::vector<int2> kvsrc(s.NKV);
+    for (int kh = 0; kh < s.NKV; ++kh)
+        for (int lam = s.NL - 1; lam >= 0; --lam)
+            if (s.kv_first[lam] <= kh && kh < s.kv_first[lam] + s.HKV_L) kvsrc[kh] = make_int2(lam, kh - s.kv_first[lam]);
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(ba_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    });
+    cudaStream_t st = e->stream;
+    cudaError_t err = lf::gemv_tc_prepare() == LF_OK ? attr : cudaErrorUnknown;
+    if (err == cudaSuccess) err = cudaMemsetAsync(b->mem, 0, b->bytes, st);
+    if (err == cudaSuccess) err = cudaMemcpyAsync(b->kvsrc, kvsrc.data(), kvsrc.size() * sizeof(int2), cudaMemcpyHostToDevice, st);
+    b->pos = e->pos;
+    if (err == cudaSuccess) err = cudaMemcpyAsync(b->d_pos, &b->pos, sizeof(int), cudaMemcpyHostToDevice, st);
+    if (err == cudaSuccess && e->pos > 0)
+        ba_copy_prefix<<<dim3(s.L * s.NKV, n_batch), 256, 0, st>>>(e->kc, e->vc, b->kc, b->vc, b->kvsrc, e->pos, s.L,
+                                                                  s.NKV, s.HKV_L, s.DH, s.ctx);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(st);
+    if (err == cudaSuccess) err = cudaGetLastError();
+    if (err != cudaSuccess) return batch_fail(e, LF_ERR_CUDA);
+
+    // capture one step
+    if (cudaStreamCreateWithFlags(&b->cap, cudaStreamNonBlocking) != cudaSuccess) return batch_fail(e, LF_ERR_CUDA);
+    if (cudaStreamBeginCapture(b->cap, cudaStreamCaptureModeRelaxed) != cudaSuccess) return batch_fail(e, LF_ERR_CUDA);
+    const lf_status qs = enqueue_batch_step(e, *b, b->cap);
+    cudaGraph_t g = nullptr;
+    const cudaError_t ce = cudaStreamEndCapture(b->cap, &g);
+    if (qs != LF_OK || ce != cudaSuccess) {
+        if (g) cudaGraphDestroy(g);
+        (void)cudaGetLastError();
+        return batch_fail(e, qs != LF_OK && qs != LF_ERR_CUDA ? qs : LF_ERR_CUDA);
+    }
+    err = cudaGraphInstantiate(&b->graph, g, 0);
+    cudaGraphDestroy(g);
+    if (err != cudaSuccess) {
+        b->graph = nullptr;
+        return batch_fail(e, LF_ERR_CUDA);
+    }
+    b->ready = true;
+    return LF_OK;
+}
+
+extern "C" lf_status lf_batch_end(lf_engine *e) {
+    if (!e) return LF_ERR_INVALID_ARG;
+    if (e->batch && e->stream) cudaStreamSynchronize(e->stream);
+    lf_batch_free(e);
+    return LF_OK;
+}
+
+extern "C" lf_status lf_batch_info(const lf_engine *e, int *n_batch, int *position) {
+    if (!e || !n_batch || !position) return LF_ERR_INVALID_ARG;
+    const bool ok = e->batch && e->batch->ready;
+    *n_batch = ok ? e->batch->B : 0;
+    *position = ok ? e->batch->pos : 0;
+    return LF_OK;
+}
+
+extern "C" lf_status lf_batch_step(lf_engine *e, const int32_t *tokens, float *logits, int32_t *argmax) {
+    if (!e || !tokens) return LF_ERR_INVALID_ARG;
+    if (e->poisoned != LF_OK) return e->poisoned;
+    if (!e->batch || !e->batch->ready) return LF_ERR_NOT_LOADED;
+    BatchState &b = *e->batch;
+    const lf::Shape &s = e->plan.sh;
+    if (b.pos >= s.ctx) return LF_ERR_CTX_OVERFLOW;
+    for (int i = 0; i < b.B; ++i)
+        if (tokens[i] < 0 || tokens[i] >= s.V) return LF_ERR_INVALID_ARG;
+    cudaStream_t st = e->stream;
+    cudaError_t err = cudaMemcpyAsync(b.tok, tokens, (size_t)b.B * sizeof(int32_t), cudaMemcpyHostToDevice, st);
+    if (err == cudaSuccess) err = cudaGraphLaunch(b.graph, st);
+    if (err == cudaSuccess && logits)
+        err = cudaMemcpyAsync(logits, b.logits, (size_t)b.B * s.V * sizeof(float), cudaMemcpyDeviceToHost, st);
+    if (err == cudaSuccess && argmax)
+        err = cudaMemcpyAsync(argmax, b.am, (size_t)b.B * sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+    if (err != cudaSuccess) {
+        (void)cudaGetLastError();
+        return batch_fail(e, LF_ERR_CUDA);
+    }
+    const lf_status r = batch_finish(e, b);
+    if (r == LF_OK) ++b.pos;
+    return r;
+}
+
+extern "C" lf_status lf_batch_generate(lf_engine *e, const int32_t *first_tokens, int n_steps, float temperature,
+                                       float top_p, uint64_t seed, int32_t *tokens_out) {
+    if (!e || !first_tokens || !tokens_out || n_steps < 1 || !(temperature >= 0.f) || !(top_p > 0.f && top_p <= 1.f))
+        return LF_ERR_INVALID_ARG;
+    if (e->poisoned != LF_OK) return e->poisoned;
+    if (!e->batch || !e->batch->ready) return LF_ERR_NOT_LOADED;
+    BatchState &b = *e->batch;
+    const lf::Shape &s = e->plan.sh;
+    if ((long long)b.pos + n_steps > s.ctx) return LF_ERR_CTX_OVERFLOW;
+    for (int i = 0; i < b.B; ++i)
+        if (first_tokens[i] < 0 || first_tokens[i] >= s.V) return LF_ERR_INVALID_ARG;
+    if (lf::sample_smem_bytes(s.V) > lf::kSampleMaxSmem) return LF_ERR_UNSUPPORTED;
+    cudaStream_t st = e->stream;
+    cudaError_t err = cudaMemcpyAsync(b.tok, first_tokens, (size_t)b.B * sizeof(int32_t), cudaMemcpyHostToDevice, st);
+    for (int i = 0; i < n_steps && err == cudaSuccess; ++i) {
+        err = cudaGraphLaunch(b.graph, st);
+        if (err != cudaSuccess) break;
+        // sample b draws with counter (input position, b): the same draw as the single-sequence sampler's
+        const lf_status ls = lf::launch_sample_batch(b.logits, s.V, b.B, temperature, top_p, seed,
+                                                     (uint32_t)(b.pos + i), b.tok, b.gen + i, s.ctx, st);
+        if (ls != LF_OK) return batch_fail(e, ls);
+    }
+    if (err == cudaSuccess)
+        err = cudaMemcpy2DAsync(tokens_out, (size_t)n_steps * sizeof(int32_t), b.gen, (size_t)s.ctx * sizeof(int32_t),
+                                (size_t)n_steps * sizeof(int32_t), b.B, cudaMemcpyDeviceToHost, st);
+    if (err != cudaSuccess) {
+        (void)cudaGetLastError();
+        return batch_fail(e, LF_ERR_CUDA);
+    }
+    const lf_status r = batch_finish(e, b);
+    if (r == LF_OK) b.pos += n_steps;
+    return r;
+}

@@ -10,6 +10,10 @@
 #include "lf_common.h"
 #include "lf_plan.h"
 
+namespace lf {
+struct BatchState;  // lf_batch.cu
+}
+
 struct lf_engine {
     lf_config cfg;
     lf::Plan plan;
@@ -30,6 +34,7 @@ struct lf_engine {
     size_t pf_bytes = 0;
     uint32_t *pf_err = nullptr;  // device word: GEMM wait timeouts during a batched prefill
     int pf_tc_attention = 1;     // batched prefill attention on the tensor cores (head_dim 128)
+    lf::BatchState *batch = nullptr;  // lf_batch_begin .. lf_batch_end (owned separately)
     lf::CtaPlan *d_cta = nullptr;
     lf::LayerPlan *d_lp = nullptr;
     size_t n_ctr = 0;
@@ -48,3 +53,6 @@ struct lf_engine {
     std::vector<void *> allocs;
     unsigned long long *trace = nullptr;  // lf_debug_trace buffer (owned separately)
 };
+
+// Frees the batched-decode state (lf_batch.cu); safe when there is none.
+void lf_batch_free(lf_engine *e);

@@ -20,6 +20,7 @@
 #include "laneformer.h"
 #include "lf_engine.h"
 #include "lf_pf_attn_tc.h"
+#include "lf_rows.cuh"
 #include "lf_tc_gemm.h"
 
 namespace {
@@ -39,32 +40,9 @@ __global__ void pf_add(float *__restrict__ x, const float *__restrict__ p, size_
         x[i] += p[i];
 }
 
-__device__ float block_sum(float v, float *red) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[w] = v;
-    __syncthreads();
-    float t = 0.f;
-    for (int i = 0; i < nw; ++i) t += red[i];
-    return t;
-}
-
-// h[i] = FP16(g * x[i] / sqrt(mean(x[i]^2) + eps)), one block per row
-__global__ void pf_rmsnorm(const float *__restrict__ x, const __half *__restrict__ g, __half *__restrict__ h,
-                           int D, float eps) {
-    __shared__ float red[32];
-    const float *xr = x + (size_t)blockIdx.x * D;
-    float ss = 0.f;
-    for (int c = threadIdx.x; c < D; c += blockDim.x) ss += xr[c] * xr[c];
-    const float inv = rsqrtf(block_sum(ss, red) / D + eps);
-    for (int c = threadIdx.x; c < D; c += blockDim.x)
-        h[(size_t)blockIdx.x * D + c] = __float2half_rn(__half2float(g[c]) * xr[c] * inv);
-}
-
 // RoPE on q and k (pairs c, c + dh/2; table rope[p][c] = (cos, sin)), q kept
-// in fp32 (CUDA-core attention) and FP16 (tensor-core attention), k and v rounded to FP16 into the cache of every lane that reads
+// in FP16 (tensor-core attention) and, when q is not null, fp32 (CUDA-core
+// attention); k and v rounded to FP16 into the cache of every lane that reads
 // that KV head.  One block per position.
 __global__ void pf_rope_kv(const float *__restrict__ qkv, const float2 *__restrict__ rope, float *__restrict__ q,
                            __half *__restrict__ q16, __half *__restrict__ kc, __half *__restrict__ vc, const int *__restrict__ kv_first,
@@ -77,8 +55,10 @@ __global__ void pf_rope_kv(const float *__restrict__ qkv, const float2 *__restri
         const float a = row[hq * DH + c], b = row[hq * DH + c + half];
         const float2 r = cs[c];
         const float qa = a * r.x - b * r.y, qb = a * r.y + b * r.x;
-        q[(size_t)i * NQ * DH + hq * DH + c] = qa;
-        q[(size_t)i * NQ * DH + hq * DH + c + half] = qb;
+        if (q) {
+            q[(size_t)i * NQ * DH + hq * DH + c] = qa;
+            q[(size_t)i * NQ * DH + hq * DH + c + half] = qb;
+        }
         q16[(size_t)i * NQ * DH + hq * DH + c] = __float2half_rn(qa);
         q16[(size_t)i * NQ * DH + hq * DH + c + half] = __float2half_rn(qb);
     }
@@ -350,7 +330,9 @@ struct PfBufs {
     size_t bytes;
 };
 
-PfBufs carve(uint8_t *base, const lf::Shape &s, int M) {
+// qf (fp32 queries) only for the CUDA-core attention, gu (fp32 gate/up) only
+// when SwiGLU is not fused into the gate/up GEMM.
+PfBufs carve(uint8_t *base, const lf::Shape &s, int M, bool need_qf, bool need_gu) {
     const size_t D = s.D, QD = (size_t)s.NQ * s.DH, QKVN = (size_t)(s.NQ + 2 * s.NKV) * s.DH, F = s.F;
     const size_t R = 2 * (size_t)s.delay + 1;
     PfBufs b{};
@@ -364,8 +346,8 @@ PfBufs carve(uint8_t *base, const lf::Shape &s, int M) {
     b.x = reinterpret_cast<float *>(take(M * D * 4));
     b.ring = reinterpret_cast<float *>(take(R * M * D * 4));
     b.qkv = reinterpret_cast<float *>(take(M * QKVN * 4));
-    b.qf = reinterpret_cast<float *>(take(M * QD * 4));
-    b.gu = reinterpret_cast<float *>(take(M * 2 * F * 4));
+    b.qf = need_qf ? reinterpret_cast<float *>(take(M * QD * 4)) : nullptr;
+    b.gu = need_gu ? reinterpret_cast<float *>(take(M * 2 * F * 4)) : nullptr;
     b.h = reinterpret_cast<__half *>(take(M * std::max(D, F) * 2));
     b.o = reinterpret_cast<__half *>(take(M * QD * 2));
     b.u = reinterpret_cast<__half *>(take(M * F * 2));
@@ -392,10 +374,12 @@ extern "C" lf_status lf_prefill_batched(lf_engine *e, const int32_t *tokens, int
     if (!e->blob) return LF_ERR_OOM;
     const int D = s.D, DH = s.DH, NQ = s.NQ, NKV = s.NKV, F = s.F, L = s.L, QD = NQ * DH;
     const int QKVN = (NQ + 2 * NKV) * DH, R = 2 * s.delay + 1, M = n, p0 = e->pos;
-    if (D % 64 || QD % 64 || F % 64 || (DH != 128 && DH != 32)) return LF_ERR_UNSUPPORTED;
+    if (D % 64 || QD % 64 || F % 64 || (DH != 128 && DH != 32) || D > 4 * kNormV * kNormThreads)
+        return LF_ERR_UNSUPPORTED;
     cudaStream_t st = e->stream;
+    const bool tc_attn = DH == 128 && e->pf_tc_attention, fused_swiglu = F % 128 == 0;
 
-    const PfBufs need = carve(nullptr, s, M);
+    const PfBufs need = carve(nullptr, s, M, !tc_attn, !fused_swiglu);
     if (need.bytes > e->pf_bytes) {
         if (e->pf_mem) cudaFree(e->pf_mem);
         e->pf_mem = nullptr;
@@ -407,7 +391,7 @@ extern "C" lf_status lf_prefill_batched(lf_engine *e, const int32_t *tokens, int
         }
         e->pf_bytes = need.bytes;
     }
-    const PfBufs b = carve(static_cast<uint8_t *>(e->pf_mem), s, M);
+    const PfBufs b = carve(static_cast<uint8_t *>(e->pf_mem), s, M, !tc_attn, !fused_swiglu);
 
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
@@ -427,21 +411,22 @@ extern "C" lf_status lf_prefill_batched(lf_engine *e, const int32_t *tokens, int
 
     const float scale = (float)(1.0 / std::sqrt((double)DH)), eps = e->cfg.rms_eps;
     const size_t MD = (size_t)M * D;
-    const int add_blocks = (int)std::min<size_t>((MD + 255) / 256, 4096);
     for (int sb = 0; sb < 2 * L; ++sb) {
         const int l = sb / 2, ua = sb - 1 - 2 * s.delay;
-        if (ua >= 0) pf_add<<<add_blocks, 256, 0, st>>>(b.x, b.ring + (size_t)(ua % R) * MD, MD);
+        // the partial of sub-block ua arrives in the residual now, just before the norm that reads it
+        const int n_arrive = ua >= 0 ? 1 : 0;
         const __half *lw = e->blob + s.off_layer0 + (long long)l * s.per_layer;
         float *P = b.ring + (size_t)(sb % R) * MD;
         lf_status gs;
         if (sb % 2 == 0) {
-            pf_rmsnorm<<<M, 256, 0, st>>>(b.x, e->gains + (size_t)l * D, b.h, D, eps);
+            pf_addnorm<<<M, kNormThreads, 0, st>>>(b.x, b.ring, MD, ua, n_arrive, R, e->gains + (size_t)l * D, b.h,
+                                                   D, eps);
             gs = lf::tc_gemm_f16(b.h, lw + s.o_wq, b.qkv, M, QKVN, D, QKVN, e->pf_err, kGemmTimeoutNs, st);
             if (gs != LF_OK) return gs == LF_ERR_CUDA ? pf_fail(e) : gs;
-            pf_rope_kv<<<M, 256, 0, st>>>(b.qkv, e->rope, b.qf, b.q16, e->kc, e->vc, e->d_kvfirst, p0, NQ, NKV, DH,
-                                          s.NL, L, l, s.HKV_L, s.ctx);
+            pf_rope_kv<<<M, 256, 0, st>>>(b.qkv, e->rope, tc_attn ? nullptr : b.qf, b.q16, e->kc, e->vc,
+                                          e->d_kvfirst, p0, NQ, NKV, DH, s.NL, L, l, s.HKV_L, s.ctx);
             const dim3 ag((M + PF_QB - 1) / PF_QB, NQ);
-            if (DH == 128 && e->pf_tc_attention) {
+            if (tc_attn) {
                 lf::TcAttnArgs ta{M, p0, NQ, s.HQ_L, s.GL, s.HKV_L, L, l, s.ctx, e->cfg.swa_window[l], scale, b.o, QD};
                 gs = lf::pf_attention_tc(b.q16, e->kc, e->vc, ta, s.NL, e->pf_err, kGemmTimeoutNs, st);
                 if (gs != LF_OK) return gs == LF_ERR_CUDA ? pf_fail(e) : gs;
@@ -455,11 +440,17 @@ extern "C" lf_status lf_prefill_batched(lf_engine *e, const int32_t *tokens, int
                                                                        e->cfg.swa_window[l], scale);
             gs = lf::tc_gemm_f16(b.o, lw + s.o_wo, P, M, D, QD, D, e->pf_err, kGemmTimeoutNs, st);
         } else {
-            pf_rmsnorm<<<M, 256, 0, st>>>(b.x, e->gains + (size_t)(L + l) * D, b.h, D, eps);
-            gs = lf::tc_gemm_f16(b.h, lw + s.o_wg, b.gu, M, 2 * F, D, 2 * F, e->pf_err, kGemmTimeoutNs, st);
+            pf_addnorm<<<M, kNormThreads, 0, st>>>(b.x, b.ring, MD, ua, n_arrive, R, e->gains + (size_t)(L + l) * D,
+                                                   b.h, D, eps);
+            if (fused_swiglu) {
+                gs = lf::tc_gemm_swiglu_f16(b.h, lw + s.o_wg, b.u, M, F, D, F, e->pf_err, kGemmTimeoutNs, st);
+            } else {
+                gs = lf::tc_gemm_f16(b.h, lw + s.o_wg, b.gu, M, 2 * F, D, 2 * F, e->pf_err, kGemmTimeoutNs, st);
+                if (gs != LF_OK) return gs == LF_ERR_CUDA ? pf_fail(e) : gs;
+                const size_t nf = (size_t)M * F;
+                pf_swiglu<<<(int)std::min<size_t>((nf + 255) / 256, 4096), 256, 0, st>>>(b.gu, b.u, F, nf);
+            }
             if (gs != LF_OK) return gs == LF_ERR_CUDA ? pf_fail(e) : gs;
-            const size_t nf = (size_t)M * F;
-            pf_swiglu<<<(int)std::min<size_t>((nf + 255) / 256, 4096), 256, 0, st>>>(b.gu, b.u, F, nf);
             gs = lf::tc_gemm_f16(b.u, lw + s.o_wd, P, M, D, F, D, e->pf_err, kGemmTimeoutNs, st);
         }
         if (gs != LF_OK) return gs == LF_ERR_CUDA ? pf_fail(e) : gs;

@@ -186,6 +186,7 @@ lf_status lf_plan_stats(const lf_config *cfg, int n_sm, int64_t stats[8]) {
 
 void lf_destroy(lf_engine *e) {
     if (!e) return;
+    lf_batch_free(e);
     for (void *p : e->allocs) cudaFree(p);
     if (e->trace) cudaFree(e->trace);
     if (e->pf_mem) cudaFree(e->pf_mem);

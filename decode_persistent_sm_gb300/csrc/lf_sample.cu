@@ -77,8 +77,16 @@ __device__ float bsum(float v, float *red, float *bcast) {
 }
 
 __global__ void __launch_bounds__(SMP_THREADS, 1)
-    sample_kernel(const float *__restrict__ logits, int V, float temperature, float top_p, uint32_t key0,
-                  uint32_t key1, uint32_t position, uint32_t sample, int *__restrict__ out) {
+    sample_kernel(const float *__restrict__ logits_all, int V, float temperature, float top_p, uint32_t key0,
+                  uint32_t key1, uint32_t position, uint32_t sample0, int *__restrict__ out_all,
+                  int *__restrict__ out2_all, int ld2) {
+    // block b: row b of the logits, sample index sample0 + b, token to out_all[b] (and out2_all[b * ld2])
+    const float *logits = logits_all + (size_t)blockIdx.x * V;
+    const uint32_t sample = sample0 + blockIdx.x;
+    auto emit = [&](int v) {
+        out_all[blockIdx.x] = v;
+        if (out2_all) out2_all[(size_t)blockIdx.x * ld2] = v;
+    };
     extern __shared__ float pv[];  // [V] unnormalised probabilities
     __shared__ float red[SMP_THREADS / 32];
     __shared__ float wtot[SMP_THREADS / 32];
@@ -96,7 +104,7 @@ __global__ void __launch_bounds__(SMP_THREADS, 1)
         const float m = bmax(best, red);
         if (best == m && idx != INT_MAX) atomicMin(&tok, idx);
         __syncthreads();
-        if (tid == 0) *out = tok == INT_MAX ? 0 : tok;
+        if (tid == 0) emit(tok == INT_MAX ? 0 : tok);
         return;
     }
 
@@ -185,16 +193,18 @@ __global__ void __launch_bounds__(SMP_THREADS, 1)
         if (tid == 0) tok = (int)lm;
         __syncthreads();
     }
-    if (tid == 0) *out = tok;
+    if (tid == 0) emit(tok);
 }
 
 }  // namespace
 
 size_t sample_smem_bytes(int vocab) { return (size_t)vocab * sizeof(float); }
 
-lf_status launch_sample(const float *logits, int vocab, float temperature, float top_p, uint64_t seed,
-                        uint32_t position, uint32_t sample, int32_t *token, cudaStream_t stream) {
-    if (!logits || !token || vocab < 1 || !(temperature >= 0.f) || !(top_p > 0.f && top_p <= 1.f))
+namespace {
+
+lf_status launch(const float *logits, int vocab, int rows, float temperature, float top_p, uint64_t seed,
+                 uint32_t position, uint32_t sample0, int32_t *token, int32_t *token2, int ld2, cudaStream_t stream) {
+    if (!logits || !token || vocab < 1 || rows < 1 || !(temperature >= 0.f) || !(top_p > 0.f && top_p <= 1.f))
         return LF_ERR_INVALID_ARG;
     if (sample_smem_bytes(vocab) > kSampleMaxSmem) return LF_ERR_UNSUPPORTED;
     static std::once_flag once;
@@ -203,9 +213,23 @@ lf_status launch_sample(const float *logits, int vocab, float temperature, float
         attr = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSampleMaxSmem);
     });
     if (attr != cudaSuccess) return LF_ERR_CUDA;
-    sample_kernel<<<1, SMP_THREADS, sample_smem_bytes(vocab), stream>>>(
-        logits, vocab, temperature, top_p, (uint32_t)seed, (uint32_t)(seed >> 32), position, sample, token);
+    sample_kernel<<<rows, SMP_THREADS, sample_smem_bytes(vocab), stream>>>(logits, vocab, temperature, top_p,
+                                                                          (uint32_t)seed, (uint32_t)(seed >> 32),
+                                                                          position, sample0, token, token2, ld2);
     return cudaGetLastError() == cudaSuccess ? LF_OK : LF_ERR_CUDA;
+}
+
+}  // namespace
+
+lf_status launch_sample(const float *logits, int vocab, float temperature, float top_p, uint64_t seed,
+                        uint32_t position, uint32_t sample, int32_t *token, cudaStream_t stream) {
+    return launch(logits, vocab, 1, temperature, top_p, seed, position, sample, token, nullptr, 0, stream);
+}
+
+lf_status launch_sample_batch(const float *logits, int vocab, int rows, float temperature, float top_p,
+                              uint64_t seed, uint32_t position, int32_t *token, int32_t *token2, int ld2,
+                              cudaStream_t stream) {
+    return launch(logits, vocab, rows, temperature, top_p, seed, position, 0, token, token2, ld2, stream);
 }
 
 }  // namespace lf

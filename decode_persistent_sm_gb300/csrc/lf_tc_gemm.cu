@@ -3,6 +3,12 @@
 // A holds the activations of M positions, B a weight matrix in its natural
 // [out][in] layout, so both operands are K-major.
 //
+// SwiGLU variant: B = [W_gate (F rows); W_up (F rows)], and tile n takes gate
+// rows n*128.. and up rows F + n*128.. as the two halves of its 256-row B
+// tile, so one accumulator holds gate and up of the same 128 hidden units; the
+// epilogue writes U[M][F] = FP16(silu(gate) * up) and the fp32 gate/up
+// product never reaches memory.
+//
 // A persistent CTA per SM walks 128 x 256 tiles of C in a grouped order: a
 // copy warp streams 128 x 64 and 256 x 64 tiles of A and B into a 4-stage
 // shared-memory ring with TMA (128-byte swizzle), one elected thread of the
@@ -26,6 +32,7 @@ namespace {
 constexpr int BM = 128, BN = 256, BK = 64;  // BK fp16 = 128 bytes = one swizzle row
 constexpr int TG_STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BH = BN / 2, BH_BYTES = BH * BK * 2;  // B is copied as two 128-row halves
 constexpr int TG_THREADS = 192;  // warp 0 copies, warp 1 MMA + TMEM owner, warps 2-5 epilogue
 constexpr uint32_t TMEM_COLS = 512;  // two 256-column accumulators
 constexpr int GROUP_M = 8;  // tile order: 8 M-tiles share each B tile while it is in L2
@@ -66,14 +73,17 @@ __device__ __forceinline__ void tile_of(int t, int mt, int nt, int &m, int &n) {
 // Persistent: CTA c computes tiles c, c + gridDim.x, ...; the stage ring and
 // the two TMEM accumulators run across tiles, so copies and MMAs of one tile
 // overlap the epilogue of the previous one.
+// kSwiGLU: N = 2F is the row count of B, the grid of tiles is M x F/128 and
+// C is the FP16 U[M][F] (row stride ldc halves); otherwise C is fp32.
+template <bool kSwiGLU>
 __global__ void __launch_bounds__(TG_THREADS, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, float *C,
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, void *C,
                    int M, int N, int K, int ldc, uint32_t *err, unsigned long long timeout_ns) {
     extern __shared__ __align__(1024) uint8_t tg_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(tg_raw) + 1023) & ~uintptr_t(1023));
     TgShared &S = *reinterpret_cast<TgShared *>(tiles + (size_t)TG_STAGES * STAGE_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int mt = (M + BM - 1) / BM, nt = (N + BN - 1) / BN, ntiles = mt * nt, nk = K / BK;
+    const int mt = (M + BM - 1) / BM, nt = kSwiGLU ? N / BN : (N + BN - 1) / BN, ntiles = mt * nt, nk = K / BK;
     const uint64_t deadline = global_timer_ns() + timeout_ns;
 
     if (threadIdx.x == 0) {
@@ -109,9 +119,15 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                         !wait_phase(S, &S.empty[s], ((kbg / TG_STAGES) - 1) & 1u, deadline, err))
                         break;
                     uint8_t *a = tiles + (size_t)s * STAGE_BYTES;
-                    mbar_arrive_expect_tx(&S.full[s], STAGE_BYTES);
+                    // B halves: rows y0.. and y1.. (gate and up rows of the same units under SwiGLU); a
+                    // plain tile's second half that lies wholly past row N is not copied (its
+                    // accumulator columns are never stored)
+                    const int y0 = kSwiGLU ? n * BH : n * BN, y1 = kSwiGLU ? N / 2 + n * BH : n * BN + BH;
+                    const bool second = kSwiGLU || y1 < N;
+                    mbar_arrive_expect_tx(&S.full[s], A_BYTES + (second ? 2 : 1) * BH_BYTES);
                     tma_load_2d(a, &tmA, kb * BK, m * BM, &S.full[s]);
-                    tma_load_2d(a + A_BYTES, &tmB, kb * BK, n * BN, &S.full[s]);
+                    tma_load_2d(a + A_BYTES, &tmB, kb * BK, y0, &S.full[s]);
+                    if (second) tma_load_2d(a + A_BYTES + BH_BYTES, &tmB, kb * BK, y1, &S.full[s]);
                 }
             }
             if (S.abort_) {  // let the copies in flight land before the CTA exits
@@ -160,13 +176,34 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
             const bool ok = __all_sync(0xffffffffu, wait_phase(S, &S.acc_full[b], (lt >> 1) & 1u, deadline, err));
             if (!ok) break;
             tc_fence_after();
+            const uint32_t tacc = tmem + (uint32_t)b * BN + ((uint32_t)(32 * q) << 16);
+            if constexpr (kSwiGLU) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < BH; c0 += 32) {
+                    float g[32], v[32];
+                    tc_ld32(tacc + (uint32_t)c0, g);
+                    tc_ld32(tacc + (uint32_t)(BH + c0), v);
+                    if (row < M) {
+                        __half *dst = static_cast<__half *>(C) + (size_t)row * ldc + n * BH + c0;
+                        __align__(16) __half o[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float2half_rn(g[i] / (1.f + expf(-g[i])) * v[i]);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            reinterpret_cast<uint4 *>(dst)[i] = reinterpret_cast<const uint4 *>(o)[i];
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&S.acc_empty[b]);
+                continue;
+            }
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 float v[32];
-                tc_ld32(tmem + (uint32_t)b * BN + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
+                tc_ld32(tacc + (uint32_t)c0, v);
                 const int col = n * BN + c0;
                 if (row < M && col < N) {
-                    float *dst = C + (size_t)row * ldc + col;
+                    float *dst = static_cast<float *>(C) + (size_t)row * ldc + col;
                     if (col + 32 <= N && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
 #pragma unroll
                         for (int i = 0; i < 32; i += 4)
@@ -234,16 +271,18 @@ bool make_map(CUtensorMap *m, const __half *ptr, int rows, int K, int box_rows) 
 
 size_t tc_gemm_smem_bytes() { return TG_SMEM; }
 
-lf_status tc_gemm_f16(const __half *A, const __half *B, float *C, int M, int N, int K, int ldc, uint32_t *err,
-                      unsigned long long timeout_ns, cudaStream_t stream) {
-    if (!A || !B || !C || !err || M < 1 || N < 1 || K < BK || K % BK || ldc < N) return LF_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15)) return LF_ERR_INVALID_ARG;
+namespace {
+
+template <bool kSwiGLU>
+lf_status launch(const __half *A, const __half *B, void *C, int M, int N, int K, int ldc, uint32_t *err,
+                 unsigned long long timeout_ns, cudaStream_t stream) {
     CUtensorMap ma, mb;
-    if (!make_map(&ma, A, M, K, BM) || !make_map(&mb, B, N, K, BN)) return LF_ERR_CUDA;
+    if (!make_map(&ma, A, M, K, BM) || !make_map(&mb, B, N, K, BH)) return LF_ERR_CUDA;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TG_SMEM);
+        attr_err = cudaFuncSetAttribute(tc_gemm_kernel<kSwiGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)TG_SMEM);
     });
     if (attr_err != cudaSuccess) return LF_ERR_CUDA;
     static int n_sm = 0;
@@ -253,10 +292,29 @@ lf_status tc_gemm_f16(const __half *A, const __half *B, float *C, int M, int N, 
             cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1)
             return LF_ERR_CUDA;
     }
-    const int ntiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    tc_gemm_kernel<<<ntiles < n_sm ? ntiles : n_sm, TG_THREADS, TG_SMEM, stream>>>(ma, mb, C, M, N, K, ldc, err,
-                                                                                 timeout_ns);
+    const int nt = kSwiGLU ? N / BN : (N + BN - 1) / BN, ntiles = ((M + BM - 1) / BM) * nt;
+    tc_gemm_kernel<kSwiGLU><<<ntiles < n_sm ? ntiles : n_sm, TG_THREADS, TG_SMEM, stream>>>(ma, mb, C, M, N, K, ldc,
+                                                                                          err, timeout_ns);
     return cudaGetLastError() == cudaSuccess ? LF_OK : LF_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+lf_status tc_gemm_f16(const __half *A, const __half *B, float *C, int M, int N, int K, int ldc, uint32_t *err,
+                      unsigned long long timeout_ns, cudaStream_t stream) {
+    if (!A || !B || !C || !err || M < 1 || N < 1 || K < BK || K % BK || ldc < N) return LF_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B)) return LF_ERR_INVALID_ARG;
+    return launch<false>(A, B, C, M, N, K, ldc, err, timeout_ns, stream);
+}
+
+lf_status tc_gemm_swiglu_f16(const __half *A, const __half *Bgu, __half *U, int M, int F, int K, int ldu,
+                             uint32_t *err, unsigned long long timeout_ns, cudaStream_t stream) {
+    if (!A || !Bgu || !U || !err || M < 1 || F < BH || F % BH || K < BK || K % BK || ldu < F || ldu % 8)
+        return LF_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(Bgu) || !aligned16(U)) return LF_ERR_INVALID_ARG;
+    return launch<true>(A, Bgu, U, M, 2 * F, K, ldu, err, timeout_ns, stream);
 }
 
 }  // namespace lf

@@ -15,6 +15,12 @@ namespace lf {
 lf_status tc_gemm_f16(const __half *A, const __half *B, float *C, int M, int N, int K, int ldc, uint32_t *err,
                       unsigned long long timeout_ns, cudaStream_t stream);
 
+// U[M][F] (FP16, row stride ldu halves, a multiple of 8) = silu(A Wg^T) * (A Wu^T)
+// elementwise, where Bgu = [Wg; Wu] holds the F gate rows then the F up rows
+// (each K long).  F a multiple of 128; the fp32 products stay in TMEM.
+lf_status tc_gemm_swiglu_f16(const __half *A, const __half *Bgu, __half *U, int M, int F, int K, int ldu,
+                             uint32_t *err, unsigned long long timeout_ns, cudaStream_t stream);
+
 // Dynamic shared memory the GEMM kernel uses per CTA.
 size_t tc_gemm_smem_bytes();
 

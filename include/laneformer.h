@@ -306,6 +306,61 @@ lf_status lf_set_prefill_attention(lf_engine *e, int tensor_cores);
 lf_status lf_matmul_f16(const void *a_device, const void *b_device, float *c_device, int m, int n, int k,
                         void *cuda_stream);
 
+/* Batched decode for pass@N (News, "Performance and infrastructure":
+ * several sampled solutions per prompt): n_batch samples (1..16) continue
+ * the engine's current sequence together, one position per step, each with
+ * its own KV cache, so every weight byte streamed from HBM serves all of
+ * them.  Each sample computes the forward of lf_decode_step under the
+ * delayed lane sum (own_lane_immediate = 0; with 1 it is LF_ERR_UNSUPPORTED)
+ * with FP16 activations into tensor-core GEMVs, fp32 accumulation.
+ *
+ * lf_batch_begin copies positions [0, position) of the engine's KV cache
+ * into every sample's cache and sets the batch position to the engine's
+ * position; the engine's own sequence is untouched by the batch calls.  The
+ * batch state (about B * 4 * L * n_kv * ctx_cap * head_dim bytes of caches)
+ * is owned by the engine until lf_batch_end, lf_batch_begin or lf_destroy.
+ * LF_ERR_INVALID_ARG for n_batch outside 1..16; LF_ERR_NOT_LOADED before
+ * lf_load_weights; LF_ERR_CTX_OVERFLOW at position == ctx_cap;
+ * LF_ERR_UNSUPPORTED for shapes the batched kernels do not take (d_model,
+ * n_q_heads * head_dim or ffn_dim not a multiple of 64, 128 not a multiple
+ * of head_dim, more than 8 query heads per KV head); LF_ERR_OOM. */
+lf_status lf_batch_begin(lf_engine *e, int n_batch);
+lf_status lf_batch_end(lf_engine *e);
+/* *n_batch and *position of the current batch (0 and 0 when there is none). */
+lf_status lf_batch_info(const lf_engine *e, int *n_batch, int *position);
+
+/* One step of every sample: tokens (host, n_batch int32, required) at the
+ * batch position; logits (host, n_batch x vocab fp32, nullable) and argmax
+ * (host, n_batch int32, lowest index among equal maxima, nullable) per
+ * sample.  Synchronous; advances the batch position by one.
+ * LF_ERR_NOT_LOADED without lf_batch_begin; LF_ERR_INVALID_ARG for a token
+ * outside [0, vocab); LF_ERR_CTX_OVERFLOW at position == ctx_cap;
+ * LF_ERR_TIMEOUT / LF_ERR_CUDA poison the engine (and end the batch). */
+lf_status lf_batch_step(lf_engine *e, const int32_t *tokens, float *logits, int32_t *argmax);
+
+/* n_steps sampled steps of every sample, the draw of lf_generate_sampled:
+ * sample b draws with counter (position of the step, b), so sample b of a
+ * batch makes the same draws as lf_generate_sampled(..., sample = b) on the
+ * same logits.  first_tokens (host, n_batch int32) are the inputs of the
+ * first step; tokens_out (host, n_batch x n_steps int32, row b = sample b)
+ * receives the drawn tokens.  temperature 0 is greedy.  Synchronous;
+ * advances the batch position by n_steps.  Errors as lf_batch_step, plus
+ * LF_ERR_INVALID_ARG for temperature < 0 or top_p outside (0, 1] and
+ * LF_ERR_UNSUPPORTED for a vocabulary above 51200. */
+lf_status lf_batch_generate(lf_engine *e, const int32_t *first_tokens, int n_steps, float temperature, float top_p,
+                            uint64_t seed, int32_t *tokens_out);
+
+/* The tensor-core GEMV of the batched decode, exported for tests:
+ * y[b][r] = sum_k w[r][k] * x[b][k] for b < batch (1..16), r < n, with w
+ * (n x k) and x (batch x k) row-major FP16 DEVICE arrays (16-byte aligned)
+ * and y a batch x n row-major fp32 DEVICE array; k a multiple of 64.  The
+ * weights are streamed once; the reduction is split over the SMs and summed
+ * in a fixed order (deterministic).  Allocates its scratch per call; runs on
+ * `cuda_stream` (NULL = legacy stream) and waits for it.  LF_ERR_INVALID_ARG
+ * for bad sizes or pointers; LF_ERR_TIMEOUT if a device-side wait ran out. */
+lf_status lf_gemv_f16(const void *w_device, const void *x_device, float *y_device, int n, int k, int batch,
+                      void *cuda_stream);
+
 /* Host-only plan statistics for `n_sm` SMs (no GPU needed): stats[0] = weight
  * rows in the stream, [1] = min rows per SM, [2] = max rows per SM, [3] = ops
  * per step, [4] = 1 if every weight row of every lane appears exactly once,

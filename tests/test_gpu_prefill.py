@@ -65,6 +65,15 @@ def test_six_layers_and_single_token_prompt():
     assert_gates(rels, agree, "6 layers")
 
 
+def test_ffn_width_not_a_multiple_of_128():
+    # the gate/up GEMM fuses SwiGLU into its epilogue only when F is a
+    # multiple of 128; F = 320 takes the separate SwiGLU pass
+    shape = synth.TINY.replace(ffn_dim=320)
+    _, _, pre_rel, pre_agree, rels, agree = prefill_then_steps(shape, 6, 75, 4)
+    assert pre_rel <= REL_L2 and pre_agree
+    assert_gates(rels, agree, "F = 320")
+
+
 def test_prefill_after_decode_steps_and_kv_contents():
     shape = synth.TINY
     eng, orc, pre_rel, pre_agree, rels, agree = prefill_then_steps(shape, 9, 40, 3, lead=21)
