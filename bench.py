@@ -679,6 +679,8 @@ def run_generation(args, world, rank, local):
 
     if args.workload == "batch":
         fill, n_tok, sizes = BATCH_SWEEP
+        if args.batch:  # one batch size, at most 64 steps (profiling runs)
+            sizes, n_tok = (args.batch,), min(args.steps, n_tok)
         shape = base
         kv = synth.make_kv(shape, SEED, fill)
         first = synth.make_tokens(SEED + rank, 16, shape.vocab)
@@ -708,17 +710,18 @@ def run_generation(args, world, rank, local):
                                      "roofline_frac": gen_roofline(shape, fill, n_tok, ms, batch=B)["frac"]}
             eng.batch_end()
         clk = clocks.stop()
-        main_v = variants["B8"]
+        main_b = 8 if "B8" in variants else sizes[0]
+        main_v = variants[f"B{main_b}"]
         if rank == 0:
             line = {"metric": "batched greedy decode tokens/s (all samples) per batch size", "value": main_v["value"],
                     "steps": n_tok, "warmup": max(args.warmup, 3), "ms_per_step": main_v["ms_per_step"],
                     "data": data + ", N(0,1) KV fill",
                     "config": {"workload": f"batched decode: KV pre-filled N(0,1) to {fill} and shared by every "
                                            f"sample, then {n_tok} greedy steps of B samples together "
-                                           f"(lf_batch_generate) for B in {list(sizes)}; value at B = 8",
+                                           f"(lf_batch_generate) for B in {list(sizes)}; value at B = {main_b}",
                                "seed": SEED, "l2": "no flush: inputs larger than L2"},
                     "variants": variants,
-                    "roofline": gen_roofline(shape, fill, n_tok, main_v["ms_per_step"], batch=8),
+                    "roofline": gen_roofline(shape, fill, n_tok, main_v["ms_per_step"], batch=main_b),
                     "cpu_baseline": None, "e2e": None,
                     "gpu_launches": len(sizes) * n_tok * (7 * shape.n_layers + 6), "clocks": clk, **common}
             print(json.dumps(line), flush=True)
@@ -849,6 +852,8 @@ def main():
                     default="step",
                     help="step: the single-step microbench (default line); e2e / long / sweep: the "
                          "generation workloads")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="--workload batch: one batch size instead of the sweep (steps = min(--steps, 64))")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: same width with fewer layers (not a bench number)")
     args = ap.parse_args()

@@ -22,6 +22,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <array>
 #include <cfloat>
 #include <climits>
 #include <cmath>
@@ -46,13 +47,20 @@ struct BatchState {
     void *mem = nullptr;
     size_t bytes = 0;
     cudaStream_t cap = nullptr;
+    std::vector<cudaStream_t> work;  // one per sub-block in flight (2 d + 1)
     cudaGraphExec_t graph = nullptr;
-    // device buffers (carved from mem)
+    // device buffers (carved from mem); per sub-block / per layer so that
+    // sub-blocks in flight together share nothing they write
     int *tok = nullptr, *gen = nullptr, *am = nullptr, *d_pos = nullptr;
     int2 *kvsrc = nullptr;  // per KV head: (lane, head within the lane) of the engine cache that holds it
-    uint32_t *err = nullptr, *cnt = nullptr, *att_cnt = nullptr;
-    float *x = nullptr, *ring = nullptr, *q = nullptr, *logits = nullptr, *ws = nullptr, *att_ws = nullptr;
-    __half *h16 = nullptr, *o16 = nullptr, *u16 = nullptr, *kc = nullptr, *vc = nullptr;
+    uint32_t *err = nullptr, *cnt = nullptr, *att_cnt = nullptr;    // att_cnt [L][B * n_kv]
+    float *x = nullptr, *ring = nullptr, *logits = nullptr, *ws = nullptr;
+    float *q = nullptr, *att_ws = nullptr;                           // [L][B][NQ * DH], [L][...]
+    __half *h16 = nullptr, *o16 = nullptr, *u16 = nullptr;          // [2L + 1][B][D], [L][B][NQ * DH], [L][B][F]
+    __half *kc = nullptr, *vc = nullptr;
+    // split-K workspace and counters of each GEMV of the step (QKV, O, gate/up, down per layer, then LM head)
+    std::vector<size_t> ws_off;
+    std::vector<int> cnt_off;
     size_t ws_floats = 0;
     int n_cnt = 0;
 };
@@ -77,90 +85,132 @@ __global__ void ba_embed(const __half *__restrict__ emb, const int *__restrict__
     for (int c = threadIdx.x; c < D; c += blockDim.x) x[(size_t)blockIdx.x * D + c] = __half2float(e[c]);
 }
 
+// Raw FP16 storage of DPL consecutive head dimensions (one lane's share of a
+// K or V row) and its conversion to fp32.
+template <int DPL>
+struct Dims;
+template <>
+struct Dims<4> {
+    using raw = uint2;
+    __device__ static void cvt(raw r, float *f) {
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&r.x));
+        const float2 c = __half22float2(*reinterpret_cast<const __half2 *>(&r.y));
+        f[0] = a.x, f[1] = a.y, f[2] = c.x, f[3] = c.y;
+    }
+};
+template <>
+struct Dims<2> {
+    using raw = uint32_t;
+    __device__ static void cvt(raw r, float *f) {
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&r));
+        f[0] = a.x, f[1] = a.y;
+    }
+};
+template <>
+struct Dims<1> {
+    using raw = unsigned short;
+    __device__ static void cvt(raw r, float *f) { f[0] = __half2float(__ushort_as_half(r)); }
+};
+
 // Decode attention of one sample, one KV head and one split of its keys:
 // keys j in [max(0, p - W + 1), p] (W = 0: all) are cut into
-// kBatchAttnSplits near-equal ranges; the CTA scores its range for the GL
-// query heads of the KV head, keeps the unnormalised P V with the running
-// max and sum, and the last CTA of the (sample, KV head) to finish merges
-// the splits in split order into FP16 o.
+// kBatchAttnSplits near-equal ranges.  In the CTA each warp walks every
+// fourth key of the range, 4 keys per round with their K and V rows loaded
+// up front; a lane holds DPL = head_dim / 32 dimensions of the GL query
+// heads of the KV head (scaled q in registers), the score is a warp sum, and
+// the running max, sum and P V stay in registers (online softmax).  The
+// warps combine in shared memory into the split's (unnormalised o, max,
+// sum); the last CTA of the (sample, KV head) to finish merges the splits in
+// split order into FP16 o.
+template <int DPL, int GL>
 __global__ void __launch_bounds__(kBatchAttnThreads)
     ba_attn(const float *__restrict__ q, const __half *__restrict__ kc, const __half *__restrict__ vc,
-            const int *__restrict__ pos_word, int L, int l, int NKV, int GL, int DH, int ctx, int window, float scale,
+            const int *__restrict__ pos_word, int L, int l, int NKV, int ctx, int window, float scale,
             float *__restrict__ ws, uint32_t *__restrict__ cnt, __half *__restrict__ o) {
-    extern __shared__ float asm_[];  // qs [GL][DH], then sc [GL][per_max]
-    __shared__ float mh[8], lh[8];
+    constexpr int DH = 32 * DPL, NW = kBatchAttnThreads / 32, KR = 4;  // KR keys per warp per round
+    using D = Dims<DPL>;
+    __shared__ float red[NW][GL][DH + 2];
     __shared__ int last;
     const int g = blockIdx.x, b = blockIdx.y, split = blockIdx.z, S = gridDim.z;
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, NQ = NKV * GL;
-    const int per_max = (ctx + S - 1) / S;
-    float *qs = asm_, *sc = asm_ + GL * DH;
     const int p = *pos_word;
     const int jlo = window > 0 ? max(0, p - window + 1) : 0, n = p - jlo + 1, per = (n + S - 1) / S;
     const int j0 = jlo + split * per, nk = max(0, min(j0 + per, p + 1) - j0);
 
-    const float *qb = q + (size_t)b * NQ * DH + (size_t)g * GL * DH;
-    for (int i = tid; i < GL * DH; i += blockDim.x) qs[i] = qb[i];
-    __syncthreads();
+    float qr[GL][DPL], acc[GL][DPL], m[GL], ls[GL];
+    const float *qb = q + (size_t)b * NQ * DH + (size_t)g * GL * DH + lane * DPL;
+#pragma unroll
+    for (int h = 0; h < GL; ++h) {
+        m[h] = -INFINITY;
+        ls[h] = 0.f;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) {
+            qr[h][i] = qb[h * DH + i] * scale;
+            acc[h][i] = 0.f;
+        }
+    }
     const size_t head = (((size_t)b * L + l) * NKV + g) * ctx;
-    const __half *kh = kc + head * DH, *vh = vc + head * DH;
-    for (int jj = tid; jj < nk; jj += blockDim.x) {
-        const uint4 *kr = reinterpret_cast<const uint4 *>(kh + (size_t)(j0 + jj) * DH);
-        float acc[8];
-        for (int h = 0; h < GL; ++h) acc[h] = 0.f;
-        for (int c8 = 0; c8 < DH / 8; ++c8) {
-            const uint4 u = kr[c8];
-            const __half2 *hp = reinterpret_cast<const __half2 *>(&u);
-            float kf[8];
+    const __half *kh = kc + (head + j0) * DH + lane * DPL, *vh = vc + (head + j0) * DH + lane * DPL;
+    for (int base = 0; base < nk; base += NW * KR) {
+        typename D::raw kr[KR], vr[KR];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float2 f = __half22float2(hp[i]);
-                kf[2 * i] = f.x;
-                kf[2 * i + 1] = f.y;
+        for (int u = 0; u < KR; ++u) {
+            const int jj = base + w + NW * u;
+            if (jj < nk) {
+                kr[u] = *reinterpret_cast<const typename D::raw *>(kh + (size_t)jj * DH);
+                vr[u] = *reinterpret_cast<const typename D::raw *>(vh + (size_t)jj * DH);
             }
+        }
+#pragma unroll
+        for (int u = 0; u < KR; ++u) {
+            if (base + w + NW * u >= nk) break;  // warp-uniform
+            float kf[DPL], vf[DPL];
+            D::cvt(kr[u], kf);
+            D::cvt(vr[u], vf);
+#pragma unroll
             for (int h = 0; h < GL; ++h) {
-                const float *qh = qs + h * DH + c8 * 8;
+                float sc = 0.f;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[h] += kf[i] * qh[i];
+                for (int i = 0; i < DPL; ++i) sc += qr[h][i] * kf[i];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, off);
+                const float mn = fmaxf(m[h], sc), al = __expf(m[h] - mn), pe = __expf(sc - mn);
+                m[h] = mn;
+                ls[h] = ls[h] * al + pe;
+#pragma unroll
+                for (int i = 0; i < DPL; ++i) acc[h][i] = acc[h][i] * al + pe * vf[i];
             }
         }
-        for (int h = 0; h < GL; ++h) sc[h * per_max + jj] = acc[h] * scale;
     }
-    __syncthreads();
-    for (int h = w; h < GL; h += blockDim.x / 32) {  // one warp per head: max, exponentials, sum
-        float m = -INFINITY;
-        for (int jj = lane; jj < nk; jj += 32) m = fmaxf(m, sc[h * per_max + jj]);
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        float s = 0.f;
-        for (int jj = lane; jj < nk; jj += 32) {
-            const float e = expf(sc[h * per_max + jj] - m);
-            sc[h * per_max + jj] = e;
-            s += e;
-        }
+    for (int h = 0; h < GL; ++h) {
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        for (int i = 0; i < DPL; ++i) red[w][h][lane * DPL + i] = acc[h][i];
         if (lane == 0) {
-            mh[h] = m;
-            lh[h] = s;
+            red[w][h][DH] = m[h];
+            red[w][h][DH + 1] = ls[h];
         }
     }
     __syncthreads();
-    const int half = DH / 2;
     float *part = ws + (((size_t)b * NKV + g) * S + split) * GL * (DH + 2);
-    for (int i = tid; i < GL * half; i += blockDim.x) {
-        const int h = i / half, c2 = i % half;
-        float ox = 0.f, oy = 0.f;
-        const float *ph = sc + h * per_max;
-        for (int jj = 0; jj < nk; ++jj) {
-            const float2 v = __half22float2(reinterpret_cast<const __half2 *>(vh + (size_t)(j0 + jj) * DH)[c2]);
-            ox += ph[jj] * v.x;
-            oy += ph[jj] * v.y;
-        }
-        part[h * (DH + 2) + 2 * c2] = ox;
-        part[h * (DH + 2) + 2 * c2 + 1] = oy;
-        if (c2 == 0) {
-            part[h * (DH + 2) + DH] = nk > 0 ? mh[h] : -INFINITY;
-            part[h * (DH + 2) + DH + 1] = nk > 0 ? lh[h] : 0.f;
+    for (int i = tid; i < GL * DH; i += blockDim.x) {
+        const int h = i / DH, c = i % DH;
+        float M = -INFINITY;
+#pragma unroll
+        for (int v = 0; v < NW; ++v)
+            if (red[v][h][DH + 1] > 0.f) M = fmaxf(M, red[v][h][DH]);
+        float sum = 0.f, lt = 0.f;
+#pragma unroll
+        for (int v = 0; v < NW; ++v)
+            if (red[v][h][DH + 1] > 0.f) {
+                const float f = __expf(red[v][h][DH] - M);
+                sum += f * red[v][h][c];
+                lt += f * red[v][h][DH + 1];
+            }
+        part[h * (DH + 2) + c] = sum;
+        if (c == 0) {
+            part[h * (DH + 2) + DH] = M;
+            part[h * (DH + 2) + DH + 1] = lt;
         }
     }
     __threadfence();
@@ -185,14 +235,38 @@ __global__ void __launch_bounds__(kBatchAttnThreads)
         float num = 0.f, den = 0.f;
         for (int s = 0; s < S; ++s) {
             const float *ps = all + ((size_t)s * GL + h) * (DH + 2);
-            const float ls = __ldcg(ps + DH + 1);
-            if (ls > 0.f) {
-                const float f = expf(__ldcg(ps + DH) - M);
+            const float lsp = __ldcg(ps + DH + 1);
+            if (lsp > 0.f) {
+                const float f = __expf(__ldcg(ps + DH) - M);
                 num += f * __ldcg(ps + c);
-                den += f * ls;
+                den += f * lsp;
             }
         }
         o[(size_t)b * NQ * DH + (size_t)(g * GL + h) * DH + c] = __float2half_rn(num / den);
+    }
+}
+
+using AttnFn = void (*)(const float *, const __half *, const __half *, const int *, int, int, int, int, int, float,
+                        float *, uint32_t *, __half *);
+
+// The instance for head_dim / group size, or null when there is none.
+template <int DPL>
+AttnFn attn_for_group(int GL) {
+    switch (GL) {
+        case 1: return ba_attn<DPL, 1>;
+        case 2: return ba_attn<DPL, 2>;
+        case 4: return ba_attn<DPL, 4>;
+        case 8: return ba_attn<DPL, 8>;
+        default: return nullptr;
+    }
+}
+
+AttnFn attn_kernel(int DH, int GL) {
+    switch (DH) {
+        case 32: return attn_for_group<1>(GL);
+        case 64: return attn_for_group<2>(GL);
+        case 128: return attn_for_group<4>(GL);
+        default: return nullptr;
     }
 }
 
@@ -255,9 +329,22 @@ __global__ void ba_copy_prefix(const __half *__restrict__ ekc, const __half *__r
 
 size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
 
-size_t attn_smem(const lf::Shape &s) {
-    const int GL = s.NQ / s.NKV, per_max = (s.ctx + lf::kBatchAttnSplits - 1) / lf::kBatchAttnSplits;
-    return (size_t)GL * (s.DH + per_max) * sizeof(float);
+size_t att_ws_floats(const lf::Shape &s, int B) {
+    return (size_t)B * s.NKV * lf::kBatchAttnSplits * (s.NQ / s.NKV) * (s.DH + 2);
+}
+
+// The GEMV shapes of one step, in order: per layer QKV, O, gate/up, down; then the LM head.
+std::vector<std::array<int, 3>> gemv_shapes(const lf::Shape &s) {
+    const int QD = s.NQ * s.DH, QKVN = (s.NQ + 2 * s.NKV) * s.DH;
+    std::vector<std::array<int, 3>> v;
+    for (int l = 0; l < s.L; ++l) {
+        v.push_back({QKVN, s.D, lf::GEMV_QKV});
+        v.push_back({s.D, QD, lf::GEMV_F32});
+        v.push_back({2 * s.F, s.D, lf::GEMV_SWIGLU});
+        v.push_back({s.D, s.F, lf::GEMV_F32});
+    }
+    v.push_back({s.V, s.D, lf::GEMV_F32});
+    return v;
 }
 
 // The buffers of a batch of B, carved from one allocation (base null: sizes only).
@@ -268,9 +355,8 @@ void carve(BatchState &b, uint8_t *base, const lf::Shape &s, int B) {
         at += al256(bytes);
         return p;
     };
-    const size_t D = s.D, QD = (size_t)s.NQ * s.DH, F = s.F, V = s.V, R = 2 * (size_t)s.delay + 1;
+    const size_t D = s.D, QD = (size_t)s.NQ * s.DH, F = s.F, V = s.V, R = 2 * (size_t)s.delay + 1, L = s.L;
     const size_t kv = (size_t)B * s.L * s.NKV * s.ctx * s.DH;
-    const int GL = s.NQ / s.NKV;
     b.tok = reinterpret_cast<int *>(take(B * sizeof(int)));
     b.gen = reinterpret_cast<int *>(take((size_t)B * s.ctx * sizeof(int)));
     b.am = reinterpret_cast<int *>(take(B * sizeof(int)));
@@ -278,16 +364,16 @@ void carve(BatchState &b, uint8_t *base, const lf::Shape &s, int B) {
     b.kvsrc = reinterpret_cast<int2 *>(take(s.NKV * sizeof(int2)));
     b.err = reinterpret_cast<uint32_t *>(take(sizeof(uint32_t)));
     b.cnt = reinterpret_cast<uint32_t *>(take((size_t)b.n_cnt * sizeof(uint32_t)));
-    b.att_cnt = reinterpret_cast<uint32_t *>(take((size_t)B * s.NKV * sizeof(uint32_t)));
+    b.att_cnt = reinterpret_cast<uint32_t *>(take(L * B * s.NKV * sizeof(uint32_t)));
     b.x = reinterpret_cast<float *>(take(B * D * 4));
     b.ring = reinterpret_cast<float *>(take(R * B * D * 4));
-    b.q = reinterpret_cast<float *>(take(B * QD * 4));
+    b.q = reinterpret_cast<float *>(take(L * B * QD * 4));
     b.logits = reinterpret_cast<float *>(take(B * V * 4));
     b.ws = reinterpret_cast<float *>(take(std::max<size_t>(b.ws_floats, 1) * 4));
-    b.att_ws = reinterpret_cast<float *>(take((size_t)B * s.NKV * lf::kBatchAttnSplits * GL * (s.DH + 2) * 4));
-    b.h16 = reinterpret_cast<__half *>(take(B * D * 2));
-    b.o16 = reinterpret_cast<__half *>(take(B * QD * 2));
-    b.u16 = reinterpret_cast<__half *>(take(B * F * 2));
+    b.att_ws = reinterpret_cast<float *>(take(L * att_ws_floats(s, B) * 4));
+    b.h16 = reinterpret_cast<__half *>(take((2 * L + 1) * B * D * 2));
+    b.o16 = reinterpret_cast<__half *>(take(L * B * QD * 2));
+    b.u16 = reinterpret_cast<__half *>(take(L * B * F * 2));
     b.kc = reinterpret_cast<__half *>(take(kv * 2));
     b.vc = reinterpret_cast<__half *>(take(kv * 2));
     b.bytes = at;
@@ -297,39 +383,71 @@ void batch_release(BatchState *b) {
     if (!b) return;
     if (b->graph) cudaGraphExecDestroy(b->graph);
     if (b->cap) cudaStreamDestroy(b->cap);
+    for (cudaStream_t w : b->work)
+        if (w) cudaStreamDestroy(w);
     if (b->mem) cudaFree(b->mem);
     delete b;
 }
 
-// Every kernel of one step, in order, on `st` (captured into the graph).
-lf_status enqueue_batch_step(lf_engine *e, BatchState &b, cudaStream_t st) {
+// Every kernel of one step, captured from `main` into the graph.  Under the
+// delayed sum, sub-block s reads only the partials of sub-blocks up to
+// s - 1 - 2d, so its chain (GEMV, attention, GEMV) runs on worker stream
+// s mod (2d + 1) after its own add + norm, and the add + norm of a later
+// sub-block waits only for the partial it adds: up to 2d + 1 sub-blocks are
+// in flight and their GEMVs overlap on the GPU.  The adds + norms stay in
+// order on `main` (they update the residual in place).
+lf_status enqueue_batch_step(lf_engine *e, BatchState &b, cudaStream_t main) {
     const lf::Shape &s = e->plan.sh;
-    const int B = b.B, D = s.D, L = s.L, R = 2 * s.delay + 1, QD = s.NQ * s.DH, QKVN = (s.NQ + 2 * s.NKV) * s.DH;
+    const int B = b.B, D = s.D, L = s.L, R = 2 * s.delay + 1, QD = s.NQ * s.DH, GL = s.NQ / s.NKV;
     const float eps = e->cfg.rms_eps, scale = (float)(1.0 / std::sqrt((double)s.DH));
     const size_t BD = (size_t)B * D;
-    lf::GemvArgs base;
-    base.B = B;
-    base.ws = b.ws;
-    base.ws_floats = b.ws_floats;
-    base.cnt = b.cnt;
-    base.n_cnt = b.n_cnt;
-    base.err = b.err;
-    base.timeout_ns = kBatchTimeoutNs;
-
-    ba_embed<<<B, 256, 0, st>>>(e->emb, b.tok, b.x, D, s.V, b.err);
-    for (int sb = 0; sb < 2 * L; ++sb) {
+    const std::vector<std::array<int, 3>> shapes = gemv_shapes(s);
+    const AttnFn attn = attn_kernel(s.DH, GL);
+    auto gemv_args = [&](int i) {
+        lf::GemvArgs a;
+        a.N = shapes[i][0];
+        a.K = shapes[i][1];
+        a.mode = shapes[i][2];
+        a.B = B;
+        a.ws = b.ws + b.ws_off[i];
+        a.ws_floats = b.ws_off[i + 1] - b.ws_off[i];
+        a.cnt = b.cnt + b.cnt_off[i];
+        a.n_cnt = b.cnt_off[i + 1] - b.cnt_off[i];
+        a.err = b.err;
+        a.timeout_ns = kBatchTimeoutNs;
+        return a;
+    };
+    std::vector<cudaEvent_t> ev_norm(2 * L), ev_part(2 * L);
+    auto destroy = [&] {
+        for (cudaEvent_t v : ev_norm)
+            if (v) cudaEventDestroy(v);
+        for (cudaEvent_t v : ev_part)
+            if (v) cudaEventDestroy(v);
+    };
+    for (int i = 0; i < 2 * L; ++i)
+        if (cudaEventCreateWithFlags(&ev_norm[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ev_part[i], cudaEventDisableTiming) != cudaSuccess) {
+            destroy();
+            return LF_ERR_CUDA;
+        }
+    lf_status gs = LF_OK;
+    ba_embed<<<B, 256, 0, main>>>(e->emb, b.tok, b.x, D, s.V, b.err);
+    for (int sb = 0; sb < 2 * L && gs == LF_OK; ++sb) {
         const int l = sb / 2, ua = sb - 1 - 2 * s.delay;
         const __half *lw = e->blob + s.off_layer0 + (long long)l * s.per_layer;
-        float *P = b.ring + (size_t)(sb % R) * BD;
+        __half *h = b.h16 + (size_t)sb * BD;
         const __half *gain = e->gains + (size_t)(sb % 2 == 0 ? l : L + l) * D;
-        pf_addnorm<<<B, kNormThreads, 0, st>>>(b.x, b.ring, BD, ua, ua >= 0 ? 1 : 0, R, gain, b.h16, D, eps);
-        lf_status gs;
+        if (ua >= 0) cudaStreamWaitEvent(main, ev_part[ua], 0);
+        pf_addnorm<<<B, kNormThreads, 0, main>>>(b.x, b.ring, BD, ua, ua >= 0 ? 1 : 0, R, gain, h, D, eps);
+        cudaEventRecord(ev_norm[sb], main);
+        cudaStream_t w = b.work[sb % R];
+        cudaStreamWaitEvent(w, ev_norm[sb], 0);
+        float *P = b.ring + (size_t)(sb % R) * BD;
         if (sb % 2 == 0) {
-            lf::GemvArgs a = base;
-            a.N = QKVN;
-            a.K = D;
-            a.mode = lf::GEMV_QKV;
-            a.q = b.q;
+            float *q = b.q + (size_t)l * B * QD;
+            __half *o16 = b.o16 + (size_t)l * B * QD;
+            lf::GemvArgs a = gemv_args(4 * l);
+            a.q = q;
             a.rope = e->rope;
             a.kc = b.kc;
             a.vc = b.vc;
@@ -340,45 +458,45 @@ lf_status enqueue_batch_step(lf_engine *e, BatchState &b, cudaStream_t st) {
             a.L = L;
             a.l = l;
             a.ctx = s.ctx;
-            if ((gs = lf::gemv_tc(lw + s.o_wq, b.h16, a, st)) != LF_OK) return gs;
-            const dim3 ag(s.NKV, B, lf::kBatchAttnSplits);
-            ba_attn<<<ag, lf::kBatchAttnThreads, attn_smem(s), st>>>(b.q, b.kc, b.vc, b.d_pos, L, l, s.NKV,
-                                                                    s.NQ / s.NKV, s.DH, s.ctx, e->cfg.swa_window[l],
-                                                                    scale, b.att_ws, b.att_cnt, b.o16);
-            a = base;
-            a.N = D;
-            a.K = QD;
+            if ((gs = lf::gemv_tc(lw + s.o_wq, h, a, w)) != LF_OK) break;
+            attn<<<dim3(s.NKV, B, lf::kBatchAttnSplits), lf::kBatchAttnThreads, 0, w>>>(
+                q, b.kc, b.vc, b.d_pos, L, l, s.NKV, s.ctx, e->cfg.swa_window[l], scale,
+                b.att_ws + (size_t)l * att_ws_floats(s, B), b.att_cnt + (size_t)l * B * s.NKV, o16);
+            a = gemv_args(4 * l + 1);
             a.y = P;
             a.ldy = D;
-            if ((gs = lf::gemv_tc(lw + s.o_wo, b.o16, a, st)) != LF_OK) return gs;
+            if ((gs = lf::gemv_tc(lw + s.o_wo, o16, a, w)) != LF_OK) break;
         } else {
-            lf::GemvArgs a = base;
-            a.N = 2 * s.F;
-            a.K = D;
-            a.mode = lf::GEMV_SWIGLU;
-            a.u = b.u16;
+            __half *u16 = b.u16 + (size_t)l * B * s.F;
+            lf::GemvArgs a = gemv_args(4 * l + 2);
+            a.u = u16;
             a.ldu = s.F;
-            if ((gs = lf::gemv_tc(lw + s.o_wg, b.h16, a, st)) != LF_OK) return gs;
-            a = base;
-            a.N = D;
-            a.K = s.F;
+            if ((gs = lf::gemv_tc(lw + s.o_wg, h, a, w)) != LF_OK) break;
+            a = gemv_args(4 * l + 3);
             a.y = P;
             a.ldy = D;
-            if ((gs = lf::gemv_tc(lw + s.o_wd, b.u16, a, st)) != LF_OK) return gs;
+            if ((gs = lf::gemv_tc(lw + s.o_wd, u16, a, w)) != LF_OK) break;
         }
+        cudaEventRecord(ev_part[sb], w);
     }
-    const int u0 = std::max(0, 2 * L - 1 - 2 * s.delay);
-    pf_addnorm<<<B, kNormThreads, 0, st>>>(b.x, b.ring, BD, u0, 2 * L - u0, R, e->gains + (size_t)2 * L * D, b.h16,
-                                           D, eps);
-    lf::GemvArgs a = base;
-    a.N = s.V;
-    a.K = D;
-    a.y = b.logits;
-    a.ldy = s.V;
-    lf_status gs = lf::gemv_tc(e->blob + s.off_lm, b.h16, a, st);
+    if (gs == LF_OK) {
+        // drain: the partials not yet in the residual (every worker joins back here)
+        const int u0 = std::max(0, 2 * L - 1 - 2 * s.delay);
+        for (int u = u0; u < 2 * L; ++u) cudaStreamWaitEvent(main, ev_part[u], 0);
+        __half *h = b.h16 + (size_t)2 * L * BD;
+        pf_addnorm<<<B, kNormThreads, 0, main>>>(b.x, b.ring, BD, u0, 2 * L - u0, R, e->gains + (size_t)2 * L * D,
+                                                 h, D, eps);
+        lf::GemvArgs a = gemv_args(4 * L);
+        a.y = b.logits;
+        a.ldy = s.V;
+        gs = lf::gemv_tc(e->blob + s.off_lm, h, a, main);
+    }
+    if (gs == LF_OK) {
+        ba_argmax<<<B, 1024, 0, main>>>(b.logits, s.V, b.am);
+        ba_bump<<<1, 1, 0, main>>>(b.d_pos);
+    }
+    destroy();
     if (gs != LF_OK) return gs;
-    ba_argmax<<<B, 1024, 0, st>>>(b.logits, s.V, b.am);
-    ba_bump<<<1, 1, 0, st>>>(b.d_pos);
     return cudaGetLastError() == cudaSuccess ? LF_OK : LF_ERR_CUDA;
 }
 
@@ -418,26 +536,25 @@ extern "C" lf_status lf_batch_begin(lf_engine *e, int n_batch) {
     if (!e->blob) return LF_ERR_OOM;
     const lf::Shape &s = e->plan.sh;
     if (s.own || s.D % 64 || (s.NQ * s.DH) % 64 || s.F % 64 || 128 % s.DH || ((s.NQ + 2 * s.NKV) * s.DH) % 128 ||
-        s.D > 4 * kNormV * kNormThreads || s.NQ / s.NKV > 8 || s.NQ % s.NKV || attn_smem(s) > 200 * 1024)
+        s.D > 4 * kNormV * kNormThreads || s.NQ % s.NKV || !attn_kernel(s.DH, s.NQ / s.NKV))
         return LF_ERR_UNSUPPORTED;
     if (e->pos >= s.ctx) return LF_ERR_CTX_OVERFLOW;
     lf_batch_free(e);
     BatchState *b = new BatchState();
     b->B = n_batch;
-    // split-K workspace: the largest need over the step's GEMVs
-    const int QD = s.NQ * s.DH, QKVN = (s.NQ + 2 * s.NKV) * s.DH;
-    const int shapes[5][3] = {{QKVN, s.D, lf::GEMV_QKV},
-                              {s.D, QD, lf::GEMV_F32},
-                              {2 * s.F, s.D, lf::GEMV_SWIGLU},
-                              {s.D, s.F, lf::GEMV_F32},
-                              {s.V, s.D, lf::GEMV_F32}};
+    // split-K workspace and counters: a region per GEMV of the step
+    const std::vector<std::array<int, 3>> shapes = gemv_shapes(s);
+    b->ws_off.assign(1, 0);
+    b->cnt_off.assign(1, 0);
     for (auto &sh : shapes) {
         size_t wf = 0;
         int nc = 0;
         lf::gemv_tc_needs(sh[0], sh[1], sh[2], &wf, &nc);
-        b->ws_floats = std::max(b->ws_floats, wf);
-        b->n_cnt = std::max(b->n_cnt, nc);
+        b->ws_off.push_back(b->ws_off.back() + ((wf + 63) & ~size_t(63)));
+        b->cnt_off.push_back(b->cnt_off.back() + nc);
     }
+    b->ws_floats = b->ws_off.back();
+    b->n_cnt = b->cnt_off.back();
     carve(*b, nullptr, s, n_batch);
     if (cudaMalloc(&b->mem, b->bytes) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -452,13 +569,8 @@ extern "C" lf_status lf_batch_begin(lf_engine *e, int n_batch) {
     for (int kh = 0; kh < s.NKV; ++kh)
         for (int lam = s.NL - 1; lam >= 0; --lam)
             if (s.kv_first[lam] <= kh && kh < s.kv_first[lam] + s.HKV_L) kvsrc[kh] = make_int2(lam, kh - s.kv_first[lam]);
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(ba_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    });
     cudaStream_t st = e->stream;
-    cudaError_t err = lf::gemv_tc_prepare() == LF_OK ? attr : cudaErrorUnknown;
+    cudaError_t err = lf::gemv_tc_prepare() == LF_OK ? cudaSuccess : cudaErrorUnknown;
     if (err == cudaSuccess) err = cudaMemsetAsync(b->mem, 0, b->bytes, st);
     if (err == cudaSuccess) err = cudaMemcpyAsync(b->kvsrc, kvsrc.data(), kvsrc.size() * sizeof(int2), cudaMemcpyHostToDevice, st);
     b->pos = e->pos;
@@ -472,6 +584,12 @@ extern "C" lf_status lf_batch_begin(lf_engine *e, int n_batch) {
 
     // capture one step
     if (cudaStreamCreateWithFlags(&b->cap, cudaStreamNonBlocking) != cudaSuccess) return batch_fail(e, LF_ERR_CUDA);
+    b->work.assign(2 * s.delay + 1, nullptr);
+    for (cudaStream_t &w : b->work)
+        if (cudaStreamCreateWithFlags(&w, cudaStreamNonBlocking) != cudaSuccess) {
+            w = nullptr;
+            return batch_fail(e, LF_ERR_CUDA);
+        }
     if (cudaStreamBeginCapture(b->cap, cudaStreamCaptureModeRelaxed) != cudaSuccess) return batch_fail(e, LF_ERR_CUDA);
     const lf_status qs = enqueue_batch_step(e, *b, b->cap);
     cudaGraph_t g = nullptr;
