@@ -224,23 +224,35 @@ __global__ void __launch_bounds__(kBatchAttnThreads)
     __syncthreads();
     if (!last) return;
     __threadfence();
+    // merge: every split's max and sum to shared memory at once, then per
+    // output the splits' P V loads in flight together, summed in split order
+    constexpr int SM = lf::kBatchAttnSplits;
+    __shared__ float fs[SM][GL], ls_all[SM][GL];
     const float *all = ws + ((size_t)b * NKV + g) * S * GL * (DH + 2);
+    if (tid < SM * GL) {
+        const int sp = tid / GL, h = tid % GL;
+        const float *ps = all + ((size_t)sp * GL + h) * (DH + 2);
+        fs[sp][h] = sp < S ? __ldcg(ps + DH) : -INFINITY;
+        ls_all[sp][h] = sp < S ? __ldcg(ps + DH + 1) : 0.f;
+    }
+    __syncthreads();
+    if (tid < GL) {  // per head: the max over splits with keys, then each split's weight
+        float M = -INFINITY;
+        for (int sp = 0; sp < SM; ++sp)
+            if (ls_all[sp][tid] > 0.f) M = fmaxf(M, fs[sp][tid]);
+        for (int sp = 0; sp < SM; ++sp) fs[sp][tid] = ls_all[sp][tid] > 0.f ? __expf(fs[sp][tid] - M) : 0.f;
+    }
+    __syncthreads();
     for (int i = tid; i < GL * DH; i += blockDim.x) {
         const int h = i / DH, c = i % DH;
-        float M = -INFINITY;
-        for (int s = 0; s < S; ++s) {
-            const float *ps = all + ((size_t)s * GL + h) * (DH + 2);
-            if (__ldcg(ps + DH + 1) > 0.f) M = fmaxf(M, __ldcg(ps + DH));
-        }
+        float ov[SM];
+#pragma unroll
+        for (int sp = 0; sp < SM; ++sp) ov[sp] = sp < S ? __ldcg(all + ((size_t)sp * GL + h) * (DH + 2) + c) : 0.f;
         float num = 0.f, den = 0.f;
-        for (int s = 0; s < S; ++s) {
-            const float *ps = all + ((size_t)s * GL + h) * (DH + 2);
-            const float lsp = __ldcg(ps + DH + 1);
-            if (lsp > 0.f) {
-                const float f = __expf(__ldcg(ps + DH) - M);
-                num += f * __ldcg(ps + c);
-                den += f * lsp;
-            }
+#pragma unroll
+        for (int sp = 0; sp < SM; ++sp) {
+            num += fs[sp][h] * ov[sp];
+            den += fs[sp][h] * ls_all[sp][h];
         }
         o[(size_t)b * NQ * DH + (size_t)(g * GL + h) * DH + c] = __float2half_rn(num / den);
     }

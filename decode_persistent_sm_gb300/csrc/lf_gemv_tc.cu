@@ -34,12 +34,13 @@ namespace lf {
 namespace {
 
 constexpr int GV_BM = 128, GV_BH = 64, GV_BK = 64, GV_NB = kGemvMaxBatch;
-constexpr int GV_STAGES = 10;
+constexpr int GV_STAGES = 5;  // ~100 KB of shared memory: two CTAs per SM
 constexpr int GV_HALF_BYTES = GV_BH * GV_BK * 2;   // 64 rows of W
 constexpr int GV_A_BYTES = 2 * GV_HALF_BYTES;      // 128 rows of W
 constexpr int GV_X_BYTES = GV_NB * GV_BK * 2;      // 16 rows of X
 constexpr int GV_STAGE_BYTES = GV_A_BYTES + GV_X_BYTES;  // 18 KB, a multiple of 1024
 constexpr int GV_THREADS = 192;
+constexpr int kCtasPerSm = 2;  // grid: two CTAs per SM, so one CTA's ramp overlaps the other's stream
 constexpr uint32_t GV_TMEM_COLS = 32;  // two 16-column accumulators
 constexpr size_t GV_SMEM = (size_t)GV_STAGES * GV_STAGE_BYTES + GV_NB * GV_BM * 4 + 256 + 1024;
 constexpr uint32_t kGvIdesc = idesc_f16(GV_BM, GV_NB);
@@ -100,7 +101,7 @@ __device__ __forceinline__ void tile_rows(const GemvArgs &a, int t, int &y0, int
     }
 }
 
-__global__ void __launch_bounds__(GV_THREADS, 1)
+__global__ void __launch_bounds__(GV_THREADS, 2)
     gemv_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ GemvArgs a, int maxseg) {
     extern __shared__ __align__(1024) uint8_t gv_raw[];
@@ -210,7 +211,9 @@ __global__ void __launch_bounds__(GV_THREADS, 1)
             const int nseg = owner((long long)t * tl.nk + tl.nk - 1, tl.G, grid) - first + 1;
             if (nseg > 1) {
                 float *slot = a.ws + ((size_t)t * maxseg + (c - first)) * GV_NB * GV_BM;
-                for (int bb = 0; bb < a.B; ++bb) slot[(size_t)bb * GV_BM + r] = v[bb];
+#pragma unroll
+                for (int bb = 0; bb < GV_NB; ++bb)
+                    if (bb < a.B) slot[(size_t)bb * GV_BM + r] = v[bb];
                 __threadfence();
                 epi_sync();
                 if (et == 0) {
@@ -226,20 +229,38 @@ __global__ void __launch_bounds__(GV_THREADS, 1)
                     continue;
                 }
                 __threadfence();
-                for (int bb = 0; bb < a.B; ++bb) {
-                    const float *base = a.ws + (size_t)t * maxseg * GV_NB * GV_BM + (size_t)bb * GV_BM + r;
-                    float acc = 0.f;
-                    for (int j = 0; j < nseg; ++j) acc += __ldcg(base + (size_t)j * GV_NB * GV_BM);
-                    v[bb] = acc;
+                // slot order j = 0, 1, ..; the loads of one slot (every batch row) are in flight together
+                const float *base = a.ws + (size_t)t * maxseg * GV_NB * GV_BM + r;
+#pragma unroll
+                for (int bb = 0; bb < GV_NB; ++bb) v[bb] = 0.f;
+                constexpr int JU = 4;  // slots loaded per round
+                for (int j0 = 0; j0 < nseg; j0 += JU) {
+                    float part[JU][GV_NB];
+#pragma unroll
+                    for (int jj = 0; jj < JU; ++jj)
+#pragma unroll
+                        for (int bb = 0; bb < GV_NB; ++bb)
+                            part[jj][bb] = bb < a.B && j0 + jj < nseg
+                                               ? __ldcg(base + ((size_t)(j0 + jj) * GV_NB + bb) * GV_BM)
+                                               : 0.f;
+#pragma unroll
+                    for (int jj = 0; jj < JU; ++jj)
+#pragma unroll
+                        for (int bb = 0; bb < GV_NB; ++bb) v[bb] += part[jj][bb];
                 }
             }
 
             if (a.mode == GEMV_F32) {
                 const int row = t * GV_BM + r;
-                if (row < a.N)
-                    for (int bb = 0; bb < a.B; ++bb) a.y[(size_t)bb * a.ldy + row] = v[bb];
+                if (row < a.N) {
+#pragma unroll
+                    for (int bb = 0; bb < GV_NB; ++bb)
+                        if (bb < a.B) a.y[(size_t)bb * a.ldy + row] = v[bb];
+                }
             } else {
-                for (int bb = 0; bb < a.B; ++bb) xch[bb * GV_BM + r] = v[bb];
+#pragma unroll
+                for (int bb = 0; bb < GV_NB; ++bb)
+                    if (bb < a.B) xch[bb * GV_BM + r] = v[bb];
                 epi_sync();
                 if (a.mode == GEMV_SWIGLU) {
                     if (r < GV_BH) {
@@ -355,7 +376,7 @@ lf_status gemv_tc_prepare() {
 
 void gemv_tc_needs(int N, int K, int mode, size_t *ws_floats, int *n_cnt) {
     const Tiling tl = tiling(N, K, mode);
-    const int nsm = sm_count();
+    const int nsm = kCtasPerSm * sm_count();
     const int grid = (int)(tl.G < nsm ? tl.G : nsm);
     const int ms = grid > 0 ? max_segments(tl, grid) : 1;
     *ws_floats = ms > 1 ? (size_t)tl.T * ms * GV_NB * GV_BM : 0;
@@ -371,7 +392,7 @@ lf_status gemv_tc(const __half *W, const __half *X, const GemvArgs &a, cudaStrea
     if (a.mode == GEMV_QKV && (!a.q || !a.kc || !a.vc || !a.rope || !a.pos || a.DH < 2 || GV_BM % a.DH ||
                                a.N != (a.NQ + 2 * a.NKV) * a.DH || a.N % GV_BM))
         return LF_ERR_INVALID_ARG;
-    const int nsm = sm_count();
+    const int nsm = kCtasPerSm * sm_count();
     if (nsm < 1) return LF_ERR_CUDA;
     const Tiling tl = tiling(a.N, a.K, a.mode);
     const int grid = (int)(tl.G < nsm ? tl.G : nsm);
