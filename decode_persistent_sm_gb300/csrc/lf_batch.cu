@@ -359,6 +359,52 @@ std::vector<std::array<int, 3>> gemv_shapes(const lf::Shape &s) {
     return v;
 }
 
+// Byte offsets of each step GEMV's weights in the engine's streaming-layout
+// copy (one entry per GEMV of gemv_shapes, then the total).
+std::vector<size_t> tiled_offsets(const lf::Shape &s) {
+    std::vector<size_t> off(1, 0);
+    for (auto &sh : gemv_shapes(s)) off.push_back(off.back() + lf::gemv_tiled_bytes(sh[0], sh[1], sh[2]));
+    return off;
+}
+
+// The row-major FP16 weights of each step GEMV in the engine's blob.
+std::vector<const __half *> gemv_weights(const lf_engine *e) {
+    const lf::Shape &s = e->plan.sh;
+    std::vector<const __half *> w;
+    for (int l = 0; l < s.L; ++l) {
+        const __half *lw = e->blob + s.off_layer0 + (long long)l * s.per_layer;
+        w.push_back(lw + s.o_wq);
+        w.push_back(lw + s.o_wo);
+        w.push_back(lw + s.o_wg);
+        w.push_back(lw + s.o_wd);
+    }
+    w.push_back(e->blob + s.off_lm);
+    return w;
+}
+
+// Builds the streaming-layout copy of every step GEMV's weights once per
+// loaded blob (about the size of the weights).
+lf_status ensure_tiled(lf_engine *e) {
+    if (e->wtile_ok) return LF_OK;
+    const lf::Shape &s = e->plan.sh;
+    const std::vector<size_t> off = tiled_offsets(s);
+    if (!e->wtile && cudaMalloc(&e->wtile, off.back()) != cudaSuccess) {
+        (void)cudaGetLastError();
+        e->wtile = nullptr;
+        return LF_ERR_OOM;
+    }
+    const auto shapes = gemv_shapes(s);
+    const auto w = gemv_weights(e);
+    for (size_t i = 0; i < shapes.size(); ++i) {
+        const lf_status st = lf::gemv_tile_weights(w[i], shapes[i][0], shapes[i][1], shapes[i][2],
+                                                   static_cast<uint8_t *>(e->wtile) + off[i], e->stream);
+        if (st != LF_OK) return st;
+    }
+    if (cudaStreamSynchronize(e->stream) != cudaSuccess) return LF_ERR_CUDA;
+    e->wtile_ok = true;
+    return LF_OK;
+}
+
 // The buffers of a batch of B, carved from one allocation (base null: sizes only).
 void carve(BatchState &b, uint8_t *base, const lf::Shape &s, int B) {
     size_t at = 0;
@@ -414,6 +460,8 @@ lf_status enqueue_batch_step(lf_engine *e, BatchState &b, cudaStream_t main) {
     const float eps = e->cfg.rms_eps, scale = (float)(1.0 / std::sqrt((double)s.DH));
     const size_t BD = (size_t)B * D;
     const std::vector<std::array<int, 3>> shapes = gemv_shapes(s);
+    const std::vector<size_t> toff = tiled_offsets(s);
+    auto wt = [&](int i) { return static_cast<const uint8_t *>(e->wtile) + toff[i]; };
     const AttnFn attn = attn_kernel(s.DH, GL);
     auto gemv_args = [&](int i) {
         lf::GemvArgs a;
@@ -446,7 +494,6 @@ lf_status enqueue_batch_step(lf_engine *e, BatchState &b, cudaStream_t main) {
     ba_embed<<<B, 256, 0, main>>>(e->emb, b.tok, b.x, D, s.V, b.err);
     for (int sb = 0; sb < 2 * L && gs == LF_OK; ++sb) {
         const int l = sb / 2, ua = sb - 1 - 2 * s.delay;
-        const __half *lw = e->blob + s.off_layer0 + (long long)l * s.per_layer;
         __half *h = b.h16 + (size_t)sb * BD;
         const __half *gain = e->gains + (size_t)(sb % 2 == 0 ? l : L + l) * D;
         if (ua >= 0) cudaStreamWaitEvent(main, ev_part[ua], 0);
@@ -470,24 +517,24 @@ lf_status enqueue_batch_step(lf_engine *e, BatchState &b, cudaStream_t main) {
             a.L = L;
             a.l = l;
             a.ctx = s.ctx;
-            if ((gs = lf::gemv_tc(lw + s.o_wq, h, a, w)) != LF_OK) break;
+            if ((gs = lf::gemv_tc(wt(4 * l), h, a, w)) != LF_OK) break;
             attn<<<dim3(s.NKV, B, lf::kBatchAttnSplits), lf::kBatchAttnThreads, 0, w>>>(
                 q, b.kc, b.vc, b.d_pos, L, l, s.NKV, s.ctx, e->cfg.swa_window[l], scale,
                 b.att_ws + (size_t)l * att_ws_floats(s, B), b.att_cnt + (size_t)l * B * s.NKV, o16);
             a = gemv_args(4 * l + 1);
             a.y = P;
             a.ldy = D;
-            if ((gs = lf::gemv_tc(lw + s.o_wo, o16, a, w)) != LF_OK) break;
+            if ((gs = lf::gemv_tc(wt(4 * l + 1), o16, a, w)) != LF_OK) break;
         } else {
             __half *u16 = b.u16 + (size_t)l * B * s.F;
             lf::GemvArgs a = gemv_args(4 * l + 2);
             a.u = u16;
             a.ldu = s.F;
-            if ((gs = lf::gemv_tc(lw + s.o_wg, h, a, w)) != LF_OK) break;
+            if ((gs = lf::gemv_tc(wt(4 * l + 2), h, a, w)) != LF_OK) break;
             a = gemv_args(4 * l + 3);
             a.y = P;
             a.ldy = D;
-            if ((gs = lf::gemv_tc(lw + s.o_wd, u16, a, w)) != LF_OK) break;
+            if ((gs = lf::gemv_tc(wt(4 * l + 3), u16, a, w)) != LF_OK) break;
         }
         cudaEventRecord(ev_part[sb], w);
     }
@@ -501,7 +548,7 @@ lf_status enqueue_batch_step(lf_engine *e, BatchState &b, cudaStream_t main) {
         lf::GemvArgs a = gemv_args(4 * L);
         a.y = b.logits;
         a.ldy = s.V;
-        gs = lf::gemv_tc(e->blob + s.off_lm, h, a, main);
+        gs = lf::gemv_tc(wt(4 * L), h, a, main);
     }
     if (gs == LF_OK) {
         ba_argmax<<<B, 1024, 0, main>>>(b.logits, s.V, b.am);
@@ -552,6 +599,9 @@ extern "C" lf_status lf_batch_begin(lf_engine *e, int n_batch) {
         return LF_ERR_UNSUPPORTED;
     if (e->pos >= s.ctx) return LF_ERR_CTX_OVERFLOW;
     lf_batch_free(e);
+    if (lf::gemv_tc_prepare() != LF_OK) return LF_ERR_CUDA;
+    const lf_status ts = ensure_tiled(e);
+    if (ts != LF_OK) return ts == LF_ERR_CUDA ? (e->poisoned = LF_ERR_CUDA) : ts;
     BatchState *b = new BatchState();
     b->B = n_batch;
     // split-K workspace and counters: a region per GEMV of the step

@@ -35,6 +35,8 @@ struct lf_engine {
     uint32_t *pf_err = nullptr;  // device word: GEMM wait timeouts during a batched prefill
     int pf_tc_attention = 1;     // batched prefill attention on the tensor cores (head_dim 128)
     lf::BatchState *batch = nullptr;  // lf_batch_begin .. lf_batch_end (owned separately)
+    void *wtile = nullptr;            // batched decode: the GEMVs' weights in their streaming layout
+    bool wtile_ok = false;            // wtile matches the loaded weights
     lf::CtaPlan *d_cta = nullptr;
     lf::LayerPlan *d_lp = nullptr;
     size_t n_ctr = 0;

@@ -25,6 +25,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "lf_gemv_tc.h"
@@ -89,20 +90,11 @@ __device__ __host__ __forceinline__ Tiling tiling(int N, int K, int mode) {
     return t;
 }
 
-// Rows of W in the two 64-row halves of tile t (the second is -1 when it lies
-// wholly past the last row).
-__device__ __forceinline__ void tile_rows(const GemvArgs &a, int t, int &y0, int &y1) {
-    if (a.mode == GEMV_SWIGLU) {
-        y0 = t * GV_BH;
-        y1 = a.N / 2 + t * GV_BH;
-    } else {
-        y0 = t * GV_BM;
-        y1 = y0 + GV_BH < a.N ? y0 + GV_BH : -1;
-    }
-}
+constexpr int GV_BLOCK_BYTES = GV_A_BYTES;  // one (tile, k-block) of the streaming layout
+constexpr int GV_PREFETCH = 4;              // k-blocks prefetched into L2 ahead of the copies
 
 __global__ void __launch_bounds__(GV_THREADS, 2)
-    gemv_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+    gemv_tc_kernel(const uint8_t *__restrict__ wt, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ GemvArgs a, int maxseg) {
     extern __shared__ __align__(1024) uint8_t gv_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(gv_raw) + 1023) & ~uintptr_t(1023));
@@ -128,7 +120,6 @@ __global__ void __launch_bounds__(GV_THREADS, 2)
         S.ep_fail = 0;
         S.last = 0;
         fence_barrier_init();
-        tma_prefetch_map(&tmW);
         tma_prefetch_map(&tmX);
     }
     if (warp == 1) tc_alloc(&S.tmem_base, GV_TMEM_COLS);
@@ -138,19 +129,21 @@ __global__ void __launch_bounds__(GV_THREADS, 2)
     const uint32_t tmem = S.tmem_base;
 
     if (warp == 0) {
-        if (lane == 0) {  // copies: W halves and the X block of every k-block of [lo, hi)
+        if (lane == 0) {  // copies: the weight block (contiguous run) and the X block of every k-block of [lo, hi)
+            const uint64_t pol = policy_evict_first();  // each weight byte is read once per step
+            for (long long g = lo; g < hi && g < lo + GV_STAGES + GV_PREFETCH; ++g)
+                if (g >= lo + GV_STAGES) bulk_prefetch_l2(wt + (size_t)g * GV_BLOCK_BYTES, GV_BLOCK_BYTES);
             int kbg = 0;
             for (long long g = lo; g < hi && !S.abort_; ++g, ++kbg) {
-                const int t = (int)(g / tl.nk), kb = (int)(g % tl.nk), s = kbg % GV_STAGES;
+                const int kb = (int)(g % tl.nk), s = kbg % GV_STAGES;
                 if (kbg >= GV_STAGES && !gv_wait(S, &S.empty[s], ((kbg / GV_STAGES) - 1) & 1u, deadline, a.err))
                     break;
-                int y0, y1;
-                tile_rows(a, t, y0, y1);
                 uint8_t *st = tiles + (size_t)s * GV_STAGE_BYTES;
-                mbar_arrive_expect_tx(&S.full[s], (y1 >= 0 ? GV_A_BYTES : GV_HALF_BYTES) + GV_X_BYTES);
-                tma_load_2d(st, &tmW, kb * GV_BK, y0, &S.full[s]);
-                if (y1 >= 0) tma_load_2d(st + GV_HALF_BYTES, &tmW, kb * GV_BK, y1, &S.full[s]);
+                mbar_arrive_expect_tx(&S.full[s], GV_BLOCK_BYTES + GV_X_BYTES);
+                bulk_g2s(st, wt + (size_t)g * GV_BLOCK_BYTES, GV_BLOCK_BYTES, &S.full[s], pol);
                 tma_load_2d(st + GV_A_BYTES, &tmX, kb * GV_BK, 0, &S.full[s]);
+                const long long gp = g + GV_STAGES + GV_PREFETCH;
+                if (gp < hi) bulk_prefetch_l2(wt + (size_t)gp * GV_BLOCK_BYTES, GV_BLOCK_BYTES);
             }
             if (S.abort_) {  // let the copies in flight land before the CTA exits
                 const uint64_t dl = global_timer_ns() + 1000000000ull;
@@ -353,6 +346,26 @@ int sm_count() {
     return n;
 }
 
+// One thread per 16-byte chunk of the streaming layout (see the header).
+__global__ void gemv_tile_kernel(const __half *__restrict__ W, uint4 *__restrict__ out, int N, int K, int mode,
+                                 long long n_chunks) {
+    const int nk = K / GV_BK;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n_chunks;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long blk = i / (GV_BM * 8);
+        const int within = (int)(i % (GV_BM * 8)), r = within / 8, pos = within % 8, c = pos ^ (r & 7);
+        const int t = (int)(blk / nk), kb = (int)(blk % nk);
+        int row;
+        if (mode == GEMV_SWIGLU)
+            row = r < GV_BH ? t * GV_BH + r : N / 2 + t * GV_BH + (r - GV_BH);
+        else
+            row = t * GV_BM + r;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row < N) v = *reinterpret_cast<const uint4 *>(W + (size_t)row * K + kb * GV_BK + c * 8);
+        out[i] = v;
+    }
+}
+
 // Largest number of segments any tile is cut into.
 int max_segments(const Tiling &tl, int grid) {
     int m = 1;
@@ -383,7 +396,22 @@ void gemv_tc_needs(int N, int K, int mode, size_t *ws_floats, int *n_cnt) {
     *n_cnt = tl.T;
 }
 
-lf_status gemv_tc(const __half *W, const __half *X, const GemvArgs &a, cudaStream_t stream) {
+size_t gemv_tiled_bytes(int N, int K, int mode) {
+    const Tiling tl = tiling(N, K, mode);
+    return (size_t)tl.G * GV_BLOCK_BYTES;
+}
+
+lf_status gemv_tile_weights(const __half *W, int N, int K, int mode, void *tiled, cudaStream_t stream) {
+    if (!W || !tiled || N < 1 || K < GV_BK || K % GV_BK || (mode == GEMV_SWIGLU && N % (2 * GV_BH)))
+        return LF_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(W) & 15) || (reinterpret_cast<uintptr_t>(tiled) & 15)) return LF_ERR_INVALID_ARG;
+    const long long n_chunks = (long long)gemv_tiled_bytes(N, K, mode) / 16;
+    gemv_tile_kernel<<<(int)std::min<long long>((n_chunks + 255) / 256, 8192), 256, 0, stream>>>(
+        W, static_cast<uint4 *>(tiled), N, K, mode, n_chunks);
+    return cudaGetLastError() == cudaSuccess ? LF_OK : LF_ERR_CUDA;
+}
+
+lf_status gemv_tc(const void *W, const __half *X, const GemvArgs &a, cudaStream_t stream) {
     if (!W || !X || a.B < 1 || a.B > GV_NB || a.N < 1 || a.K < GV_BK || a.K % GV_BK || !a.err)
         return LF_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(W) & 15) || (reinterpret_cast<uintptr_t>(X) & 15)) return LF_ERR_INVALID_ARG;
@@ -399,12 +427,10 @@ lf_status gemv_tc(const __half *W, const __half *X, const GemvArgs &a, cudaStrea
     const int ms = max_segments(tl, grid);
     if (ms > 1 && (!a.ws || !a.cnt || a.n_cnt < tl.T || a.ws_floats < (size_t)tl.T * ms * GV_NB * GV_BM))
         return LF_ERR_UNSUPPORTED;
-    CUtensorMap mw, mx;
-    if (!make_map(&mw, W, a.N, a.K, GV_BH, CU_TENSOR_MAP_L2_PROMOTION_NONE) ||
-        !make_map(&mx, X, a.B, a.K, GV_NB, CU_TENSOR_MAP_L2_PROMOTION_L2_128B))
-        return LF_ERR_CUDA;
+    CUtensorMap mx;
+    if (!make_map(&mx, X, a.B, a.K, GV_NB, CU_TENSOR_MAP_L2_PROMOTION_L2_128B)) return LF_ERR_CUDA;
     if (gemv_tc_prepare() != LF_OK) return LF_ERR_CUDA;
-    gemv_tc_kernel<<<grid, GV_THREADS, GV_SMEM, stream>>>(mw, mx, a, ms);
+    gemv_tc_kernel<<<grid, GV_THREADS, GV_SMEM, stream>>>(static_cast<const uint8_t *>(W), mx, a, ms);
     return cudaGetLastError() == cudaSuccess ? LF_OK : LF_ERR_CUDA;
 }
 
@@ -420,7 +446,8 @@ extern "C" lf_status lf_gemv_f16(const void *w_device, const void *x_device, flo
     lf::gemv_tc_needs(n, k, lf::GEMV_F32, &wsf, &ncnt);
     void *scratch = nullptr;
     const size_t cnt_bytes = ((size_t)ncnt * sizeof(uint32_t) + 255) & ~size_t(255);
-    const size_t bytes = 256 + cnt_bytes + wsf * sizeof(float);
+    const size_t ws_bytes = (wsf * sizeof(float) + 255) & ~size_t(255);
+    const size_t bytes = 256 + cnt_bytes + ws_bytes + lf::gemv_tiled_bytes(n, k, lf::GEMV_F32);
     if (cudaMalloc(&scratch, bytes) != cudaSuccess) {
         (void)cudaGetLastError();
         return LF_ERR_OOM;
@@ -440,8 +467,10 @@ extern "C" lf_status lf_gemv_f16(const void *w_device, const void *x_device, flo
     a.timeout_ns = 2000000000ull;
     lf_status r = LF_OK;
     uint32_t werr = 0;
+    void *tiled = static_cast<uint8_t *>(scratch) + 256 + cnt_bytes + ws_bytes;
     if (cudaMemsetAsync(scratch, 0, 256 + cnt_bytes, st) != cudaSuccess) r = LF_ERR_CUDA;
-    if (r == LF_OK) r = lf::gemv_tc(static_cast<const __half *>(w_device), static_cast<const __half *>(x_device), a, st);
+    if (r == LF_OK) r = lf::gemv_tile_weights(static_cast<const __half *>(w_device), n, k, lf::GEMV_F32, tiled, st);
+    if (r == LF_OK) r = lf::gemv_tc(tiled, static_cast<const __half *>(x_device), a, st);
     if (r == LF_OK && (cudaMemcpyAsync(&werr, scratch, sizeof(werr), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
                        cudaStreamSynchronize(st) != cudaSuccess))
         r = LF_ERR_CUDA;

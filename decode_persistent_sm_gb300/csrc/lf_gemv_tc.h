@@ -41,10 +41,22 @@ struct GemvArgs {
     unsigned long long timeout_ns = 0;
 };
 
-// Enqueues Y = W X^T on `stream`.  W is row-major fp16 [N][K], X row-major
-// fp16 [B][K]; both 16-byte aligned.  INVALID_ARG on bad sizes, UNSUPPORTED
-// when the workspace or the counters are too small.
-lf_status gemv_tc(const __half *W, const __half *X, const GemvArgs &a, cudaStream_t stream);
+// The weights in the GEMV's streaming layout: one 16 KB block per (tile t,
+// k-block kb) at block index t * (K / 64) + kb, each block the tile's 128
+// rows x 64 columns in the 128-byte-swizzled K-major order the MMA reads
+// (row r at byte r * 128, its 16-byte chunk c at position c ^ (r % 8)).
+// Tile t holds rows 128t .. 128t + 127 (zero past N), or under GEMV_SWIGLU
+// gate rows 64t .. and up rows N/2 + 64t ...  A CTA's run of k-blocks is
+// then one contiguous stretch of memory.
+size_t gemv_tiled_bytes(int N, int K, int mode);
+// Enqueues the re-layout of row-major fp16 W [N][K] into `tiled`.
+lf_status gemv_tile_weights(const __half *W, int N, int K, int mode, void *tiled, cudaStream_t stream);
+
+// Enqueues Y = W X^T on `stream`, W given in the streaming layout above
+// (tiled, 16-byte aligned), X row-major fp16 [B][K] (16-byte aligned).
+// INVALID_ARG on bad sizes, UNSUPPORTED when the workspace or the counters
+// are too small.
+lf_status gemv_tc(const void *tiled, const __half *X, const GemvArgs &a, cudaStream_t stream);
 
 // One-time kernel attributes (call before capturing launches into a graph).
 lf_status gemv_tc_prepare();

@@ -187,6 +187,7 @@ lf_status lf_plan_stats(const lf_config *cfg, int n_sm, int64_t stats[8]) {
 void lf_destroy(lf_engine *e) {
     if (!e) return;
     lf_batch_free(e);
+    if (e->wtile) cudaFree(e->wtile);
     for (void *p : e->allocs) cudaFree(p);
     if (e->trace) cudaFree(e->trace);
     if (e->pf_mem) cudaFree(e->pf_mem);
@@ -292,6 +293,8 @@ lf_status lf_load_weights(lf_engine *e, const void *host_blob, size_t nbytes) {
     const lf::Plan &P = e->plan;
     const lf::Shape &s = P.sh;
     if (nbytes != (size_t)s.n_params * 2) return LF_ERR_INVALID_ARG;
+    e->wtile_ok = false;  // the batched decode's weight layout is rebuilt from the new blob
+    lf_batch_free(e);
     __half *staging = nullptr;
     long long *d_src = nullptr;
     cudaError_t err = cudaMalloc(&staging, (size_t)P.staging_elems * sizeof(__half));
