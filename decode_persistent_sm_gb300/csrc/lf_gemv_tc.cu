@@ -41,7 +41,7 @@ constexpr int GV_A_BYTES = 2 * GV_HALF_BYTES;      // 128 rows of W
 constexpr int GV_X_BYTES = GV_NB * GV_BK * 2;      // 16 rows of X
 constexpr int GV_STAGE_BYTES = GV_A_BYTES + GV_X_BYTES;  // 18 KB, a multiple of 1024
 constexpr int GV_THREADS = 192;
-constexpr int kCtasPerSm = 2;  // grid: two CTAs per SM, so one CTA's ramp overlaps the other's stream
+constexpr int kCtasPerSm = 1;  // grid: one CTA per SM; a second GEMV (another sub-block) fits beside it
 constexpr uint32_t GV_TMEM_COLS = 32;  // two 16-column accumulators
 constexpr size_t GV_SMEM = (size_t)GV_STAGES * GV_STAGE_BYTES + GV_NB * GV_BM * 4 + 256 + 1024;
 constexpr uint32_t kGvIdesc = idesc_f16(GV_BM, GV_NB);
