@@ -37,7 +37,8 @@
 
 namespace lf {
 
-constexpr int kBatchAttnSplits = 16;  // key splits per (sample, KV head)
+constexpr int kBatchAttnSplits = 16;        // most key splits per (sample, KV head)
+constexpr int kBatchAttnKeysPerSplit = 128;  // keys per split below that
 constexpr int kBatchAttnThreads = 128;
 constexpr unsigned long long kBatchTimeoutNs = 2000000000ull;
 
@@ -131,10 +132,14 @@ __global__ void __launch_bounds__(kBatchAttnThreads)
     using D = Dims<DPL>;
     __shared__ float red[NW][GL][DH + 2];
     __shared__ int last;
-    const int g = blockIdx.x, b = blockIdx.y, split = blockIdx.z, S = gridDim.z;
+    const int g = blockIdx.x, b = blockIdx.y, split = blockIdx.z;
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, NQ = NKV * GL;
     const int p = *pos_word;
-    const int jlo = window > 0 ? max(0, p - window + 1) : 0, n = p - jlo + 1, per = (n + S - 1) / S;
+    const int jlo = window > 0 ? max(0, p - window + 1) : 0, n = p - jlo + 1;
+    // splits in use: about kBatchAttnKeysPerSplit keys each, at most gridDim.z (the rest exit at once)
+    const int S = min((int)gridDim.z, (n + lf::kBatchAttnKeysPerSplit - 1) / lf::kBatchAttnKeysPerSplit);
+    if (split >= S) return;
+    const int per = (n + S - 1) / S;
     const int j0 = jlo + split * per, nk = max(0, min(j0 + per, p + 1) - j0);
 
     float qr[GL][DPL], acc[GL][DPL], m[GL], ls[GL];
