@@ -242,6 +242,24 @@ def write_trace(eng, path, tokens, shape):
               file=sys.stderr)
 
 
+def max_over_ranks(x: float, world: int, device="cuda") -> float:
+    """The largest x over all ranks of the process group (each rank passes
+    its own); x itself when there is one rank."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, units_per_rank: int, worst_ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time (every rank runs the same work on its own GPU)."""
+    return world * units_per_rank / (worst_ms / 1e3)
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -337,13 +355,9 @@ def run_ours(args, world, rank, local):
     clk = clocks.stop()
     eng.synchronize()  # raises if any timed step failed
     launches = eng.info()["launches"] - launches0
-    total_ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(ev0.elapsed_time(ev1), world)
     ms = total_ms / args.steps
-    value = world * args.steps / (total_ms / 1e3)
+    value = job_rate(world, args.steps, total_ms)
 
     # end to end through the C ABI: token in by value, logits + argmax back
     # into pinned host memory, every step synchronous
@@ -354,12 +368,8 @@ def run_ours(args, world, rank, local):
     for i in range(n_e2e):
         eng.set_position(POS)
         eng.decode_step_into(int(tokens[i]), host_logits.data_ptr())
-    e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = {"value": world * n_e2e / e2e_s, "unit": UNIT, "h2d_bytes_per_step": 4,
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e = {"value": job_rate(world, n_e2e, e2e_s * 1e3), "unit": UNIT, "h2d_bytes_per_step": 4,
            "d2h_bytes_per_step": shape.vocab * 4 + 4 * 8}
 
     if args.trace:
@@ -462,11 +472,7 @@ def run_generation(args, world, rank, local):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
     def worst(x):  # max over ranks
-        if world == 1:
-            return x
-        t = torch.tensor([x], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks(x, world)
 
     base = synth.FULL
     blob = synth.make_weights(base, SEED)
