@@ -138,17 +138,19 @@ static std::vector<int> build_ops(const Shape &s) {
             // With a delay the FFN of layer l does not read the attention of
             // layer l, so it is streamed while the attention runs beside it.
             // With a delay of 2 or more, o_proj of layer l - 1 (whose lane sum
-            // is first read at sub-block 2l + 3) waits until after the QKV rows
-            // of layer l, which gives the attention warps a layer's worth of
-            // slack.  The last layer's o_proj closes the step.
+            // is first read at sub-block 2l + 3, the FFN of layer l + 1) waits
+            // until after the FFN rows of layer l: the attention warps get the
+            // QKV and FFN streams of a whole layer as slack, and the lane sum
+            // forms while the QKV rows of layer l + 1 stream.  The last layer's
+            // o_proj closes the step.
             const bool late = (d >= 2);
             adds_upto(sa - 1 - 2 * d);
             ops.push_back(make_op(OP_NORM, l));
             ops.push_back(make_op(OP_QKV, l));
-            if (late && l > 0) ops.push_back(make_op(OP_OPROJ, l - 1));
             adds_upto(sf - 1 - 2 * d);
             ops.push_back(make_op(OP_NORM, L + l));
             ops.push_back(make_op(OP_GATEUP, l));
+            if (late && l > 0) ops.push_back(make_op(OP_OPROJ, l - 1));
             ops.push_back(make_op(OP_DOWN, l));
             ops.push_back(make_op(OP_ATTN, l));
             if (!late || l + 1 == L) ops.push_back(make_op(OP_OPROJ, l));
