@@ -5,8 +5,9 @@
 // head's FP16 cache come in tiles of 128.  Two passes over the key tiles:
 //   pass 1: S = Q K^T (tcgen05.mma into TMEM, 128 columns); each of the
 //           four softmax warps reads its 32 rows (tcgen05.ld, one query row
-//           per thread) and keeps the row's running max and sum;
-//   pass 2: S again; P = exp(S - max) in FP16 written to shared memory in the
+//           per thread) and keeps the row's max (no exponentials);
+//   pass 2: S again; P = exp(S - max) (the row sum accumulated in fp32 from
+//           the same exponentials) in FP16 written to shared memory in the
 //           128-byte-swizzled K-major operand layout; the V tile transposed
 //           into the same layout; O += P V^T (tcgen05.mma into TMEM columns
 //           256..383), so O never needs rescaling.
@@ -198,25 +199,15 @@ __global__ void __launch_bounds__(A_THREADS, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t sb = trow + (uint32_t)b * AK;
-            if (j < 0) {  // pass 1: running max and sum of the row
+            if (j < 0) {  // pass 1: the row's max
 #pragma unroll 1
                 for (int c0 = 0; c0 < AK; c0 += 32) {
                     float v[32];
                     tc_ld32(sb + (uint32_t)c0, v);
-                    float mt = -INFINITY;
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int col = c0 + i;
-                        v[i] = (col >= vlo && col <= vhi) ? v[i] * sc2 : -INFINITY;
-                        mt = fmaxf(mt, v[i]);
-                    }
-                    if (mt != -INFINITY) {
-                        const float mn = fmaxf(m2, mt);
-                        float sum = 0.f;
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) sum += exp2f(v[i] - mn);  // exp2f(-inf) = 0
-                        l = (m2 == -INFINITY ? 0.f : l * exp2f(m2 - mn)) + sum;
-                        m2 = mn;
+                        if (col >= vlo && col <= vhi) m2 = fmaxf(m2, v[i] * sc2);
                     }
                 }
                 tc_fence_before();
@@ -233,7 +224,9 @@ __global__ void __launch_bounds__(A_THREADS, 1)
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const int col = c0 + 8 * c8 + i;
-                            hv[i] = __float2half_rn((col >= vlo && col <= vhi) ? exp2f(v[8 * c8 + i] * sc2 - m2) : 0.f);
+                            const float pe = (col >= vlo && col <= vhi) ? exp2f(v[8 * c8 + i] * sc2 - m2) : 0.f;
+                            l += pe;
+                            hv[i] = __float2half_rn(pe);
                         }
                         pk[c0 / 8 + c8] = *reinterpret_cast<const uint4 *>(hv);
                     }
