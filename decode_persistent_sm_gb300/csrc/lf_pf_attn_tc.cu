@@ -199,17 +199,24 @@ __global__ void __launch_bounds__(A_THREADS, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t sb = trow + (uint32_t)b * AK;
-            if (j < 0) {  // pass 1: the row's max
+            if (j < 0) {  // pass 1: the row's max (on raw scores; sc2 > 0 scales it once at the end)
+                float mr = -INFINITY;
 #pragma unroll 1
                 for (int c0 = 0; c0 < AK; c0 += 32) {
                     float v[32];
                     tc_ld32(sb + (uint32_t)c0, v);
+                    if (c0 >= vlo && c0 + 31 <= vhi) {  // the whole chunk is in the row's key range
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int col = c0 + i;
-                        if (col >= vlo && col <= vhi) m2 = fmaxf(m2, v[i] * sc2);
+                        for (int i = 0; i < 32; ++i) mr = fmaxf(mr, v[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int col = c0 + i;
+                            if (col >= vlo && col <= vhi) mr = fmaxf(mr, v[i]);
+                        }
                     }
                 }
+                if (mr != -INFINITY) m2 = fmaxf(m2, mr * sc2);
                 tc_fence_before();
                 mbar_arrive(&S.bp[b]);
             } else {  // pass 2: P of the row in registers, then into shared memory
@@ -218,15 +225,21 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                 for (int c0 = 0; c0 < AK; c0 += 32) {
                     float v[32];
                     tc_ld32(sb + (uint32_t)c0, v);
+                    const bool full = c0 >= vlo && c0 + 31 <= vhi;  // no column of the chunk is masked
 #pragma unroll
                     for (int c8 = 0; c8 < 4; ++c8) {
-                        __align__(16) __half hv[8];
+                        __align__(16) __half2 hv[4];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
+                        for (int i = 0; i < 8; i += 2) {
                             const int col = c0 + 8 * c8 + i;
-                            const float pe = (col >= vlo && col <= vhi) ? exp2f(v[8 * c8 + i] * sc2 - m2) : 0.f;
-                            l += pe;
-                            hv[i] = __float2half_rn(pe);
+                            float p0 = exp2f(fmaf(v[8 * c8 + i], sc2, -m2));
+                            float p1 = exp2f(fmaf(v[8 * c8 + i + 1], sc2, -m2));
+                            if (!full) {
+                                p0 = (col >= vlo && col <= vhi) ? p0 : 0.f;
+                                p1 = (col + 1 >= vlo && col + 1 <= vhi) ? p1 : 0.f;
+                            }
+                            l += p0 + p1;
+                            hv[i / 2] = __floats2half2_rn(p0, p1);
                         }
                         pk[c0 / 8 + c8] = *reinterpret_cast<const uint4 *>(hv);
                     }
