@@ -40,41 +40,6 @@ __global__ void pf_add(float *__restrict__ x, const float *__restrict__ p, size_
         x[i] += p[i];
 }
 
-// RoPE on q and k (pairs c, c + dh/2; table rope[p][c] = (cos, sin)), q kept
-// in FP16 (tensor-core attention) and, when q is not null, fp32 (CUDA-core
-// attention); k and v rounded to FP16 into the cache of every lane that reads
-// that KV head.  One block per position.
-__global__ void pf_rope_kv(const float *__restrict__ qkv, const float2 *__restrict__ rope, float *__restrict__ q,
-                           __half *__restrict__ q16, __half *__restrict__ kc, __half *__restrict__ vc, const int *__restrict__ kv_first,
-                           int p0, int NQ, int NKV, int DH, int NL, int L, int l, int HKV_L, int ctx) {
-    const int i = blockIdx.x, p = p0 + i, half = DH / 2;
-    const float *row = qkv + (size_t)i * (NQ + 2 * NKV) * DH;
-    const float2 *cs = rope + (size_t)p * half;
-    for (int t = threadIdx.x; t < NQ * half; t += blockDim.x) {
-        const int hq = t / half, c = t % half;
-        const float a = row[hq * DH + c], b = row[hq * DH + c + half];
-        const float2 r = cs[c];
-        const float qa = a * r.x - b * r.y, qb = a * r.y + b * r.x;
-        if (q) {
-            q[(size_t)i * NQ * DH + hq * DH + c] = qa;
-            q[(size_t)i * NQ * DH + hq * DH + c + half] = qb;
-        }
-        q16[(size_t)i * NQ * DH + hq * DH + c] = __float2half_rn(qa);
-        q16[(size_t)i * NQ * DH + hq * DH + c + half] = __float2half_rn(qb);
-    }
-    for (int t = threadIdx.x; t < NL * HKV_L * half; t += blockDim.x) {
-        const int lg = t / half, c = t % half, lam = lg / HKV_L, g = lg % HKV_L;
-        const int kh = kv_first[lam] + g;
-        const float a = row[(NQ + kh) * DH + c], b = row[(NQ + kh) * DH + c + half];
-        const float2 r = cs[c];
-        const size_t at = ((((size_t)lam * L + l) * HKV_L + g) * ctx + p) * DH;
-        kc[at + c] = __float2half_rn(a * r.x - b * r.y);
-        kc[at + c + half] = __float2half_rn(a * r.y + b * r.x);
-        vc[at + c] = __float2half_rn(row[(NQ + NKV + kh) * DH + c]);
-        vc[at + c + half] = __float2half_rn(row[(NQ + NKV + kh) * DH + c + half]);
-    }
-}
-
 // u = FP16(silu(gate) * up); gu rows are [gate (F) | up (F)]
 __global__ void pf_swiglu(const float *__restrict__ gu, __half *__restrict__ u, int F, size_t n) {
     for (size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x; t < n; t += (size_t)gridDim.x * blockDim.x) {
@@ -325,7 +290,7 @@ size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 // Scratch of one batched prefill of M positions, carved from one allocation.
 struct PfBufs {
     int *tok;
-    float *x, *ring, *qkv, *qf, *gu;
+    float *x, *ring, *qf, *gu;
     __half *h, *o, *u, *q16;
     size_t bytes;
 };
@@ -333,7 +298,7 @@ struct PfBufs {
 // qf (fp32 queries) only for the CUDA-core attention, gu (fp32 gate/up) only
 // when SwiGLU is not fused into the gate/up GEMM.
 PfBufs carve(uint8_t *base, const lf::Shape &s, int M, bool need_qf, bool need_gu) {
-    const size_t D = s.D, QD = (size_t)s.NQ * s.DH, QKVN = (size_t)(s.NQ + 2 * s.NKV) * s.DH, F = s.F;
+    const size_t D = s.D, QD = (size_t)s.NQ * s.DH, F = s.F;
     const size_t R = 2 * (size_t)s.delay + 1;
     PfBufs b{};
     size_t at = 0;
@@ -345,7 +310,6 @@ PfBufs carve(uint8_t *base, const lf::Shape &s, int M, bool need_qf, bool need_g
     b.tok = reinterpret_cast<int *>(take(M * sizeof(int)));
     b.x = reinterpret_cast<float *>(take(M * D * 4));
     b.ring = reinterpret_cast<float *>(take(R * M * D * 4));
-    b.qkv = reinterpret_cast<float *>(take(M * QKVN * 4));
     b.qf = need_qf ? reinterpret_cast<float *>(take(M * QD * 4)) : nullptr;
     b.gu = need_gu ? reinterpret_cast<float *>(take(M * 2 * F * 4)) : nullptr;
     b.h = reinterpret_cast<__half *>(take(M * std::max(D, F) * 2));
@@ -373,7 +337,7 @@ extern "C" lf_status lf_prefill_batched(lf_engine *e, const int32_t *tokens, int
         if (tokens[i] < 0 || tokens[i] >= s.V) return LF_ERR_INVALID_ARG;
     if (!e->blob) return LF_ERR_OOM;
     const int D = s.D, DH = s.DH, NQ = s.NQ, NKV = s.NKV, F = s.F, L = s.L, QD = NQ * DH;
-    const int QKVN = (NQ + 2 * NKV) * DH, R = 2 * s.delay + 1, M = n, p0 = e->pos;
+    const int R = 2 * s.delay + 1, M = n, p0 = e->pos;
     if (D % 64 || QD % 64 || F % 64 || (DH != 128 && DH != 32) || D > 4 * kNormV * kNormThreads)
         return LF_ERR_UNSUPPORTED;
     cudaStream_t st = e->stream;
@@ -421,10 +385,25 @@ extern "C" lf_status lf_prefill_batched(lf_engine *e, const int32_t *tokens, int
         if (sb % 2 == 0) {
             pf_addnorm<<<M, kNormThreads, 0, st>>>(b.x, b.ring, MD, ua, n_arrive, R, e->gains + (size_t)l * D, b.h,
                                                    D, eps);
-            gs = lf::tc_gemm_f16(b.h, lw + s.o_wq, b.qkv, M, QKVN, D, QKVN, e->pf_err, kGemmTimeoutNs, st);
+            // QKV projection with RoPE and the KV-cache append in the GEMM epilogue
+            lf::QkvEpi qe;
+            qe.q16 = b.q16;
+            qe.qf = tc_attn ? nullptr : b.qf;
+            qe.kc = e->kc;
+            qe.vc = e->vc;
+            qe.rope = e->rope;
+            qe.kv_first = e->d_kvfirst;
+            qe.p0 = p0;
+            qe.NQ = NQ;
+            qe.NKV = NKV;
+            qe.DH = DH;
+            qe.NL = s.NL;
+            qe.L = L;
+            qe.l = l;
+            qe.HKV_L = s.HKV_L;
+            qe.ctx = s.ctx;
+            gs = lf::tc_gemm_qkv_rope_f16(b.h, lw + s.o_wq, M, D, qe, e->pf_err, kGemmTimeoutNs, st);
             if (gs != LF_OK) return gs == LF_ERR_CUDA ? pf_fail(e) : gs;
-            pf_rope_kv<<<M, 256, 0, st>>>(b.qkv, e->rope, tc_attn ? nullptr : b.qf, b.q16, e->kc, e->vc,
-                                          e->d_kvfirst, p0, NQ, NKV, DH, s.NL, L, l, s.HKV_L, s.ctx);
             const dim3 ag((M + PF_QB - 1) / PF_QB, NQ);
             if (tc_attn) {
                 lf::TcAttnArgs ta{M, p0, NQ, s.HQ_L, s.GL, s.HKV_L, L, l, s.ctx, e->cfg.swa_window[l], scale, b.o, QD};

@@ -73,12 +73,18 @@ __device__ __forceinline__ void tile_of(int t, int mt, int nt, int &m, int &n) {
 // Persistent: CTA c computes tiles c, c + gridDim.x, ...; the stage ring and
 // the two TMEM accumulators run across tiles, so copies and MMAs of one tile
 // overlap the epilogue of the previous one.
-// kSwiGLU: N = 2F is the row count of B, the grid of tiles is M x F/128 and
-// C is the FP16 U[M][F] (row stride ldc halves); otherwise C is fp32.
-template <bool kSwiGLU>
+enum GemmMode : int { GEMM_F32 = 0, GEMM_SWIGLU = 1, GEMM_QKV = 2 };
+
+// GEMM_SWIGLU: N = 2F is the row count of B, the grid of tiles is M x F/128
+// and C is the FP16 U[M][F] (row stride ldc halves); GEMM_QKV: the epilogue
+// rotates q and k (RoPE at position p0 + row) and writes q and the K/V cache
+// rows (qe); otherwise C is fp32.
+template <int kMode>
 __global__ void __launch_bounds__(TG_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, void *C,
-                   int M, int N, int K, int ldc, uint32_t *err, unsigned long long timeout_ns) {
+                   int M, int N, int K, int ldc, uint32_t *err, unsigned long long timeout_ns,
+                   const __grid_constant__ QkvEpi qe) {
+    constexpr bool kSwiGLU = kMode == GEMM_SWIGLU;
     extern __shared__ __align__(1024) uint8_t tg_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(tg_raw) + 1023) & ~uintptr_t(1023));
     TgShared &S = *reinterpret_cast<TgShared *>(tiles + (size_t)TG_STAGES * STAGE_BYTES);
@@ -177,6 +183,68 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t tacc = tmem + (uint32_t)b * BN + ((uint32_t)(32 * q) << 16);
+            if constexpr (kMode == GEMM_QKV) {
+                // every head of the tile is whole (256 % DH == 0), so both columns of each RoPE pair
+                // (c, c + DH/2) are in this thread's row
+                const int DH = qe.DH, half = DH / 2, pos = qe.p0 + row;
+#pragma unroll 1
+                for (int hl = 0; hl < BN / DH && n * BN + hl * DH < N; ++hl) {
+                    const int hd = (n * BN + hl * DH) / DH;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < half; c0 += 16) {
+                        float va[16], vb[16];
+                        tc_ld16(tacc + (uint32_t)(hl * DH + c0), va);
+                        tc_ld16(tacc + (uint32_t)(hl * DH + half + c0), vb);
+                        if (row >= M) continue;
+                        if (hd < qe.NQ + qe.NKV) {  // q and k: rotate the pairs
+                            const float2 *cs = qe.rope + (size_t)pos * half + c0;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const float2 r = cs[i];
+                                const float x0 = va[i], x1 = vb[i];
+                                va[i] = x0 * r.x - x1 * r.y;
+                                vb[i] = x0 * r.y + x1 * r.x;
+                            }
+                        }
+                        __align__(16) __half ha[16], hb[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            ha[i] = __float2half_rn(va[i]);
+                            hb[i] = __float2half_rn(vb[i]);
+                        }
+                        auto put = [&](__half *dst) {  // dims c0.. and half + c0.. of one head row
+#pragma unroll
+                            for (int i = 0; i < 2; ++i) {
+                                reinterpret_cast<uint4 *>(dst + c0)[i] = reinterpret_cast<const uint4 *>(ha)[i];
+                                reinterpret_cast<uint4 *>(dst + half + c0)[i] = reinterpret_cast<const uint4 *>(hb)[i];
+                            }
+                        };
+                        if (hd < qe.NQ) {
+                            const size_t at = (size_t)row * qe.NQ * DH + (size_t)hd * DH;
+                            put(qe.q16 + at);
+                            if (qe.qf) {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    qe.qf[at + c0 + i] = va[i];
+                                    qe.qf[at + half + c0 + i] = vb[i];
+                                }
+                            }
+                        } else {  // into the cache of every lane that reads this KV head
+                            const bool is_k = hd < qe.NQ + qe.NKV;
+                            const int kh = is_k ? hd - qe.NQ : hd - qe.NQ - qe.NKV;
+                            __half *cache = is_k ? qe.kc : qe.vc;
+                            for (int lam = 0; lam < qe.NL; ++lam) {
+                                const int g = kh - qe.kv_first[lam];
+                                if (g < 0 || g >= qe.HKV_L) continue;
+                                put(cache + ((((size_t)lam * qe.L + qe.l) * qe.HKV_L + g) * qe.ctx + pos) * DH);
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&S.acc_empty[b]);
+                continue;
+            }
             if constexpr (kSwiGLU) {
 #pragma unroll 1
                 for (int c0 = 0; c0 < BH; c0 += 32) {
@@ -273,15 +341,16 @@ size_t tc_gemm_smem_bytes() { return TG_SMEM; }
 
 namespace {
 
-template <bool kSwiGLU>
+template <int kMode>
 lf_status launch(const __half *A, const __half *B, void *C, int M, int N, int K, int ldc, uint32_t *err,
-                 unsigned long long timeout_ns, cudaStream_t stream) {
+                 unsigned long long timeout_ns, cudaStream_t stream, const QkvEpi &qe = QkvEpi()) {
+    constexpr bool kSwiGLU = kMode == GEMM_SWIGLU;
     CUtensorMap ma, mb;
     if (!make_map(&ma, A, M, K, BM) || !make_map(&mb, B, N, K, BH)) return LF_ERR_CUDA;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(tc_gemm_kernel<kSwiGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(tc_gemm_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)TG_SMEM);
     });
     if (attr_err != cudaSuccess) return LF_ERR_CUDA;
@@ -293,8 +362,8 @@ lf_status launch(const __half *A, const __half *B, void *C, int M, int N, int K,
             return LF_ERR_CUDA;
     }
     const int nt = kSwiGLU ? N / BN : (N + BN - 1) / BN, ntiles = ((M + BM - 1) / BM) * nt;
-    tc_gemm_kernel<kSwiGLU><<<ntiles < n_sm ? ntiles : n_sm, TG_THREADS, TG_SMEM, stream>>>(ma, mb, C, M, N, K, ldc,
-                                                                                          err, timeout_ns);
+    tc_gemm_kernel<kMode><<<ntiles < n_sm ? ntiles : n_sm, TG_THREADS, TG_SMEM, stream>>>(ma, mb, C, M, N, K, ldc,
+                                                                                        err, timeout_ns, qe);
     return cudaGetLastError() == cudaSuccess ? LF_OK : LF_ERR_CUDA;
 }
 
@@ -306,7 +375,7 @@ lf_status tc_gemm_f16(const __half *A, const __half *B, float *C, int M, int N, 
                       unsigned long long timeout_ns, cudaStream_t stream) {
     if (!A || !B || !C || !err || M < 1 || N < 1 || K < BK || K % BK || ldc < N) return LF_ERR_INVALID_ARG;
     if (!aligned16(A) || !aligned16(B)) return LF_ERR_INVALID_ARG;
-    return launch<false>(A, B, C, M, N, K, ldc, err, timeout_ns, stream);
+    return launch<GEMM_F32>(A, B, C, M, N, K, ldc, err, timeout_ns, stream);
 }
 
 lf_status tc_gemm_swiglu_f16(const __half *A, const __half *Bgu, __half *U, int M, int F, int K, int ldu,
@@ -314,7 +383,19 @@ lf_status tc_gemm_swiglu_f16(const __half *A, const __half *Bgu, __half *U, int 
     if (!A || !Bgu || !U || !err || M < 1 || F < BH || F % BH || K < BK || K % BK || ldu < F || ldu % 8)
         return LF_ERR_INVALID_ARG;
     if (!aligned16(A) || !aligned16(Bgu) || !aligned16(U)) return LF_ERR_INVALID_ARG;
-    return launch<true>(A, Bgu, U, M, 2 * F, K, ldu, err, timeout_ns, stream);
+    return launch<GEMM_SWIGLU>(A, Bgu, U, M, 2 * F, K, ldu, err, timeout_ns, stream);
+}
+
+lf_status tc_gemm_qkv_rope_f16(const __half *A, const __half *Wqkv, int M, int K, const QkvEpi &e, uint32_t *err,
+                               unsigned long long timeout_ns, cudaStream_t stream) {
+    const int N = (e.NQ + 2 * e.NKV) * e.DH;
+    if (!A || !Wqkv || !err || !e.q16 || !e.kc || !e.vc || !e.rope || !e.kv_first || M < 1 || K < BK || K % BK ||
+        e.DH < 32 || BN % e.DH || e.DH % 32 || e.NQ < 1 || e.NKV < 1 || e.NL < 1 || e.p0 < 0 || e.p0 + M > e.ctx)
+        return LF_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(Wqkv) || !aligned16(e.q16) || !aligned16(e.kc) || !aligned16(e.vc))
+        return LF_ERR_INVALID_ARG;
+    __half *none = e.q16;  // C is not written in this mode
+    return launch<GEMM_QKV>(A, Wqkv, none, M, N, K, N, err, timeout_ns, stream, e);
 }
 
 }  // namespace lf

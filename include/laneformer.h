@@ -278,7 +278,7 @@ lf_status lf_decode_step_static_scratch(lf_engine *e, int32_t token, float *logi
  * advances the position by n; logits (host, vocab floats, nullable) and
  * argmax (host, nullable) receive the last position's result, which also
  * stays on the device (lf_get_logits_device / lf_get_argmax_device).
- * Scratch is allocated on first use and kept (about 0.25 MB per position
+ * Scratch is allocated on first use and kept (about 0.14 MB per position
  * at full shape, delay 2).  Synchronous.  LF_ERR_INVALID_ARG for n < 1, a
  * NULL tokens array or a token outside [0, vocab); LF_ERR_CTX_OVERFLOW if
  * position + n > ctx_cap; LF_ERR_OOM when the resident weights or the
