@@ -33,6 +33,7 @@ struct lf_engine {
     void *pf_mem = nullptr;      // lf_prefill_batched scratch (grow-only, owned separately)
     size_t pf_bytes = 0;
     uint32_t *pf_err = nullptr;  // device word: GEMM wait timeouts during a batched prefill
+    __half *pf_vt = nullptr;     // batched prefill: V caches transposed for the tensor-core attention (owned separately)
     int pf_tc_attention = 1;     // batched prefill attention on the tensor cores (head_dim 128)
     lf::BatchState *batch = nullptr;  // lf_batch_begin .. lf_batch_end (owned separately)
     void *wtile = nullptr;            // batched decode: the GEMVs' weights in their streaming layout

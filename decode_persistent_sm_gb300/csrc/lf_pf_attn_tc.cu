@@ -8,9 +8,11 @@
 //           per thread) and keeps the row's max (no exponentials);
 //   pass 2: S again; P = exp(S - max) (the row sum accumulated in fp32 from
 //           the same exponentials) in FP16 written to shared memory in the
-//           128-byte-swizzled K-major operand layout; the V tile transposed
-//           into the same layout; O += P V^T (tcgen05.mma into TMEM columns
-//           256..383), so O never needs rescaling.
+//           128-byte-swizzled K-major operand layout; the V^T tile ([dim][key],
+//           written transposed beside the cache by the QKV projection) comes
+//           by TMA straight into the same layout, double-buffered; O += P V^T
+//           (tcgen05.mma into TMEM columns 256..383), so O never needs
+//           rescaling.
 // K tiles and S are double-buffered (two shared-memory K buffers, two sets
 // of TMEM columns), so S of the next step is computed while the softmax
 // warps work on this one, and the P.V MMAs of a step overlap the next
@@ -36,7 +38,7 @@ constexpr int A_THREADS = 192;
 constexpr uint32_t A_TMEM_COLS = 512;  // S buffers in columns [0, 128) and [128, 256), O in [256, 384)
 constexpr uint32_t TM_O = 256;
 constexpr int HALF_TILE = AQ * 64 * 2;  // one [128 rows][64] FP16 swizzled tile, 16 KB
-constexpr int OFF_Q = 0, OFF_K = 2 * HALF_TILE /* two K buffers */, OFF_V = 6 * HALF_TILE, OFF_VT = 8 * HALF_TILE,
+constexpr int OFF_Q = 0, OFF_K = 2 * HALF_TILE /* two K buffers */, OFF_VT = 6 * HALF_TILE /* two V^T buffers */,
               OFF_P = 10 * HALF_TILE, A_TILES = 12 * HALF_TILE;
 constexpr size_t A_SMEM = (size_t)A_TILES + 1024 + 256;
 constexpr uint32_t kIdescA = idesc_f16(AQ, AK);  // S: N = keys; O: N = head dimension (also 128)
@@ -49,8 +51,9 @@ struct AttnShared {
     uint64_t bk[2];   // K buffer b loaded (steps b, b + 2, ...)
     uint64_t bs[2];   // S buffer b computed
     uint64_t bp[2];   // S buffer b read by the softmax warps (128 arrivals)
-    uint64_t bpw;     // pass 2: P and V^T written (128 arrivals)
-    uint64_t bv;      // V tile loaded
+    uint64_t bpw;     // pass 2: P written (128 arrivals)
+    uint64_t bv[2];   // V^T buffer b loaded (pass-2 steps b, b + 2, ...)
+    uint64_t bvr[2];  // V^T buffer b read by the P.V MMAs
     uint64_t bo;      // P.V MMAs done
     uint32_t tmem;
     volatile int abort_;
@@ -72,7 +75,7 @@ __device__ __forceinline__ bool await_phase(AttnShared &S, uint64_t *bar, uint32
 
 __global__ void __launch_bounds__(A_THREADS, 1)
     pf_attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV, const TcAttnArgs a, uint32_t *err,
+                      const __grid_constant__ CUtensorMap tmVT, const TcAttnArgs a, uint32_t *err,
                       unsigned long long timeout_ns) {
     extern __shared__ __align__(1024) uint8_t at_raw[];
     uint8_t *t = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(at_raw) + 1023) & ~uintptr_t(1023));
@@ -95,14 +98,17 @@ __global__ void __launch_bounds__(A_THREADS, 1)
             S.nbs_[b] = 0;
         }
         mbar_init(&S.bpw, 128);
-        mbar_init(&S.bv, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&S.bv[b], 1);
+            mbar_init(&S.bvr[b], 1);
+        }
         mbar_init(&S.bo, 1);
         S.abort_ = 0;
         S.nbo_ = 0;
         fence_barrier_init();
         tma_prefetch_map(&tmQ);
         tma_prefetch_map(&tmK);
-        tma_prefetch_map(&tmV);
+        tma_prefetch_map(&tmVT);
     }
     if (warp == 1) tc_alloc(&S.tmem, A_TMEM_COLS);
     tc_fence_before();
@@ -112,7 +118,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0) {  // copies
-            int nk[2] = {0, 0}, nv = 0;
+            int nk[2] = {0, 0}, nv[2] = {0, 0};
             mbar_arrive_expect_tx(&S.bq, 2 * HALF_TILE);
             tma_load_2d(t + OFF_Q, &tmQ, h * ADH, i0, &S.bq);
             tma_load_2d(t + OFF_Q + HALF_TILE, &tmQ, h * ADH + 64, i0, &S.bq);
@@ -125,11 +131,14 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                 tma_load_3d(kb, &tmK, 0, kt * AK, z, &S.bk[b]);
                 tma_load_3d(kb + HALF_TILE, &tmK, 64, kt * AK, z, &S.bk[b]);
                 ++nk[b];
-                if (j >= 0) {  // the V staging tile is free once the previous transpose is written
-                    if (j > 0 && !await_phase(S, &S.bpw, (j - 1) & 1u, deadline, err)) break;
-                    mbar_arrive_expect_tx(&S.bv, 2 * HALF_TILE);
-                    tma_load_3d(t + OFF_V, &tmV, 0, kt * AK, z, &S.bv);
-                    ++nv;
+                if (j >= 0) {  // V^T buffer j & 1 is free once the P.V MMAs of pass-2 step j - 2 read it
+                    const int vb = j & 1;
+                    if (j >= 2 && !await_phase(S, &S.bvr[vb], ((j - 2) >> 1) & 1u, deadline, err)) break;
+                    uint8_t *vt = t + OFF_VT + vb * 2 * HALF_TILE;
+                    mbar_arrive_expect_tx(&S.bv[vb], 2 * HALF_TILE);
+                    tma_load_3d(vt, &tmVT, kt * AK, 0, z, &S.bv[vb]);
+                    tma_load_3d(vt + HALF_TILE, &tmVT, kt * AK + 64, 0, z, &S.bv[vb]);
+                    ++nv[vb];
                 }
             }
             if (S.abort_) {  // let the copies in flight land
@@ -140,19 +149,22 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                     if (nk[b] > 0)
                         while (!mbar_try_wait(&S.bk[b], (nk[b] - 1) & 1u) && global_timer_ns() < dl) {
                         }
-                if (nv > 0)
-                    while (!mbar_try_wait(&S.bv, (nv - 1) & 1u) && global_timer_ns() < dl) {
-                    }
+                for (int b = 0; b < 2; ++b)
+                    if (nv[b] > 0)
+                        while (!mbar_try_wait(&S.bv[b], (nv[b] - 1) & 1u) && global_timer_ns() < dl) {
+                        }
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {  // MMAs
-            const uint32_t q = smem_u32(t + OFF_Q), p = smem_u32(t + OFF_P), vt = smem_u32(t + OFF_VT);
+            const uint32_t q = smem_u32(t + OFF_Q), p = smem_u32(t + OFF_P), vt0 = smem_u32(t + OFF_VT);
             // O += P V^T of pass-2 step s, once the softmax warps wrote P and V^T
             auto pv = [&](int s) -> bool {
-                const int j = s - ntiles;
+                const int j = s - ntiles, vb = j & 1;
                 if (!await_phase(S, &S.bpw, j & 1u, deadline, err)) return false;
+                if (!await_phase(S, &S.bv[vb], (j >> 1) & 1u, deadline, err)) return false;
                 tc_fence_after();
+                const uint32_t vt = vt0 + (uint32_t)vb * 2 * HALF_TILE;
 #pragma unroll
                 for (int kk = 0; kk < AK / 16; ++kk) {
                     const uint32_t off = (uint32_t)(kk >> 2) * HALF_TILE + (uint32_t)(kk & 3) * 32;
@@ -160,6 +172,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                            (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(&S.bo);
+                tc_commit(&S.bvr[vb]);
                 S.nbo_ = j + 1;
                 return true;
             };
@@ -253,18 +266,6 @@ __global__ void __launch_bounds__(A_THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < AK / 8; ++c)
                     *reinterpret_cast<uint4 *>(t + OFF_P + (c >> 3) * HALF_TILE + sw128_offset(row, (8 * c) & 63)) = pk[c];
-                ok = __all_sync(0xffffffffu, await_phase(S, &S.bv, j & 1u, deadline, err));
-                if (!ok) break;
-                // V^T row d = st: 8 keys at a time, gathered from the staged [key][d] tile
-                const __half *vst = reinterpret_cast<const __half *>(t + OFF_V);
-#pragma unroll 2
-                for (int c = 0; c < AK / 8; ++c) {
-                    __align__(16) __half hv[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) hv[i] = vst[(size_t)(8 * c + i) * ADH + st];
-                    *reinterpret_cast<uint4 *>(t + OFF_VT + (c >> 3) * HALF_TILE + sw128_offset(st, (8 * c) & 63)) =
-                        *reinterpret_cast<const uint4 *>(hv);
-                }
                 fence_proxy_async_shared();  // the tensor core reads what these threads wrote
                 tc_fence_before();
                 mbar_arrive(&S.bpw);
@@ -331,7 +332,7 @@ EncodeTiled encoder() {
 
 }  // namespace
 
-lf_status pf_attention_tc(const __half *q16, const __half *kc, const __half *vc, const TcAttnArgs &a, int NL,
+lf_status pf_attention_tc(const __half *q16, const __half *kc, const __half *vt, const TcAttnArgs &a, int NL,
                           uint32_t *err, unsigned long long timeout_ns, cudaStream_t stream) {
     EncodeTiled enc = encoder();
     if (!enc) return LF_ERR_CUDA;
@@ -357,10 +358,12 @@ lf_status pf_attention_tc(const __half *q16, const __half *kc, const __half *vc,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return LF_ERR_CUDA;
     }
-    {
-        const cuuint32_t box[3] = {(cuuint32_t)ADH, (cuuint32_t)AK, 1};
-        if (enc(&mv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half *>(vc), kd, ks, box, e3,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    {  // V^T: [lane-layer-head][128 dims][ctx] FP16, boxes of 64 positions x 128 dims, swizzled
+        const cuuint64_t vd[3] = {(cuuint64_t)a.ctx, (cuuint64_t)ADH, (cuuint64_t)NL * a.L * a.HKV_L};
+        const cuuint64_t vs[2] = {(cuuint64_t)a.ctx * 2, (cuuint64_t)a.ctx * ADH * 2};
+        const cuuint32_t box[3] = {64, (cuuint32_t)ADH, 1};
+        if (enc(&mv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half *>(vt), vd, vs, box, e3,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return LF_ERR_CUDA;
     }

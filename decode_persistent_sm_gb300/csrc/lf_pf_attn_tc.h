@@ -19,9 +19,12 @@ struct TcAttnArgs {
 };
 
 // Causal windowed attention, head dimension 128: q16 [M][NQ * 128] FP16 (RoPE
-// applied), K and V from the lanes' FP16 caches (the new positions already
-// appended).  Enqueued on `stream`; a device-side wait that runs out sets *err.
-lf_status pf_attention_tc(const __half *q16, const __half *kc, const __half *vc, const TcAttnArgs &a, int NL,
+// applied), K from the lanes' FP16 cache and V from vt, the same values
+// transposed ([lane][layer][kv head][128 dims][ctx], positions past those
+// written holding finite values, e.g. zero); the new positions already
+// appended to both.  Enqueued on `stream`; a device-side wait that runs out
+// sets *err.
+lf_status pf_attention_tc(const __half *q16, const __half *kc, const __half *vt, const TcAttnArgs &a, int NL,
                           uint32_t *err, unsigned long long timeout_ns, cudaStream_t stream);
 
 }  // namespace lf

@@ -40,6 +40,22 @@ __global__ void pf_add(float *__restrict__ x, const float *__restrict__ p, size_
         x[i] += p[i];
 }
 
+// vt[z][d][p] = vc[z][p][d] for positions p < P (32 x 32 tiles through shared memory).
+__global__ void pf_transpose_v(const __half *__restrict__ vc, __half *__restrict__ vt, int P, int DH, int ctx) {
+    __shared__ __half tile[32][33];
+    const size_t z = blockIdx.z;
+    const int p0 = blockIdx.x * 32, d0 = blockIdx.y * 32, tx = threadIdx.x;
+    for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+        const int p = p0 + r;
+        tile[r][tx] = p < P ? vc[(z * ctx + p) * DH + d0 + tx] : __float2half(0.f);
+    }
+    __syncthreads();
+    for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+        const int p = p0 + tx;
+        if (p < P) vt[(z * DH + d0 + r) * ctx + p] = tile[tx][r];
+    }
+}
+
 // u = FP16(silu(gate) * up); gu rows are [gate (F) | up (F)]
 __global__ void pf_swiglu(const float *__restrict__ gu, __half *__restrict__ u, int F, size_t n) {
     for (size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x; t < n; t += (size_t)gridDim.x * blockDim.x) {
@@ -356,6 +372,16 @@ extern "C" lf_status lf_prefill_batched(lf_engine *e, const int32_t *tokens, int
         e->pf_bytes = need.bytes;
     }
     const PfBufs b = carve(static_cast<uint8_t *>(e->pf_mem), s, M, !tc_attn, !fused_swiglu);
+    const size_t z_count = (size_t)s.NL * s.L * s.HKV_L;
+    if (tc_attn && !e->pf_vt) {  // V transposed beside the cache, zero where nothing was written yet
+        const size_t bytes = z_count * s.ctx * DH * sizeof(__half);
+        if (cudaMalloc(&e->pf_vt, bytes) != cudaSuccess) {
+            (void)cudaGetLastError();
+            e->pf_vt = nullptr;
+            return LF_ERR_OOM;
+        }
+        if (cudaMemsetAsync(e->pf_vt, 0, bytes, st) != cudaSuccess) return pf_fail(e);
+    }
 
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
@@ -368,6 +394,10 @@ extern "C" lf_status lf_prefill_batched(lf_engine *e, const int32_t *tokens, int
     });
     if (attr_err != cudaSuccess) return pf_fail(e);
 
+    // the positions before this prompt (decode steps or an earlier prefill) into the transposed copy
+    if (tc_attn && p0 > 0)
+        pf_transpose_v<<<dim3((p0 + 31) / 32, DH / 32, (unsigned)z_count), dim3(32, 8), 0, st>>>(e->vc, e->pf_vt, p0,
+                                                                                                 DH, s.ctx);
     if (cudaMemcpyAsync(b.tok, tokens, (size_t)M * sizeof(int), cudaMemcpyHostToDevice, st) != cudaSuccess ||
         cudaMemsetAsync(e->pf_err, 0, sizeof(uint32_t), st) != cudaSuccess)
         return pf_fail(e);
@@ -391,6 +421,7 @@ extern "C" lf_status lf_prefill_batched(lf_engine *e, const int32_t *tokens, int
             qe.qf = tc_attn ? nullptr : b.qf;
             qe.kc = e->kc;
             qe.vc = e->vc;
+            qe.vt = tc_attn ? e->pf_vt : nullptr;
             qe.rope = e->rope;
             qe.kv_first = e->d_kvfirst;
             qe.p0 = p0;
@@ -407,7 +438,7 @@ extern "C" lf_status lf_prefill_batched(lf_engine *e, const int32_t *tokens, int
             const dim3 ag((M + PF_QB - 1) / PF_QB, NQ);
             if (tc_attn) {
                 lf::TcAttnArgs ta{M, p0, NQ, s.HQ_L, s.GL, s.HKV_L, L, l, s.ctx, e->cfg.swa_window[l], scale, b.o, QD};
-                gs = lf::pf_attention_tc(b.q16, e->kc, e->vc, ta, s.NL, e->pf_err, kGemmTimeoutNs, st);
+                gs = lf::pf_attention_tc(b.q16, e->kc, e->pf_vt, ta, s.NL, e->pf_err, kGemmTimeoutNs, st);
                 if (gs != LF_OK) return gs == LF_ERR_CUDA ? pf_fail(e) : gs;
             } else if (DH == 128)
                 pf_attention<128><<<ag, 128, pf_attn_smem<128>(), st>>>(b.qf, e->kc, e->vc, b.o, M, p0, NQ, s.HQ_L,

@@ -191,6 +191,7 @@ void lf_destroy(lf_engine *e) {
     for (void *p : e->allocs) cudaFree(p);
     if (e->trace) cudaFree(e->trace);
     if (e->pf_mem) cudaFree(e->pf_mem);
+    if (e->pf_vt) cudaFree(e->pf_vt);
     if (e->h_status) cudaFreeHost(e->h_status);
     delete e;
 }

@@ -236,7 +236,16 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                             for (int lam = 0; lam < qe.NL; ++lam) {
                                 const int g = kh - qe.kv_first[lam];
                                 if (g < 0 || g >= qe.HKV_L) continue;
-                                put(cache + ((((size_t)lam * qe.L + qe.l) * qe.HKV_L + g) * qe.ctx + pos) * DH);
+                                const size_t z = ((size_t)lam * qe.L + qe.l) * qe.HKV_L + g;
+                                put(cache + (z * qe.ctx + pos) * DH);
+                                if (!is_k && qe.vt) {  // and transposed: a warp's 32 positions are contiguous
+                                    __half *col = qe.vt + z * DH * qe.ctx + pos;
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i) {
+                                        col[(size_t)(c0 + i) * qe.ctx] = ha[i];
+                                        col[(size_t)(half + c0 + i) * qe.ctx] = hb[i];
+                                    }
+                                }
                             }
                         }
                     }

@@ -28,6 +28,7 @@ struct QkvEpi {
     __half *q16 = nullptr;  // [M][NQ * DH] rotated queries (FP16)
     float *qf = nullptr;    // the same in fp32 (nullable)
     __half *kc = nullptr, *vc = nullptr;  // per-lane caches [NL][L][HKV_L][ctx][DH]
+    __half *vt = nullptr;                 // V transposed, [NL][L][HKV_L][DH][ctx] (nullable)
     const float2 *rope = nullptr;         // [ctx][DH / 2] (cos, sin)
     const int *kv_first = nullptr;        // device: first KV head of each lane
     int p0 = 0, NQ = 0, NKV = 0, DH = 0, NL = 0, L = 0, l = 0, HKV_L = 0, ctx = 0;

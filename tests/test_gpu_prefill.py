@@ -154,3 +154,29 @@ def test_tensor_core_and_cuda_core_attention_agree_past_the_window():
     assert rel_l2(g1, g0) <= REL_L2 and a1 == a0
     for (l1, m1), (l0, m0) in zip(s1, s0):
         assert rel_l2(l1, l0) <= REL_L2 and m1 == m0
+
+
+@pytest.mark.slow
+def test_tensor_core_attention_after_decode_steps():
+    # a prefill that starts at position 37, after decode steps: the tensor-core
+    # attention reads the earlier positions' V through the transposed copy, the
+    # CUDA-core attention from the cache itself; both must give the same function
+    from decode_persistent_sm_gb300 import Engine
+    shape = synth.FULL
+    blob = synth.make_weights(shape, 6)
+    tokens = synth.make_tokens(6, 37 + 150 + 3, shape.vocab)
+    out = {}
+    with Engine.from_shape(shape) as eng:
+        eng.load_weights(blob)
+        for tc in (True, False):
+            eng.reset()
+            eng.set_prefill_attention(tc)
+            for t in tokens[:37]:
+                eng.decode_step(int(t))
+            got, am = eng.prefill_batched(tokens[37:187])
+            steps = [eng.decode_step(int(t)) for t in tokens[187:]]
+            out[tc] = (got, am, steps)
+    (g1, a1, s1), (g0, a0, s0) = out[True], out[False]
+    assert rel_l2(g1, g0) <= REL_L2 and a1 == a0
+    for (l1, m1), (l0, m0) in zip(s1, s0):
+        assert rel_l2(l1, l0) <= REL_L2 and m1 == m0
