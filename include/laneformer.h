@@ -279,7 +279,8 @@ lf_status lf_decode_step_static_scratch(lf_engine *e, int32_t token, float *logi
  * argmax (host, nullable) receive the last position's result, which also
  * stays on the device (lf_get_logits_device / lf_get_argmax_device).
  * Scratch is allocated on first use and kept (about 0.14 MB per position
- * at full shape, delay 2).  Synchronous.  LF_ERR_INVALID_ARG for n < 1, a
+ * at full shape, delay 2, plus a transposed copy of the V caches, the size
+ * of the V cache, for the tensor-core attention).  Synchronous.  LF_ERR_INVALID_ARG for n < 1, a
  * NULL tokens array or a token outside [0, vocab); LF_ERR_CTX_OVERFLOW if
  * position + n > ctx_cap; LF_ERR_OOM when the resident weights or the
  * scratch could not be allocated; LF_ERR_TIMEOUT if a GEMM's device-side
