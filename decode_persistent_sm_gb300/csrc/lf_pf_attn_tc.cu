@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0) {  // MMAs
             const uint32_t q = smem_u32(t + OFF_Q), p = smem_u32(t + OFF_P), vt0 = smem_u32(t + OFF_VT);
-            // O += P V^T of pass-2 step s, once the softmax warps wrote P and V^T
+            // O += P V^T of pass-2 step s, once the softmax warps wrote P and V^T has arrived
             auto pv = [&](int s) -> bool {
                 const int j = s - ntiles, vb = j & 1;
                 if (!await_phase(S, &S.bpw, j & 1u, deadline, err)) return false;

@@ -5,10 +5,11 @@
 // vector, so the prompt's forward needs no lanes: sub-block s reads
 // x(s) = e + sum_{u <= s-1-2d} P[u], where P[u] is the full projection output
 // of sub-block u (the lanes' partials summed).  Each sub-block runs over all
-// n positions at once: RMSNorm to FP16, one tensor-core GEMM against the
-// weight matrix in its file layout, then RoPE + KV-cache append (attention)
-// or SwiGLU (FFN), causal windowed attention over the cache, and a second
-// GEMM whose output is P[s]; P[s] joins the residual 2d + 1 sub-blocks later.
+// n positions at once: the arriving partial added and the RMSNorm to FP16 in
+// one kernel, one tensor-core GEMM against the weight matrix in its file
+// layout with RoPE + the KV-cache append (attention) or SwiGLU (FFN) in its
+// epilogue, causal windowed attention over the cache, and a second GEMM whose
+// output is P[s]; P[s] joins the residual 2d + 1 sub-blocks later.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 

@@ -9,14 +9,21 @@
 // epilogue writes U[M][F] = FP16(silu(gate) * up) and the fp32 gate/up
 // product never reaches memory.
 //
+// QKV variant: the epilogue applies RoPE to the q and k columns (a 256-column
+// tile holds whole heads, so both columns of each pair are in the thread's
+// row) and writes q in FP16 (and fp32 on request), k and v into the FP16
+// caches of every lane that reads the head and v also transposed; the fp32
+// product never reaches memory.
+//
 // A persistent CTA per SM walks 128 x 256 tiles of C in a grouped order: a
 // copy warp streams 128 x 64 and 256 x 64 tiles of A and B into a 4-stage
 // shared-memory ring with TMA (128-byte swizzle), one elected thread of the
 // MMA warp issues tcgen05.mma (kind::f16, fp32 accumulators in one of two
 // 256-column TMEM buffers) and releases each stage with tcgen05.commit, and
 // four epilogue warps read a finished accumulator back with tcgen05.ld (each
-// warp its 32 TMEM lanes = rows) and store it while the next tile's MMAs run.  Every wait is bounded: on a timeout the CTA records an error,
-// lets its copies and MMAs in flight finish (bounded), frees TMEM and exits.
+// warp its 32 TMEM lanes = rows) and store it while the next tile's MMAs run.
+// Every wait is bounded: on a timeout the CTA records an error, lets its
+// copies and MMAs in flight finish (bounded), frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
