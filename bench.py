@@ -419,7 +419,7 @@ GEN_WORKLOADS = {
 SWEEP_CTX, SWEEP_STEPS = 2048, 256
 PREFILL_N = 3584
 PASSN = (128, 8, 256, 0.8, 0.95)  # prompt, samples, tokens per sample, temperature, top_p
-BATCH_SWEEP = (512, 64, (1, 2, 4, 8, 16))  # KV fill, greedy steps per batch size, batch sizes
+BATCH_SWEEP = (512, 64, (1, 2, 4, 8, 16))  # KV fill (--position), greedy steps per batch size, batch sizes
 
 
 def timed_generation(eng, stream, first_token: int, n: int):
@@ -684,7 +684,8 @@ def run_generation(args, world, rank, local):
         return
 
     if args.workload == "batch":
-        fill, n_tok, sizes = BATCH_SWEEP
+        _, n_tok, sizes = BATCH_SWEEP
+        fill = POS  # --position: the KV fill every sample starts from (default 512)
         if args.batch:  # one batch size, at most 64 steps (profiling runs)
             sizes, n_tok = (args.batch,), min(args.steps, n_tok)
         shape = base
