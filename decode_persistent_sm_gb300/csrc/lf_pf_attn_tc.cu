@@ -2,21 +2,21 @@
 // (sm_103a, tcgen05 + TMA), head dimension 128.
 //
 // One CTA = 128 queries of one q head (one TMEM lane per query).  Keys of the
-// head's FP16 cache come in tiles of 128.  Two passes over the key tiles:
-//   pass 1: S = Q K^T (tcgen05.mma into TMEM, 128 columns); each of the
-//           four softmax warps reads its 32 rows (tcgen05.ld, one query row
-//           per thread) and keeps the row's max (no exponentials);
-//   pass 2: S again; P = exp(S - max) (the row sum accumulated in fp32 from
-//           the same exponentials) in FP16 written to shared memory in the
-//           128-byte-swizzled K-major operand layout; the V^T tile ([dim][key],
-//           written transposed beside the cache by the QKV projection) comes
-//           by TMA straight into the same layout, double-buffered; O += P V^T
-//           (tcgen05.mma into TMEM columns 256..383), so O never needs
-//           rescaling.
+// head's FP16 cache come in tiles of 128, one pass over them:
+//   S = Q K^T (tcgen05.mma into TMEM, 128 columns); each of the four softmax
+//   warps reads its 32 rows (tcgen05.ld, one query row per thread), updates
+//   the row's running max m and writes P = exp(S - m) in FP16 to shared memory
+//   in the 128-byte-swizzled K-major operand layout (the row sum accumulated
+//   in fp32 from the same exponentials); the V^T tile ([dim][key], written
+//   transposed beside the cache by the QKV projection) comes by TMA straight
+//   into the same layout, double-buffered; O += P V^T (tcgen05.mma into TMEM
+//   columns 256..383).  The running max moves lazily: only when a row's max
+//   grows by more than 2^8 (so P stays below 256) are its O row (tcgen05.ld /
+//   scale / tcgen05.st, after the previous P.V is done) and its sum rescaled.
 // K tiles and S are double-buffered (two shared-memory K buffers, two sets
-// of TMEM columns), so S of the next step is computed while the softmax
-// warps work on this one, and the P.V MMAs of a step overlap the next
-// step's softmax.
+// of TMEM columns), so S of the next tile is computed while the softmax
+// warps work on this one, and the P.V MMAs of a tile overlap the next
+// tile's softmax.
 // Finally O / sum is stored per row.  Warp 0 issues the TMA copies, one
 // thread of warp 1 issues the MMAs (and owns the TMEM allocation), warps 2-5
 // do the softmax.  Every wait is bounded; a timed-out CTA records the error,
@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     const int rows = min(AQ, a.M - i0);
     const int p_first = a.p0 + i0, p_last = a.p0 + i0 + rows - 1;
     const int lo = a.window > 0 ? max(0, p_first - a.window + 1) : 0, hi = p_last;
-    const int kt0 = lo / AK, ntiles = hi / AK - kt0 + 1, nsteps = 2 * ntiles;
+    const int kt0 = lo / AK, ntiles = hi / AK - kt0 + 1, nsteps = ntiles;  // one step per key tile
     const int lam = h / a.HQ_L, g = (h % a.HQ_L) / a.GL, z = (lam * a.L + a.l) * a.HKV_L + g;
     const uint64_t deadline = global_timer_ns() + timeout_ns;
 
@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
             tma_load_2d(t + OFF_Q, &tmQ, h * ADH, i0, &S.bq);
             tma_load_2d(t + OFF_Q + HALF_TILE, &tmQ, h * ADH + 64, i0, &S.bq);
             for (int step = 0; step < nsteps; ++step) {
-                const int b = step & 1, kt = kt0 + step % ntiles, j = step - ntiles;
+                const int b = step & 1, kt = kt0 + step, j = step;
                 // K buffer b is free once S of step - 2 is computed
                 if (step >= 2 && !await_phase(S, &S.bs[b], ((step - 2) >> 1) & 1u, deadline, err)) break;
                 uint8_t *kb = t + OFF_K + b * 2 * HALF_TILE;
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                 tma_load_3d(kb, &tmK, 0, kt * AK, z, &S.bk[b]);
                 tma_load_3d(kb + HALF_TILE, &tmK, 64, kt * AK, z, &S.bk[b]);
                 ++nk[b];
-                if (j >= 0) {  // V^T buffer j & 1 is free once the P.V MMAs of pass-2 step j - 2 read it
+                {  // V^T buffer j & 1 is free once the P.V MMAs of step j - 2 read it
                     const int vb = j & 1;
                     if (j >= 2 && !await_phase(S, &S.bvr[vb], ((j - 2) >> 1) & 1u, deadline, err)) break;
                     uint8_t *vt = t + OFF_VT + vb * 2 * HALF_TILE;
@@ -158,9 +158,9 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0) {  // MMAs
             const uint32_t q = smem_u32(t + OFF_Q), p = smem_u32(t + OFF_P), vt0 = smem_u32(t + OFF_VT);
-            // O += P V^T of pass-2 step s, once the softmax warps wrote P and V^T has arrived
+            // O += P V^T of step s, once the softmax warps wrote P and V^T has arrived
             auto pv = [&](int s) -> bool {
-                const int j = s - ntiles, vb = j & 1;
+                const int j = s, vb = j & 1;
                 if (!await_phase(S, &S.bpw, j & 1u, deadline, err)) return false;
                 if (!await_phase(S, &S.bv[vb], (j >> 1) & 1u, deadline, err)) return false;
                 tc_fence_after();
@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                 }
                 tc_commit(&S.bs[b]);
                 S.nbs_[b] = (step >> 1) + 1;
-                if (step >= 1 && step - 1 >= ntiles) ok = pv(step - 1);  // overlaps the softmax of this step
+                if (step >= 1) ok = pv(step - 1);  // overlaps the softmax of this step
             }
             if (ok) pv(nsteps - 1);
         }
@@ -205,71 +205,87 @@ __global__ void __launch_bounds__(A_THREADS, 1)
         const float sc2 = a.scale * kLog2e;  // scores in the log2 domain
         float m2 = -INFINITY, l = 0.f;
         bool ok = true;
+        constexpr float kLazy = 8.f;  // log2 of the largest P before the max moves
         for (int step = 0; step < nsteps; ++step) {
-            const int b = step & 1, kt = kt0 + step % ntiles, j = step - ntiles;
+            const int b = step & 1, kt = kt0 + step, j = step;
             const int vlo = klo - kt * AK, vhi = khi - kt * AK;  // valid columns of the tile
             ok = __all_sync(0xffffffffu, ok && await_phase(S, &S.bs[b], (step >> 1) & 1u, deadline, err));
             if (!ok) break;
             tc_fence_after();
             const uint32_t sb = trow + (uint32_t)b * AK;
-            if (j < 0) {  // pass 1: the row's max (on raw scores; sc2 > 0 scales it once at the end)
-                float mr = -INFINITY;
+            // the tile's max of the row (raw scores; sc2 > 0 scales it once)
+            float mr = -INFINITY;
 #pragma unroll 1
-                for (int c0 = 0; c0 < AK; c0 += 32) {
-                    float v[32];
-                    tc_ld32(sb + (uint32_t)c0, v);
-                    if (c0 >= vlo && c0 + 31 <= vhi) {  // the whole chunk is in the row's key range
+            for (int c0 = 0; c0 < AK; c0 += 32) {
+                float v[32];
+                tc_ld32(sb + (uint32_t)c0, v);
+                if (c0 >= vlo && c0 + 31 <= vhi) {  // the whole chunk is in the row's key range
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) mr = fmaxf(mr, v[i]);
-                    } else {
+                    for (int i = 0; i < 32; ++i) mr = fmaxf(mr, v[i]);
+                } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int col = c0 + i;
-                            if (col >= vlo && col <= vhi) mr = fmaxf(mr, v[i]);
-                        }
+                    for (int i = 0; i < 32; ++i) {
+                        const int col = c0 + i;
+                        if (col >= vlo && col <= vhi) mr = fmaxf(mr, v[i]);
                     }
                 }
-                if (mr != -INFINITY) m2 = fmaxf(m2, mr * sc2);
-                tc_fence_before();
-                mbar_arrive(&S.bp[b]);
-            } else {  // pass 2: P of the row in registers, then into shared memory
-                uint4 pk[AK / 8];
-#pragma unroll
-                for (int c0 = 0; c0 < AK; c0 += 32) {
-                    float v[32];
-                    tc_ld32(sb + (uint32_t)c0, v);
-                    const bool full = c0 >= vlo && c0 + 31 <= vhi;  // no column of the chunk is masked
-#pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) {
-                        __align__(16) __half2 hv[4];
-#pragma unroll
-                        for (int i = 0; i < 8; i += 2) {
-                            const int col = c0 + 8 * c8 + i;
-                            float p0 = exp2f(fmaf(v[8 * c8 + i], sc2, -m2));
-                            float p1 = exp2f(fmaf(v[8 * c8 + i + 1], sc2, -m2));
-                            if (!full) {
-                                p0 = (col >= vlo && col <= vhi) ? p0 : 0.f;
-                                p1 = (col + 1 >= vlo && col + 1 <= vhi) ? p1 : 0.f;
-                            }
-                            l += p0 + p1;
-                            hv[i / 2] = __floats2half2_rn(p0, p1);
-                        }
-                        pk[c0 / 8 + c8] = *reinterpret_cast<const uint4 *>(hv);
-                    }
-                }
-                tc_fence_before();
-                mbar_arrive(&S.bp[b]);  // S buffer b may be recomputed
-                if (j > 0) {  // the previous P.V MMAs must have read P and V^T
-                    ok = __all_sync(0xffffffffu, await_phase(S, &S.bo, (j - 1) & 1u, deadline, err));
-                    if (!ok) break;
-                }
-#pragma unroll
-                for (int c = 0; c < AK / 8; ++c)
-                    *reinterpret_cast<uint4 *>(t + OFF_P + (c >> 3) * HALF_TILE + sw128_offset(row, (8 * c) & 63)) = pk[c];
-                fence_proxy_async_shared();  // the tensor core reads what these threads wrote
-                tc_fence_before();
-                mbar_arrive(&S.bpw);
             }
+            // the running max moves only by more than kLazy (then O and the sum are rescaled)
+            float fac = 1.f;
+            if (mr != -INFINITY && mr * sc2 > m2 + kLazy) {
+                const float mn = mr * sc2;
+                fac = exp2f(m2 - mn);  // 0 while the row had no key yet (O and l are 0 then)
+                l *= fac;
+                m2 = mn;
+            }
+            // P of the row in registers
+            uint4 pk[AK / 8];
+#pragma unroll
+            for (int c0 = 0; c0 < AK; c0 += 32) {
+                float v[32];
+                tc_ld32(sb + (uint32_t)c0, v);
+                const bool full = c0 >= vlo && c0 + 31 <= vhi;  // no column of the chunk is masked
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    __align__(16) __half2 hv[4];
+#pragma unroll
+                    for (int i = 0; i < 8; i += 2) {
+                        const int col = c0 + 8 * c8 + i;
+                        float p0 = exp2f(fmaf(v[8 * c8 + i], sc2, -m2));
+                        float p1 = exp2f(fmaf(v[8 * c8 + i + 1], sc2, -m2));
+                        if (!full) {
+                            p0 = (col >= vlo && col <= vhi) ? p0 : 0.f;
+                            p1 = (col + 1 >= vlo && col + 1 <= vhi) ? p1 : 0.f;
+                        }
+                        l += p0 + p1;
+                        hv[i / 2] = __floats2half2_rn(p0, p1);
+                    }
+                    pk[c0 / 8 + c8] = *reinterpret_cast<const uint4 *>(hv);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&S.bp[b]);  // S buffer b may be recomputed
+            if (j > 0) {  // the previous P.V MMAs must be done: they read P, and O may be rescaled
+                ok = __all_sync(0xffffffffu, await_phase(S, &S.bo, (j - 1) & 1u, deadline, err));
+                if (!ok) break;
+                if (__any_sync(0xffffffffu, fac != 1.f)) {  // rescale the O rows of this warp (1 elsewhere)
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c0 = 0; c0 < ADH; c0 += 32) {
+                        float o[32];
+                        tc_ld32(trow + TM_O + (uint32_t)c0, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] *= fac;
+                        tc_st32(trow + TM_O + (uint32_t)c0, o);
+                    }
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < AK / 8; ++c)
+                *reinterpret_cast<uint4 *>(t + OFF_P + (c >> 3) * HALF_TILE + sw128_offset(row, (8 * c) & 63)) = pk[c];
+            fence_proxy_async_shared();  // the tensor core reads what these threads wrote
+            tc_fence_before();
+            mbar_arrive(&S.bpw);
         }
         // epilogue: O / l of this row
         if (ok) ok = __all_sync(0xffffffffu, await_phase(S, &S.bo, (ntiles - 1) & 1u, deadline, err));
