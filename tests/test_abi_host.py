@@ -123,3 +123,18 @@ def test_own_lane_plan_adds_a_lane_sum_per_sub_block(lib, lanes, delay):
     # keep separate global sums (one more REDUCE and one more ADD)
     assert b[3] == a[3] + 2 * (2 * shape.n_layers) + 2
 
+
+
+def test_header_is_plain_c(tmp_path):
+    # the boundary is a C ABI: the header compiles as ISO C99 (no C++ or torch types)
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if not cc:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "laneformer.h"\nint main(void) { return (int)LF_OK; }\n')
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only", "-I", inc,
+                        str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
