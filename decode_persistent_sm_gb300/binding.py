@@ -15,7 +15,7 @@ TRACE_WORDS = 6  # LF_TRACE_WORDS
 STATUS = {
     0: "LF_OK", 1: "LF_ERR_INVALID_ARG", 2: "LF_ERR_OOM", 3: "LF_ERR_CUDA",
     4: "LF_ERR_NOT_LOADED", 5: "LF_ERR_CTX_OVERFLOW", 6: "LF_ERR_TIMEOUT",
-    7: "LF_ERR_UNSUPPORTED",
+    7: "LF_ERR_UNSUPPORTED", 8: "LF_ERR_BOUNDS",
 }
 
 # Every function declared in include/laneformer.h with its ctypes signature.
@@ -60,6 +60,9 @@ _SIGS = {
     "lf_batch_step": (_ci, [_vp, _vp, _vp, _vp]),
     "lf_batch_generate": (_ci, [_vp, _vp, _ci, ctypes.c_float, ctypes.c_float, ctypes.c_uint64, _vp]),
     "lf_gemv_f16": (_ci, [_vp, _vp, _vp, _ci, _ci, _ci, _vp]),
+    "lf_stream_read": (_ci, [_vp, ctypes.c_size_t, _vp, _ci, _vp, _vp]),
+    "lf_debug_canaries": (_ci, [_vp, ctypes.POINTER(_ci)]),
+    "lf_debug_corrupt_canary": (_ci, [_vp, _ci, _ci]),
 }
 
 
@@ -78,28 +81,31 @@ class LaneformerError(RuntimeError):
         super().__init__(f"{call}: {STATUS.get(code, code)}")
 
 
-_lib = None
+_DEBUG_LIB_PATH = os.path.join(_PKG, "liblaneformer_debug.so")
+_libs = {}
 
 
-def library_path() -> str:
-    return _LIB_PATH
+def library_path(debug: bool = False) -> str:
+    return _DEBUG_LIB_PATH if debug else _LIB_PATH
 
 
-def load_library():
-    """Loads liblaneformer.so; raises if it has not been built."""
-    global _lib
-    if _lib is None:
-        if not os.path.exists(_LIB_PATH):
+def load_library(debug: bool = False):
+    """Loads liblaneformer.so (or its debug build, liblaneformer_debug.so:
+    device-side bounds checks and buffer canaries); raises if it has not been
+    built."""
+    if debug not in _libs:
+        path = library_path(debug)
+        if not os.path.exists(path):
             raise RuntimeError(
-                f"{_LIB_PATH} is missing: build the CUDA engine first "
+                f"{path} is missing: build the CUDA engine first "
                 "(python -c 'import __graft_entry__ as g; g.build()')")
-        lib = ctypes.CDLL(_LIB_PATH)
+        lib = ctypes.CDLL(path)
         for name, (res, args) in _SIGS.items():
             fn = getattr(lib, name)
             fn.restype = res
             fn.argtypes = args
-        _lib = lib
-    return _lib
+        _libs[debug] = lib
+    return _libs[debug]
 
 
 def config_from_shape(shape, **overrides) -> LfConfig:
@@ -136,6 +142,14 @@ def gemv_f16(w_ptr: int, x_ptr: int, y_ptr: int, n: int, k: int, batch: int, str
     _check("lf_gemv_f16", lib.lf_gemv_f16(w_ptr, x_ptr, y_ptr, int(n), int(k), int(batch), stream))
 
 
+def stream_read(src_ptr: int, nbytes: int, sink_ptr: int, sink_len: int, status_ptr: int,
+                stream: Optional[int] = None):
+    """lf_stream_read: enqueue one read-only pass over nbytes of device memory
+    in the decode kernel's copy pattern (a measurement of the read ceiling)."""
+    lib = load_library()
+    _check("lf_stream_read", lib.lf_stream_read(src_ptr, int(nbytes), sink_ptr, int(sink_len), status_ptr, stream))
+
+
 def sample_token(logits_ptr: int, vocab: int, temperature: float, top_p: float, seed: int, position: int,
                  sample: int, token_ptr: int, stream: Optional[int] = None):
     """lf_sample: enqueue one draw from device logits into a device int32."""
@@ -157,8 +171,8 @@ def plan_stats(cfg: LfConfig, n_sm: int) -> Tuple[int, np.ndarray]:
 class Engine:
     """One decode session on the current CUDA device."""
 
-    def __init__(self, cfg: LfConfig):
-        self._lib = load_library()
+    def __init__(self, cfg: LfConfig, debug: bool = False):
+        self._lib = load_library(debug)
         self.cfg = cfg
         self.vocab = cfg.vocab
         h = _vp()
@@ -166,8 +180,8 @@ class Engine:
         self._h = h
 
     @classmethod
-    def from_shape(cls, shape, **overrides) -> "Engine":
-        return cls(config_from_shape(shape, **overrides))
+    def from_shape(cls, shape, debug: bool = False, **overrides) -> "Engine":
+        return cls(config_from_shape(shape, **overrides), debug=debug)
 
     def close(self):
         if getattr(self, "_h", None):

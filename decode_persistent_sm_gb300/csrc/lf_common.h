@@ -11,6 +11,32 @@
 
 namespace lf {
 
+// Debug build (compiled with -DLF_DEBUG, liblaneformer_debug.so): the decode
+// kernel checks every ring, KV, tile, partial and output index before it
+// uses it, and every engine buffer carries canary words before and after it
+// that the host checks after each step.  A failed check records the error
+// word kErrBounds + site (the access is skipped, no trap), and the call
+// returns LF_ERR_BOUNDS.  In the release build the checks compile away.
+#ifdef LF_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+constexpr uint32_t kErrBounds = 0x100;
+constexpr int kGuardBytes = 256;        // canary region before and after each engine buffer
+constexpr unsigned char kGuardByte = 0xA5;
+enum BoundsSite : int {
+    SITE_WEIGHT_TILE = 1,  // a weight tile past the end of the CTA's stream
+    SITE_KV_APPEND = 2,    // the KV append outside the cache (position, lane, head)
+    SITE_KV_TILE = 3,      // an attention K / V tile outside the cache or the tile buffer
+    SITE_QKV_ROW = 4,      // a q / k / v value outside the lane's row, or the RoPE table
+    SITE_UNITS = 5,        // a GEMV input or SwiGLU unit past the shared buffers
+    SITE_PARTIAL = 6,      // a lane-sum partial index (sub-block, slot, pieces)
+    SITE_LANE_SUM = 7,     // a lane sum R[u] index
+    SITE_ATTN_PART = 8,    // an attention partial (acc, m, l) index or a merge row
+    SITE_LOGIT = 9,        // an LM-head row past the vocabulary
+};
+
 // CTA shape: 16 streaming warps run the GEMVs over weight tiles that 1
 // producer warp streams into a ring of shared-memory stages with bulk copies;
 // 2 attention warps run split-K attention and the o_proj merge on the side

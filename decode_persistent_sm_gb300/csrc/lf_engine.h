@@ -54,6 +54,12 @@ struct lf_engine {
     size_t dev_bytes = 0;
     long long launches = 0;
     std::vector<void *> allocs;
+    // debug build: the canary regions (kGuardBytes each) before and after
+    // every buffer allocated at create / load time
+    struct Guard {
+        unsigned char *front, *back;
+    };
+    std::vector<Guard> guards;
     unsigned long long *trace = nullptr;  // lf_debug_trace buffer (owned separately)
 };
 

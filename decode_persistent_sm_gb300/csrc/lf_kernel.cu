@@ -124,6 +124,25 @@ __device__ __forceinline__ void record_error(const KParams &p, volatile int *abo
     *abort_flag = 1;
 }
 
+// Debug build: false (and the error word kErrBounds + site, with the index)
+// when `ok` fails; the caller then skips the access.  The release build
+// compiles this to `true`.
+__device__ __forceinline__ bool in_bounds(const KParams &p, volatile int *abort_flag, bool ok, int site,
+                                          long long index, int op) {
+    if constexpr (kDebugChecks) {
+        if (!ok) {
+            if (atomicCAS(&p.err[0], 0u, kErrBounds + (uint32_t)site) == 0u) {
+                p.err[1] = (uint32_t)op;
+                p.err[2] = (uint32_t)blockIdx.x;
+                p.err[3] = (uint32_t)index;
+            }
+            *abort_flag = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
 // ============================================================ streaming warps
 template <int D, int DH>
 struct Streamer {
@@ -152,6 +171,9 @@ struct Streamer {
     // pieces one chunk's summing warp needs are contiguous.
     __device__ size_t pidx(int c) const { return ((size_t)(c >> 5) * p.n_cta + cta) * kRChunk + (c & 31); }
     __device__ void fail(uint32_t code) { record_error(p, &S.abort_, code, S.cur_op); }
+    __device__ bool ok(bool cond, int site, long long index) {
+        return in_bounds(p, &S.abort_, cond, site, index, S.cur_op);
+    }
 
     // Thread 0 polls `ptr` until it reaches `target` (wrap-safe), the global
     // error word is set, or the deadline passes.  All streamers leave together.
@@ -232,6 +254,7 @@ struct Streamer {
     }
 
     __device__ void load_r(int u, float *dst, bool accumulate) {
+        if (!ok(u >= 0 && u < 2 * p.L, SITE_LANE_SUM, u)) return;
         const float *r = p.R + (size_t)u * D;
 #pragma unroll
         for (int i = 0; i < C::NCHT; ++i) {
@@ -467,6 +490,7 @@ struct Streamer {
     // CTA's full-width partial into the lane-sum slot `out`.  onto = true
     // starts from the partial already there, which this same thread wrote.
     __device__ void axpy_op(int n_rows, const float *coef, float *out, bool onto) {
+        if (!ok(n_rows <= kMaxUnitsPerCta && n_rows <= kMaxORowsPerCta, SITE_UNITS, n_rows)) n_rows = 0;
         float acc[C::NX];
         if constexpr (C::kBlockRow) {
 #pragma unroll
@@ -547,13 +571,16 @@ struct Streamer {
         // RoPE factors of this thread's pair in the first block, fetched now so
         // that the load is long done when the epilogue runs.
         float2 cs0 = make_float2(1.f, 0.f);
-        if (tid < min(lp.qkv_n, kRedRows / 2))
+        const bool pos_ok = ok(p.pos >= 0 && p.pos < p.ctx, SITE_QKV_ROW, p.pos);
+        if (tid < min(lp.qkv_n, kRedRows / 2) && pos_ok)
             cs0 = __ldg(p.rope + (size_t)p.pos * half + (lp.qkv_begin + tid) % half);
         dot_op(2 * lp.qkv_n, [&](int b0, int nb) {
             const int t = tid;
             if (t < nb / 2) {
                 const int j = lp.qkv_begin + b0 / 2 + t;
                 const int hs = j / half, c = j % half;
+                if constexpr (kDebugChecks)
+                    if (!ok(hs < p.HQ_L + 2 * p.HKV_L && pos_ok, SITE_QKV_ROW, j)) return;
                 const float inv = inv_rms();
                 float a = row_sum(2 * t) * inv, b = row_sum(2 * t + 1) * inv;
                 if (hs < p.HQ_L + p.HKV_L) {  // RoPE on q and k
@@ -572,8 +599,10 @@ struct Streamer {
                     __half *cache = isk ? p.kc : p.vc;
                     const size_t at =
                         ((((size_t)lane_id * p.L + l) * p.HKV_L + g) * p.ctx + p.pos) * DH;
-                    cache[at + c] = ha;
-                    cache[at + c + half] = hb;
+                    if (ok(lane_id < p.NL && l < p.L && g >= 0 && g < p.HKV_L, SITE_KV_APPEND, g)) {
+                        cache[at + c] = ha;
+                        cache[at + c + half] = hb;
+                    }
                 }
                 qkvb[hs * DH + c] = a;
                 qkvb[hs * DH + c + half] = b;
@@ -591,7 +620,7 @@ struct Streamer {
         const LayerPlan lp = p.lp[(size_t)cta * p.L + l];
         dot_op(2 * lp.ffn_n, [&](int b0, int nb) {
             const int t = tid;
-            if (t < nb / 2) {
+            if (t < nb / 2 && ok(b0 / 2 + t < kMaxUnitsPerCta, SITE_UNITS, b0 / 2 + t)) {
                 const float inv = inv_rms();
                 const float a = row_sum(2 * t) * inv, b = row_sum(2 * t + 1) * inv;
                 S.ubuf[b0 / 2 + t] = a / (1.f + expf(-a)) * b;
@@ -605,6 +634,7 @@ struct Streamer {
     __device__ void down(int l) {
         const LayerPlan lp = p.lp[(size_t)cta * p.L + l];
         const int u = 2 * l + 1;
+        if (!ok(u < 2 * p.L && p.pslots > 0, SITE_PARTIAL, u)) return;
         axpy_op(lp.ffn_n, S.ubuf, p.part + (size_t)(u % p.pslots) * p.n_cta * D, false);
         if (p.tail_fused && l == p.L - 1) return;  // each thread reads back only its own columns
         arrive_partial(u);
@@ -627,6 +657,7 @@ struct Streamer {
         cons_sync();
         const bool fused = p.tail_fused && l == p.L - 1;
         const int u = fused ? 2 * l + 1 : 2 * l;
+        if (!ok(u < 2 * p.L && p.pslots > 0, SITE_PARTIAL, u)) return;
         axpy_op(lp.o_n, S.obuf[l & 1], p.part + (size_t)(u % p.pslots) * p.n_cta * D, fused);
         arrive_partial(u);
     }
@@ -656,6 +687,7 @@ struct Streamer {
         dot_op(cp.lm_count, [&](int b0, int nb) {
             if (tid < nb) {
                 const int v = cp.lm_begin + b0 + tid;
+                if (!ok(v >= 0 && v < p.V, SITE_LOGIT, v)) return;
                 const float z = row_sum(tid) * inv_rms();
                 p.logits[v] = z;
                 if (better(z, v, bv, bi)) { bv = z; bi = v; }
@@ -757,6 +789,15 @@ struct Attention {
     }
 
     __device__ void fail(uint32_t code) { record_error(p, &S.abort_, code, cur_op); }
+    __device__ bool ok(bool cond, int site, long long index) {
+        return in_bounds(p, &S.abort_, cond, site, index, cur_op);
+    }
+    // a K or V tile of keys [j0, j0 + n) of heads g0 .. g0 + hc - 1
+    __device__ bool tile_ok(int lane_id, int g0, int j0, int n) {
+        return ok(lane_id < p.NL && g0 >= 0 && g0 + p.hc <= p.HKV_L && j0 >= 0 && n >= 0 && n <= p.kt &&
+                      j0 + n <= p.ctx && p.hc * p.kt * DH * 2 <= kAttnBuf / 2,
+                  SITE_KV_TILE, j0);
+    }
 
     __device__ void wait_geq(const uint32_t *ptr, uint32_t target) {
         if (at == 0 && !S.abort_) {
@@ -777,7 +818,7 @@ struct Attention {
     // this tile's P.V runs and its V while the next scores run.  Only thread 0
     // issues, at most one tile ahead of the waits.
     __device__ void issue_k(int l, int lane_id, int g0, int j0, int n) {
-        if (at == 0 && !S.abort_ && kiss == kwait) {
+        if (at == 0 && !S.abort_ && kiss == kwait && tile_ok(lane_id, g0, j0, n)) {
             const uint32_t bytes = (uint32_t)n * DH * 2;
             mbar_arrive_expect_tx(&S.abarK, (uint32_t)p.hc * bytes);
             for (int g = 0; g < p.hc; ++g) {
@@ -788,7 +829,7 @@ struct Attention {
         }
     }
     __device__ void issue_v(int l, int lane_id, int g0, int j0, int n) {
-        if (at == 0 && !S.abort_ && viss == vwait) {
+        if (at == 0 && !S.abort_ && viss == vwait && tile_ok(lane_id, g0, j0, n)) {
             const uint32_t bytes = (uint32_t)n * DH * 2;
             mbar_arrive_expect_tx(&S.abarV, (uint32_t)p.hc * bytes);
             for (int g = 0; g < p.hc; ++g) {
@@ -1022,7 +1063,8 @@ struct Attention {
             // scratch read back within this layer: kept in L2 ahead of the weight stream
             float *dst = p.apart + (((size_t)l * p.n_cta + cta) * p.HQ_L + (size_t)g0 * GL) * (DH + 2);
             const uint64_t keep = policy_evict_last();
-            {
+            const bool part_ok = ok(l < p.L && g0 * GL + NQ <= p.HQ_L && NQ <= kMaxChunkHeads, SITE_ATTN_PART, g0);
+            if (part_ok) {
                 const int dp = at % DP, grp = at / DP;
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
@@ -1033,7 +1075,7 @@ struct Attention {
                     }
                 }
             }
-            if (at < NQ) {
+            if (at < NQ && part_ok) {
                 st_hint(dst + at * (DH + 2) + DH, S.am[at], keep);
                 st_hint(dst + at * (DH + 2) + DH + 1, S.al[at], keep);
             }
@@ -1054,7 +1096,13 @@ struct Attention {
         const int S_ = cp.S;
         wait_geq(&p.barB[l * p.NL + cp.lane], p.epoch * (uint32_t)S_);
         float *ob = S.obuf[l & 1];
-        if (lp.o_n > 0) {
+        const bool rows_ok =
+            lp.o_n <= 0 ||
+            ok(lp.o_begin >= 0 && lp.o_begin + lp.o_n <= p.HQ_L * DH && lp.o_n <= kMaxORowsPerCta &&
+                   (lp.o_begin + lp.o_n - 1) / DH - lp.o_begin / DH < 4 && cp.cta0 + S_ <= p.n_cta &&
+                   S_ <= kMaxLaneCtas,
+               SITE_ATTN_PART, lp.o_begin);
+        if (lp.o_n > 0 && rows_ok) {
             const int a0 = lp.o_begin / DH, nh = (lp.o_begin + lp.o_n - 1) / DH - a0 + 1;
             const size_t stride = (size_t)p.HQ_L * (DH + 2);
             const float *base = p.apart + ((size_t)l * p.n_cta + cp.cta0) * stride;
@@ -1197,6 +1245,10 @@ __device__ void produce(const KParams &p, Smem<D, DH> &S, uint8_t *stages, uint6
             int stage;
             if (!claim(stage)) { stop = true; return; }
             const uint32_t bytes = (uint32_t)n * 2 * D;
+            if (!in_bounds(p, &S.abort_, w + bytes <= w_end, SITE_WEIGHT_TILE, (long long)it, -1)) {
+                stop = true;
+                return;
+            }
             const uint8_t *want = w + bytes + ahead;
             if (want > w_end) want = w_end;
             while (pf < want) {
@@ -1288,6 +1340,12 @@ __device__ void help(const KParams &p, Smem<D, DH> &S, uint64_t deadline) {
     for (int oi = 0; oi < p.n_ops && ok; ++oi) {
         const int op = __ldg(p.ops + oi);
         const int t = op_type(op), u = op_arg(op);
+        if ((t == OP_REDUCE || t == OP_LREDUCE) &&
+            !in_bounds(p, &S.abort_, u < 2 * p.L && p.pslots > 0 && p.n_cta <= kMaxCtas && cp.S <= kMaxCtas,
+                       SITE_PARTIAL, u, oi)) {
+            ok = false;
+            break;
+        }
         const float *slot = p.part + (size_t)(u % p.pslots) * p.n_cta * D;
         if (t == OP_LREDUCE) {
             // own-lane reading: this CTA's chunks c = k, k + S, ... of the

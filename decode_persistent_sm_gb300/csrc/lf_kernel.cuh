@@ -56,6 +56,14 @@ struct KParams {
     unsigned long long *trace;
 };
 
+// Status of a decode step from its error word's code (0 = none) and the
+// debug build's canary flag.
+inline lf_status status_of_error_word(uint32_t code, uint32_t canary) {
+    if (canary != 0 || (code & ~0xffu) == kErrBounds) return LF_ERR_BOUNDS;
+    if (code == 6u) return LF_ERR_INVALID_ARG;  // a chained step read a token outside [0, vocab)
+    return code ? LF_ERR_TIMEOUT : LF_OK;
+}
+
 // Dynamic shared memory needed by the kernel for (D, DH); 0 if unsupported.
 size_t decode_smem_bytes(int D, int DH);
 // One decode step; grid = n_cta CTAs (one per SM), cooperative launch.

@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstdint>
 #include <mutex>
 
 #include "laneformer.h"
@@ -46,6 +47,45 @@ cudaError_t scratch_address(int dev, unsigned char **out) {
 }
 
 size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+
+// cuMemGetAddressRange, taken from the driver through the runtime (no link
+// against libcuda).  Looked up once; null if the driver does not offer it.
+typedef int (*AddressRangeFn)(unsigned long long *base, size_t *size, unsigned long long dptr);
+AddressRangeFn address_range_fn() {
+    static AddressRangeFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<AddressRangeFn>(p);
+    }();
+    return fn;
+}
+
+// True when the kernel may write `bytes` at `p`: 4-byte aligned, and either
+// device memory of the engine's device whose allocation holds all `bytes`,
+// or managed / mapped host memory with a device address.  A host pointer
+// that the GPU cannot reach, a pointer on another device, or a buffer too
+// short is refused here rather than faulting on the device.
+bool writable_output(const lf_engine *e, const void *p, size_t bytes) {
+    if (!p || (reinterpret_cast<uintptr_t>(p) & 3u)) return false;
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    if (a.type == cudaMemoryTypeManaged || a.type == cudaMemoryTypeHost) return a.devicePointer != nullptr;
+    if (a.type != cudaMemoryTypeDevice || a.device != e->device) return false;
+    AddressRangeFn range = address_range_fn();
+    if (!range) return false;
+    unsigned long long base = 0;
+    size_t size = 0;
+    const unsigned long long at = reinterpret_cast<uintptr_t>(p);
+    if (range(&base, &size, at) != 0) return false;
+    return at >= base && at - base + bytes <= size;
+}
 
 struct Carve {
     size_t part, R, qkv, apart, cand_v, cand_i, ctr, total;
@@ -88,6 +128,9 @@ extern "C" lf_status lf_decode_step_static_scratch(lf_engine *e, int32_t token,
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return LF_ERR_CUDA;
     if (dev != e->device || dev < 0 || dev >= kMaxDevices) return LF_ERR_INVALID_ARG;
+    if (!writable_output(e, logits_device, (size_t)s.V * sizeof(float)) ||
+        !writable_output(e, argmax_device, sizeof(int32_t)))
+        return LF_ERR_INVALID_ARG;
     unsigned char *base = nullptr;
     if (scratch_address(dev, &base) != cudaSuccess) return LF_ERR_CUDA;
 
@@ -153,8 +196,8 @@ extern "C" lf_status lf_decode_step_static_scratch(lf_engine *e, int32_t token,
         return LF_ERR_CUDA;
     }
     if (werr[0] != 0) {
-        e->poisoned = LF_ERR_TIMEOUT;
-        return LF_ERR_TIMEOUT;
+        e->poisoned = lf::status_of_error_word(werr[0], 0);
+        return e->poisoned;
     }
     return LF_OK;
 }

@@ -31,11 +31,58 @@ template <class T>
 cudaError_t dalloc(lf_engine *e, T **p, size_t count) {
     size_t bytes = std::max<size_t>(count * sizeof(T), 16);
     void *q = nullptr;
+    if constexpr (lf::kDebugChecks) {  // canary regions before and after the buffer
+        const size_t body = (bytes + lf::kGuardBytes - 1) / lf::kGuardBytes * lf::kGuardBytes;
+        cudaError_t err = cudaMalloc(&q, body + 2 * lf::kGuardBytes);
+        if (err != cudaSuccess) return err;
+        e->allocs.push_back(q);
+        unsigned char *b = static_cast<unsigned char *>(q);
+        err = cudaMemset(b, lf::kGuardByte, lf::kGuardBytes);
+        if (err == cudaSuccess) err = cudaMemset(b + lf::kGuardBytes + body, lf::kGuardByte, lf::kGuardBytes);
+        if (err != cudaSuccess) return err;
+        e->guards.push_back({b, b + lf::kGuardBytes + body});
+        e->dev_bytes += body + 2 * lf::kGuardBytes;
+        *p = reinterpret_cast<T *>(b + lf::kGuardBytes);
+        return cudaSuccess;
+    }
     cudaError_t err = cudaMalloc(&q, bytes);
     if (err != cudaSuccess) return err;
     e->allocs.push_back(q);
     e->dev_bytes += bytes;
     *p = static_cast<T *>(q);
+    return cudaSuccess;
+}
+
+// Debug build: flag |= 1 when a word of a canary region differs from the
+// pattern (one block per guarded buffer of this batch of at most 64).
+constexpr int kGuardBatch = 64;
+struct GuardBatch {
+    const uint32_t *front[kGuardBatch];
+    const uint32_t *back[kGuardBatch];
+    int n;
+};
+__global__ void check_guards(const __grid_constant__ GuardBatch g, uint32_t *flag) {
+    const uint32_t want = 0x01010101u * lf::kGuardByte;
+    if (blockIdx.x >= (unsigned)g.n) return;
+    for (int w = threadIdx.x; w < lf::kGuardBytes / 4; w += blockDim.x)
+        if (g.front[blockIdx.x][w] != want || g.back[blockIdx.x][w] != want) atomicOr(flag, 1u);
+}
+
+// Enqueues the canary check of every guarded buffer; the result lands in
+// status word 3.  Nothing in the release build.
+cudaError_t enqueue_guard_check(lf_engine *e) {
+    if constexpr (!lf::kDebugChecks) return cudaSuccess;
+    for (size_t i0 = 0; i0 < e->guards.size(); i0 += kGuardBatch) {
+        GuardBatch g{};
+        g.n = (int)std::min<size_t>(kGuardBatch, e->guards.size() - i0);
+        for (int i = 0; i < g.n; ++i) {
+            g.front[i] = reinterpret_cast<const uint32_t *>(e->guards[i0 + i].front);
+            g.back[i] = reinterpret_cast<const uint32_t *>(e->guards[i0 + i].back);
+        }
+        check_guards<<<g.n, 64, 0, e->stream>>>(g, e->status + 3);
+        cudaError_t err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+    }
     return cudaSuccess;
 }
 
@@ -98,6 +145,7 @@ const char *lf_status_string(lf_status s) {
         case LF_ERR_CTX_OVERFLOW: return "context capacity reached";
         case LF_ERR_TIMEOUT: return "device wait timed out";
         case LF_ERR_UNSUPPORTED: return "unsupported configuration";
+        case LF_ERR_BOUNDS: return "debug check failed (device bounds check or buffer canary)";
     }
     return "unknown status";
 }
@@ -377,16 +425,16 @@ lf_status lf_load_kv(lf_engine *e, const void *host_kv, size_t nbytes, int n_pos
 }
 
 static lf_status read_status(lf_engine *e, float *logits, int32_t *argmax) {
-    cudaError_t err = cudaMemcpyAsync(e->h_status, e->status, 8 * sizeof(uint32_t),
-                                      cudaMemcpyDeviceToHost, e->stream);
+    cudaError_t err = enqueue_guard_check(e);
+    if (err == cudaSuccess)
+        err = cudaMemcpyAsync(e->h_status, e->status, 8 * sizeof(uint32_t), cudaMemcpyDeviceToHost, e->stream);
     if (err == cudaSuccess && logits)
         err = cudaMemcpyAsync(logits, e->logits, (size_t)e->plan.sh.V * sizeof(float),
                               cudaMemcpyDeviceToHost, e->stream);
     if (err == cudaSuccess) err = cudaStreamSynchronize(e->stream);
     if (err != cudaSuccess) return cuda_fail(e, err);
-    if (e->h_status[4] != 0) {
-        // code 6: a chained step read a token outside [0, vocab) on the device
-        e->poisoned = e->h_status[4] == 6u ? LF_ERR_INVALID_ARG : LF_ERR_TIMEOUT;
+    if (e->h_status[4] != 0 || e->h_status[3] != 0) {
+        e->poisoned = lf::status_of_error_word(e->h_status[4], e->h_status[3]);
         return e->poisoned;
     }
     if (argmax) *argmax = (int32_t)e->h_status[0];
@@ -672,6 +720,30 @@ lf_status lf_debug_read_trace(lf_engine *e, uint64_t *out, size_t n_words, int32
     if (err != cudaSuccess) return cuda_fail(e, err);
     if (ops) std::memcpy(ops, e->plan.ops.data(), e->plan.ops.size() * sizeof(int32_t));
     return LF_OK;
+}
+
+lf_status lf_debug_canaries(lf_engine *e, int *n_guarded) {
+    if (!e) return LF_ERR_INVALID_ARG;
+    if constexpr (!lf::kDebugChecks) {
+        return LF_ERR_UNSUPPORTED;
+    } else {
+        if (n_guarded) *n_guarded = (int)e->guards.size();
+        if (e->poisoned != LF_OK) return e->poisoned;
+        return read_status(e, nullptr, nullptr);
+    }
+}
+
+lf_status lf_debug_corrupt_canary(lf_engine *e, int i, int back) {
+    if (!e) return LF_ERR_INVALID_ARG;
+    if constexpr (!lf::kDebugChecks) {
+        return LF_ERR_UNSUPPORTED;
+    } else {
+        if (i < 0 || i >= (int)e->guards.size()) return LF_ERR_INVALID_ARG;
+        const uint32_t word = 0x12345678u;
+        unsigned char *at = back ? e->guards[i].back + 8 : e->guards[i].front + lf::kGuardBytes - 4;
+        cudaError_t err = cudaMemcpy(at, &word, sizeof(word), cudaMemcpyHostToDevice);
+        return err == cudaSuccess ? LF_OK : cuda_fail(e, err);
+    }
 }
 
 lf_status lf_engine_info(const lf_engine *e, int64_t info[8]) {

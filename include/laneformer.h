@@ -13,9 +13,9 @@
  *  - Plain C types only; pointers are HOST pointers unless a name says
  *    "device".  The engine owns all device memory it allocates; the caller
  *    keeps ownership of every buffer it passes.
- *  - Every call returns an lf_status.  After LF_ERR_CUDA or LF_ERR_TIMEOUT
- *    (or a bad token found on the device by a chained step, reported as
- *    LF_ERR_INVALID_ARG) the engine is poisoned: every call but lf_reset and
+ *  - Every call returns an lf_status.  After LF_ERR_CUDA, LF_ERR_TIMEOUT or
+ *    LF_ERR_BOUNDS (or a bad token found on the device by a chained step,
+ *    reported as LF_ERR_INVALID_ARG) the engine is poisoned: every call but lf_reset and
  *    lf_destroy returns that status again until lf_reset succeeds.
  *  - Calls run on the engine stream (default: the legacy stream, or the one
  *    given to lf_set_stream) and are synchronous unless stated otherwise.
@@ -41,7 +41,9 @@ typedef enum {
     LF_ERR_NOT_LOADED = 4,    /* decode or prefill before lf_load_weights */
     LF_ERR_CTX_OVERFLOW = 5,  /* the position would reach ctx_cap */
     LF_ERR_TIMEOUT = 6,       /* a bounded device-side wait ran out */
-    LF_ERR_UNSUPPORTED = 7    /* a valid config this build has no kernel for */
+    LF_ERR_UNSUPPORTED = 7,   /* a valid config this build has no kernel for */
+    LF_ERR_BOUNDS = 8         /* debug build only: a device-side bounds check or a
+                                 canary around an engine buffer failed */
 } lf_status;
 
 /*
@@ -183,8 +185,11 @@ const char *lf_status_string(lf_status s);
  * every later call; NULL selects the legacy default stream. */
 lf_status lf_set_stream(lf_engine *e, void *cuda_stream);
 
-/* Device pointers to the last step's logits (vocab fp32) and argmax (int32);
- * valid until lf_destroy. */
+/* Device pointers to the logits (vocab fp32) and argmax (int32) of the last
+ * step run through the engine's own buffers (lf_decode_step, lf_prefill,
+ * lf_prefill_batched, the generation calls); valid until lf_destroy.  A
+ * lf_decode_step_static_scratch step writes only the caller's buffers and
+ * leaves these as they were. */
 lf_status lf_get_logits_device(lf_engine *e, const float **dptr);
 lf_status lf_get_argmax_device(lf_engine *e, const int32_t **dptr);
 
@@ -248,6 +253,12 @@ lf_status lf_debug_read_trace(lf_engine *e, uint64_t *out, size_t n_words, int32
  * cudaMalloc, cudaFree or other allocating call.
  *   logits_device: DEVICE array of vocab floats, written by the step.
  *   argmax_device: DEVICE int32, written by the step.
+ * Both must be 4-byte aligned and reachable from the engine's device: device
+ * memory of that device (for logits, an allocation with room for vocab
+ * floats from the pointer on) or managed / mapped host memory; anything else
+ * (a plain host pointer, memory of another device) is LF_ERR_INVALID_ARG.
+ * The results go only to these buffers: lf_get_logits_device and
+ * lf_get_argmax_device keep pointing at the last lf_decode_step's results.
  * The engine's device must be the current device.  The first call on a
  * device looks up the array's device address (once per device); make that
  * first call before any stream capture.  Every call uses the same array and
@@ -258,7 +269,8 @@ lf_status lf_debug_read_trace(lf_engine *e, uint64_t *out, size_t n_words, int32
  * device-side timeout.  Returns LF_ERR_UNSUPPORTED when the engine's working
  * set does not fit the array (the full 2.3B lane model needs about 26 MB on
  * 152 SMs) or the config asks for the own-lane-immediate reading,
- * LF_ERR_INVALID_ARG for null outputs or another current device,
+ * LF_ERR_INVALID_ARG for outputs that fail the checks above or another
+ * current device,
  * and the same statuses as lf_decode_step otherwise.
  */
 #define LF_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
@@ -361,6 +373,43 @@ lf_status lf_batch_generate(lf_engine *e, const int32_t *first_tokens, int n_ste
  * for bad sizes or pointers; LF_ERR_TIMEOUT if a device-side wait ran out. */
 lf_status lf_gemv_f16(const void *w_device, const void *x_device, float *y_device, int n, int k, int batch,
                       void *cuda_stream);
+
+/*
+ * Debug build.  liblaneformer_debug.so is the same library compiled with
+ * LF_DEBUG: before every weight-tile, KV, q/k/v, partial, lane-sum,
+ * attention-partial and logit access the decode kernel checks the index
+ * against its buffer; a failed check skips the access, records the site
+ * and the index in the step's error word and the step returns
+ * LF_ERR_BOUNDS (no trap, the context stays usable).  Every buffer the
+ * engine allocates at create and load time sits between two 256-byte canary
+ * regions, which the host checks after every step that reports a status
+ * (lf_decode_step with outputs, lf_synchronize, lf_prefill, the generation
+ * calls): an overwritten canary poisons the engine with LF_ERR_BOUNDS.
+ *
+ * lf_debug_canaries checks every canary now (synchronously) and writes the
+ * number of guarded buffers to *n_guarded (nullable): LF_OK, or
+ * LF_ERR_BOUNDS for an overwritten canary.  lf_debug_corrupt_canary writes
+ * one word into the front (back = 0) or back canary of guarded buffer i,
+ * from the host, so that a test can see the check fire.  Both return
+ * LF_ERR_UNSUPPORTED in the release library.
+ */
+lf_status lf_debug_canaries(lf_engine *e, int *n_guarded);
+lf_status lf_debug_corrupt_canary(lf_engine *e, int i, int back);
+
+/* Measurement call, not a step of the decode: one read of `bytes` of device
+ * memory at `src_device` in the decode kernel's weight-copy pattern (one CTA
+ * per SM, each reading one contiguous range with 32 KB bulk copies into a
+ * ring of four shared-memory stages, evict-first), with no arithmetic on the
+ * data.  Its duration is the read-only ceiling of the decode step's weight
+ * stream (the step is bound by reading its weights once: Blog, "Designing
+ * the architecture").  `bytes` a multiple of 32768, src_device 16-byte
+ * aligned; sink_device receives one checksum float per SM (sink_len >= the
+ * SM count); *status_device (4-byte aligned device word, left as it is on
+ * success) is set to 1 if a device-side wait ran out.  Asynchronous on
+ * `cuda_stream` (NULL = legacy stream); returns LF_ERR_INVALID_ARG for bad
+ * arguments, LF_ERR_CUDA if the launch failed. */
+lf_status lf_stream_read(const void *src_device, size_t bytes, float *sink_device, int sink_len,
+                         uint32_t *status_device, void *cuda_stream);
 
 /* Host-only plan statistics for `n_sm` SMs (no GPU needed): stats[0] = weight
  * rows in the stream, [1] = min rows per SM, [2] = max rows per SM, [3] = ops

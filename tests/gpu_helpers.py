@@ -1,4 +1,14 @@
-"""Shared pieces of the GPU parity tests: tolerances and teacher forcing."""
+"""Shared pieces of the GPU parity tests: tolerances, teacher forcing and a
+record of the observed error magnitudes.
+
+Every comparison of GPU logits with the oracle's goes through `note`, which
+keeps, per test, the worst logits rel-L2, the largest absolute logit error,
+the argmax agreement and the top-2 margins of the oracle's logits.  The
+session summary (tests/conftest.py) prints them, and writes them as JSON to
+the file named by the LF_PARITY_JSON environment variable when it is set.
+"""
+import os
+
 import numpy as np
 
 import oracle
@@ -7,6 +17,9 @@ import oracle
 # teacher forcing (the GPU is fed the same tokens as the oracle).
 REL_L2 = 1e-2
 ARGMAX_MIN = 0.99
+
+# per test id: lists of (rel-L2, max abs error, top-2 margin, argmax agrees)
+RECORDS = {}
 
 
 def rel_l2(got, ref) -> float:
@@ -20,13 +33,48 @@ def top2_margin(ref) -> float:
     return float(s[-1] - s[-2])
 
 
+def _test_id() -> str:
+    return os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+
+
+def note(got, ref, am=None):
+    """Records one GPU-vs-oracle comparison of a logits vector (and of the
+    GPU's argmax when given); returns its rel-L2."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    r = rel_l2(got, ref)
+    ok = None if am is None else bool(int(am) == oracle.argmax(ref))
+    RECORDS.setdefault(_test_id(), []).append((r, float(np.max(np.abs(got - ref))), top2_margin(ref), ok))
+    return r
+
+
+def summarise(rows):
+    """Worst rel-L2, max abs error, agreement, and the agreement over steps
+    whose oracle top-2 margin exceeds 4x the largest absolute error seen in
+    the test (with the number of steps that filter excludes)."""
+    rels = np.array([r[0] for r in rows])
+    absd = np.array([r[1] for r in rows])
+    marg = np.array([r[2] for r in rows])
+    flags = [r[3] for r in rows if r[3] is not None]
+    out = {"n": len(rows), "worst_rel_l2": float(rels.max()), "median_rel_l2": float(np.median(rels)),
+           "max_abs_err": float(absd.max())}
+    if flags:
+        agree = np.array([r[3] for r in rows if r[3] is not None], dtype=bool)
+        m = np.array([r[2] for r in rows if r[3] is not None])
+        clear = m > 4.0 * absd.max()
+        out.update({"argmax_n": int(agree.size), "agree": float(agree.mean()),
+                    "agree_clear_margin": float(agree[clear].mean()) if clear.any() else None,
+                    "excluded_near_ties": int((~clear).sum())})
+    return out
+
+
 def teacher_forced(engine, orc, tokens):
     """Feeds `tokens` to both; returns (rel errors, argmax agree flags, margins, max abs err)."""
     rels, agree, margins, abserr = [], [], [], []
     for t in tokens:
         ref = orc.step(int(t))
         got, am = engine.decode_step(int(t))
-        rels.append(rel_l2(got, ref))
+        rels.append(note(got, ref, am))
         agree.append(am == oracle.argmax(ref))
         margins.append(top2_margin(ref))
         abserr.append(float(np.max(np.abs(got - ref))))

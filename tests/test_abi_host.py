@@ -42,10 +42,25 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(names) == set(binding._SIGS), "binding must wrap exactly the declared calls"
 
 
+def test_debug_library_exports_the_same_symbols():
+    from decode_persistent_sm_gb300 import binding, build
+    build.build(debug=True)
+    dbg = binding.load_library(debug=True)
+    names = declared_functions()
+    assert not [n for n in names if not hasattr(dbg, n)]
+
+
+def test_debug_calls_are_refused_by_the_release_library(lib):
+    # (no engine needed: a null engine is refused first, then the build kind)
+    assert lib.lf_debug_canaries(None, None) == 1
+    assert lib.lf_debug_corrupt_canary(None, 0, 0) == 1
+
+
 def test_status_strings(lib):
-    for code in range(8):
+    for code in range(9):
         assert lib.lf_status_string(code)
     assert lib.lf_status_string(0) == b"ok"
+    assert b"debug" in lib.lf_status_string(8)
 
 
 def cfg(shape, **kw):

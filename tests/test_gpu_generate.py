@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 import synth
-from gpu_helpers import REL_L2, rel_l2
+from gpu_helpers import REL_L2, note, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -138,5 +138,5 @@ def test_out_of_vocabulary_device_token_poisons_until_reset():
         for t in tokens:
             got, am = eng.decode_step(int(t))
             ref = orc.step(int(t))
-            assert rel_l2(got, ref) <= REL_L2
+            assert note(got, ref, am) <= REL_L2
             assert am == oracle.argmax(ref)

@@ -8,7 +8,7 @@ import pytest
 
 import oracle
 import synth
-from gpu_helpers import REL_L2, assert_gates, rel_l2, teacher_forced
+from gpu_helpers import REL_L2, assert_gates, note, rel_l2, teacher_forced
 
 pytestmark = pytest.mark.gpu
 
@@ -30,7 +30,7 @@ def run(shape, seed, n, kv_fill=0):
         for t in tokens:
             got, am = eng.decode_step(int(t))
             rb, ra = orc_b.step(int(t)), orc_a.step(int(t))
-            rels.append(rel_l2(got, rb))
+            rels.append(note(got, rb, am))
             agree.append(am == oracle.argmax(rb))
             gaps.append(rel_l2(ra, rb))
     return np.array(rels), np.array(agree), np.array(gaps)

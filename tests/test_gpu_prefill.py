@@ -12,7 +12,7 @@ import pytest
 
 import oracle
 import synth
-from gpu_helpers import REL_L2, assert_gates, rel_l2, teacher_forced
+from gpu_helpers import REL_L2, assert_gates, note, rel_l2, teacher_forced
 
 pytestmark = pytest.mark.gpu
 
@@ -29,13 +29,13 @@ def prefill_then_steps(shape, seed, n_prompt, n_steps, gain_std=0.1, lead=0):
         for t in tokens[:lead]:
             got, am = eng.decode_step(int(t))
             ref = orc.step(int(t))
-            assert rel_l2(got, ref) <= REL_L2
+            assert note(got, ref, am) <= REL_L2
         prompt = tokens[lead:lead + n_prompt]
         got, am = eng.prefill_batched(prompt)
         for t in prompt:
             ref = orc.step(int(t))
         assert eng.position == lead + n_prompt
-        pre_rel, pre_agree = rel_l2(got, ref), am == oracle.argmax(ref)
+        pre_rel, pre_agree = note(got, ref, am), am == oracle.argmax(ref)
         rels, agree, _, _ = teacher_forced(eng, orc, tokens[lead + n_prompt:])
         return eng, orc, pre_rel, pre_agree, rels, agree
 
