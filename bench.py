@@ -379,6 +379,8 @@ def run_ours(args, world, rank, local):
     eng.set_stream(stream.cuda_stream)
     eng.load_weights(blob)
     eng.load_kv(kv, POS)
+    if args.idle_prefetch_kb >= 0:
+        eng.set_idle_prefetch(args.idle_prefetch_kb * 1024, args.idle_after_ns)
     if args.l2_prefetch_kb >= 0 or args.lm_prefetch_kb >= 0:
         eng.set_l2_prefetch(max(args.l2_prefetch_kb, 0) * 1024 if args.l2_prefetch_kb >= 0 else 128 * 1024,
                             args.lm_prefetch_kb * 1024 if args.lm_prefetch_kb >= 0 else 128 * 1024)
@@ -502,6 +504,23 @@ def timed_generation(eng, stream, first_token: int, n: int):
     return buf[1:].cpu().numpy(), per, evs[0].elapsed_time(evs[n])
 
 
+def timed_generate_fused(eng, stream, first_token: int, n: int):
+    """lf_generate (all n steps in one launch of the persistent kernel) timed
+    with CUDA events around the call; per-step latencies from the steps'
+    completion stamps.  Returns (tokens, per-step ms, total ms)."""
+    import torch
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    toks, _ = eng.generate(int(first_token), n)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    stamps = eng.generate_stamps(n).astype(np.int64)
+    per = list(np.diff(stamps) / 1e6)
+    return toks, per, e0.elapsed_time(e1)
+
+
 def latency_summary(per_ms):
     a = np.sort(np.asarray(per_ms))
     return {"p50_ms": float(np.percentile(a, 50)), "p99_ms": float(np.percentile(a, 99)),
@@ -536,6 +555,8 @@ def run_generation(args, world, rank, local):
         return max_over_ranks(x, world)
 
     base = synth.FULL
+    if args.layers:  # a smaller model of the same width, for profiler captures only
+        base = base.replace(n_layers=args.layers, swa_window=base.swa_window[:args.layers])
     blob = synth.make_weights(base, SEED)
     stream = torch.cuda.current_stream()
     data = "synthetic (seeded N(0,0.02) FP16 weights, uniform random token ids)"
@@ -602,6 +623,8 @@ def run_generation(args, world, rank, local):
                             "h2d_bytes_per_step": PREFILL_N * 4, "d2h_bytes_per_step": shape.vocab * 4 + 4,
                             "call": "lf_prefill_batched with host token ids and host logits"},
                     "gpu_launches": None, "clocks": clk, **common}
+            if args.layers:
+                line["config"] = {"workload": f"profiling case: {args.layers} layers of the full width"}
             print(json.dumps(line), flush=True)
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -815,9 +838,9 @@ def run_generation(args, world, rank, local):
                 eng.set_position(SWEEP_CTX)
                 if world > 1:
                     torch.distributed.barrier()
-                _, per, total = timed_generation(eng, stream, first, SWEEP_STEPS)
+                _, per, total = timed_generate_fused(eng, stream, first, SWEEP_STEPS)
                 total = worst(total)
-                launches += SWEEP_STEPS
+                launches += 1
             variants[f"delay{delay}_lanes{lanes}" + ("_own" if own else "")] = {
                 "value": world * SWEEP_STEPS / (total / 1e3), "ms_per_step": total / SWEEP_STEPS,
                 **latency_summary(per)}
@@ -828,7 +851,7 @@ def run_generation(args, world, rank, local):
                     "steps": SWEEP_STEPS, "warmup": max(args.warmup, 3), "ms_per_step": main_v["ms_per_step"],
                     "data": data + ", N(0,1) KV fill",
                     "config": {"workload": f"sweep: KV pre-filled N(0,1) to {SWEEP_CTX}, then {SWEEP_STEPS} greedy "
-                                           "tokens chained on the device for delay in {0,1,2} x lanes in {1,8}, "
+                                           "tokens in one lf_generate launch for delay in {0,1,2} x lanes in {1,8}, "
                                            "both readings of the delayed sum for delay > 0 (_own: each lane "
                                            "adds its own partial at once); value = delay 2, 8 lanes", "seed": SEED,
                                "l2": "no flush: inputs larger than L2"},
@@ -860,9 +883,14 @@ def run_generation(args, world, rank, local):
     clocks.start()
     if world > 1:
         torch.distributed.barrier()
-    gen, per, total = timed_generation(eng, stream, int(prompt[-1]), n_gen)
+    gen, per, total = timed_generate_fused(eng, stream, int(prompt[-1]), n_gen)
     clk = clocks.stop()
     total = worst(total)
+    # the same steps as separate launches (one per token, chained on the device)
+    eng.reset()
+    eng.prefill_batched(prompt[:-1], logits=False)
+    gen_sep, per_sep, total_sep = timed_generation(eng, stream, int(prompt[-1]), n_gen)
+    total_sep = worst(total_sep)
     # end to end through lf_generate: tokens back in host memory
     eng.reset()
     eng.prefill_batched(prompt[:-1], logits=False)
@@ -889,12 +917,17 @@ def run_generation(args, world, rank, local):
                 "latency": latency_summary(per),
                 "prefill_ms": prefill_ms, "prefill": f"{n_prompt - 1} positions, lf_prefill_batched, host-timed",
                 "prefill_ms_decode_loop": loop_prefill_ms,
+                "timing": "lf_generate: all steps in one launch of the persistent kernel, CUDA events "
+                          "around the call; latency from the steps' completion stamps",
+                "separate_launches": {"value": world * n_gen / (total_sep / 1e3), "ms_per_step": total_sep / n_gen,
+                                      **latency_summary(per_sep),
+                                      "tokens_match": bool(np.array_equal(gen, gen_sep))},
                 "chain_matches_lf_generate": bool(np.array_equal(gen, gen2)),
                 "roofline": gen_roofline(shape, pos0, n_gen, ms), "cpu_baseline": cpu,
                 "e2e": {"value": world * n_gen / e2e_s, "unit": UNIT, "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 4 + 32 / n_gen,
                         "call": "lf_generate (first token by value, tokens and status copied back once)"},
-                "gpu_launches": n_gen, "clocks": clk, **common}
+                "gpu_launches": 1, "clocks": clk, **common}
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -923,6 +956,10 @@ def main():
                          "generation workloads")
     ap.add_argument("--batch", type=int, default=0,
                     help="--workload batch: one batch size instead of the sweep (steps = min(--steps, 64))")
+    ap.add_argument("--idle-prefetch-kb", type=int, default=-1,
+                    help="step workload: L2 lead (KiB per SM) the copy warp builds while it waits for a stage")
+    ap.add_argument("--idle-after-ns", type=int, default=4000,
+                    help="step workload: wait before the idle prefetch starts")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: same width with fewer layers (not a bench number)")
     args = ap.parse_args()

@@ -31,6 +31,7 @@ _SIGS = {
     "lf_prefill_batched": (_ci, [_vp, _vp, _ci, _vp, _vp]),
     "lf_set_prefill_attention": (_ci, [_vp, _ci]),
     "lf_generate": (_ci, [_vp, _i32, _ci, _vp, _vp]),
+    "lf_generate_stamps": (_ci, [_vp, _vp, _ci]),
     "lf_generate_sampled": (_ci, [_vp, _i32, _ci, ctypes.c_float, ctypes.c_float, ctypes.c_uint64, ctypes.c_uint32,
                                   _vp, _vp]),
     "lf_sample": (_ci, [_vp, _ci, ctypes.c_float, ctypes.c_float, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
@@ -53,6 +54,7 @@ _SIGS = {
     "lf_decode_step_static_scratch": (_ci, [_vp, _i32, _vp, _vp]),
     "lf_debug_trace": (_ci, [_vp, _ci]),
     "lf_set_l2_prefetch": (_ci, [_vp, ctypes.c_uint32, ctypes.c_uint32]),
+    "lf_set_idle_prefetch": (_ci, [_vp, ctypes.c_uint32, ctypes.c_uint32]),
     "lf_debug_read_trace": (_ci, [_vp, _vp, ctypes.c_size_t, _vp]),
     "lf_batch_begin": (_ci, [_vp, _ci]),
     "lf_batch_end": (_ci, [_vp]),
@@ -237,6 +239,12 @@ class Engine:
         _check("lf_generate", rc)
         return toks, out
 
+    def generate_stamps(self, n: int) -> np.ndarray:
+        """Per-step completion times (ns, device timer) of the last generate()."""
+        out = np.zeros(int(n), dtype=np.uint64)
+        _check("lf_generate_stamps", self._lib.lf_generate_stamps(self._h, out.ctypes.data, int(n)))
+        return out
+
     def generate_sampled(self, first_token: int, n: int, temperature: float, top_p: float, seed: int,
                          sample: int = 0, logits: bool = False):
         """lf_generate_sampled: n steps, each token drawn from the step's logits
@@ -353,6 +361,9 @@ class Engine:
     def set_l2_prefetch(self, bytes_per_sm: int, lm_bytes_per_sm: int = 128 * 1024):
         _check("lf_set_l2_prefetch",
                self._lib.lf_set_l2_prefetch(self._h, int(bytes_per_sm), int(lm_bytes_per_sm)))
+
+    def set_idle_prefetch(self, bytes_per_sm: int, after_ns: int = 4000):
+        _check("lf_set_idle_prefetch", self._lib.lf_set_idle_prefetch(self._h, int(bytes_per_sm), int(after_ns)))
 
     def debug_skip_arrival(self, cta: int):
         _check("lf_debug_skip_arrival", self._lib.lf_debug_skip_arrival(self._h, int(cta)))

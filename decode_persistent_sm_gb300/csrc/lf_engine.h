@@ -29,6 +29,8 @@ struct lf_engine {
     uint32_t *ctr = nullptr;     // barA | barB | cnt | ready | fin
     uint32_t *status = nullptr;  // [0] argmax, [4..7] error word
     int32_t *gen = nullptr;      // lf_generate: argmax of each step, [ctx_cap]
+    unsigned long long *stamps = nullptr;  // lf_generate: completion time of each step (ns), [ctx_cap]
+    int gen_n = 0;               // steps of the last lf_generate
     __half *blob = nullptr;      // FP16 weights in file layout: GEMM operands of lf_prefill_batched
     void *pf_mem = nullptr;      // lf_prefill_batched scratch (grow-only, owned separately)
     size_t pf_bytes = 0;
@@ -51,6 +53,8 @@ struct lf_engine {
     int skip_cta = -1;
     unsigned l2_prefetch_bytes = 128u * 1024u;
     unsigned lm_prefetch_bytes = 128u * 1024u;
+    unsigned idle_prefetch_bytes = 768u * 1024u;
+    unsigned idle_after_ns = 4000;
     size_t dev_bytes = 0;
     long long launches = 0;
     std::vector<void *> allocs;

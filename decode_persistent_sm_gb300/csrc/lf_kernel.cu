@@ -88,6 +88,8 @@ struct Smem {
     volatile int abort_;
     volatile int prod_done;
     volatile int issued;
+    volatile int stop_s, stop_a;  // abort flag as the streaming / attention warps saw it after a token
+    volatile int atok;            // attention warps: token of this launch they work on
 };
 
 template <int D, int DH>
@@ -155,10 +157,11 @@ struct Streamer {
     uint32_t it;
     int npar;          // RMSNorm slot in S.nred of the last NORM
     int pre_u, pre_g;  // lane sum prefetched into rpre / gains prefetched into S.gsm
+    int tk;            // token of this launch
     float x[C::NX], h[C::NX], rpre[C::NX];
 
     __device__ Streamer(const KParams &p_, Smem<D, DH> &S_, uint8_t *st, uint64_t dl)
-        : p(p_), S(S_), stages(st), deadline(dl), it(0), npar(0), pre_u(-1), pre_g(-1) {
+        : p(p_), S(S_), stages(st), deadline(dl), it(0), npar(0), pre_u(-1), pre_g(-1), tk(0) {
         tid = threadIdx.x;
         warp = tid >> 5;
         lane = tid & 31;
@@ -166,6 +169,9 @@ struct Streamer {
     }
 
     __device__ CtaPlan plan() const { return p.cta[cta]; }
+    // epoch (counter targets) and position of the current token
+    __device__ uint32_t ep() const { return p.epoch + (uint32_t)tk; }
+    __device__ int pos() const { return p.pos + tk; }
     __device__ int col(int i) const { return C::kBlockRow ? 8 * (tid + kConsThreads * i) : 8 * lane; }
     // Lane-sum partials are chunk-major, [chunk][cta][32 floats], so that the
     // pieces one chunk's summing warp needs are contiguous.
@@ -238,12 +244,15 @@ struct Streamer {
     // ------------------------------------------------------------- residual
     __device__ void embed() {
         int tok = p.token;
-        if (p.token_src) {  // written by an earlier launch on the same stream
+        if (tk > 0) {  // the previous token of this launch: its argmax, once published
+            wait_geq(p.tok_ready, ep() - 1u);
+            tok = __ldcg(p.argmax + tk - 1);
+        } else if (p.token_src) {  // written by an earlier launch on the same stream
             tok = __ldcg(p.token_src);
-            if (tok < 0 || tok >= p.V) {
-                if (tid == 0) fail(6u);
-                tok = 0;
-            }
+        }
+        if ((tk > 0 || p.token_src) && (tok < 0 || tok >= p.V)) {
+            if (tid == 0) fail(6u);
+            tok = 0;
         }
         const __half *e = p.emb + (size_t)tok * D;
 #pragma unroll
@@ -285,7 +294,7 @@ struct Streamer {
     // sub-block just produced (warp-local, like add).
     __device__ void ladd(int u) {
         const int lam = plan().lane;
-        const uint32_t target = p.epoch * (uint32_t)plan().S;
+        const uint32_t target = ep() * (uint32_t)plan().S;
         if (lane == 0 && !S.abort_) {
             const uint64_t t0 = (p.trace && tid == 0) ? global_timer_ns() : 0;
             while (true) {
@@ -315,7 +324,7 @@ struct Streamer {
             if (p.own_lane) sub_own(u);
             return;
         }
-        const uint32_t target = p.epoch * (uint32_t)p.nch;
+        const uint32_t target = ep() * (uint32_t)p.nch;
         if (lane == 0 && !S.abort_) {
             const uint64_t t0 = (p.trace && tid == 0) ? global_timer_ns() : 0;
             while (true) {
@@ -338,7 +347,7 @@ struct Streamer {
         const int u = op_next_add(op);
         if (u < 0 || u == pre_u) return;
         const uint32_t v = ld_acquire(&p.ready[u]);
-        if (!__all_sync(0xffffffffu, (int)(v - p.epoch * (uint32_t)p.nch) >= 0)) return;
+        if (!__all_sync(0xffffffffu, (int)(v - ep() * (uint32_t)p.nch) >= 0)) return;
         load_r(u, rpre, false);
         pre_u = u;
     }
@@ -571,9 +580,10 @@ struct Streamer {
         // RoPE factors of this thread's pair in the first block, fetched now so
         // that the load is long done when the epilogue runs.
         float2 cs0 = make_float2(1.f, 0.f);
-        const bool pos_ok = ok(p.pos >= 0 && p.pos < p.ctx, SITE_QKV_ROW, p.pos);
+        const int pos = this->pos();
+        const bool pos_ok = ok(pos >= 0 && pos < p.ctx, SITE_QKV_ROW, pos);
         if (tid < min(lp.qkv_n, kRedRows / 2) && pos_ok)
-            cs0 = __ldg(p.rope + (size_t)p.pos * half + (lp.qkv_begin + tid) % half);
+            cs0 = __ldg(p.rope + (size_t)pos * half + (lp.qkv_begin + tid) % half);
         dot_op(2 * lp.qkv_n, [&](int b0, int nb) {
             const int t = tid;
             if (t < nb / 2) {
@@ -584,7 +594,7 @@ struct Streamer {
                 const float inv = inv_rms();
                 float a = row_sum(2 * t) * inv, b = row_sum(2 * t + 1) * inv;
                 if (hs < p.HQ_L + p.HKV_L) {  // RoPE on q and k
-                    const float2 cs = b0 == 0 ? cs0 : __ldg(p.rope + (size_t)p.pos * half + c);
+                    const float2 cs = b0 == 0 ? cs0 : __ldg(p.rope + (size_t)pos * half + c);
                     const float a2 = a * cs.x - b * cs.y;
                     const float b2 = a * cs.y + b * cs.x;
                     a = a2;
@@ -598,7 +608,7 @@ struct Streamer {
                     b = __half2float(hb);
                     __half *cache = isk ? p.kc : p.vc;
                     const size_t at =
-                        ((((size_t)lane_id * p.L + l) * p.HKV_L + g) * p.ctx + p.pos) * DH;
+                        ((((size_t)lane_id * p.L + l) * p.HKV_L + g) * p.ctx + pos) * DH;
                     if (ok(lane_id < p.NL && l < p.L && g >= 0 && g < p.HKV_L, SITE_KV_APPEND, g)) {
                         cache[at + c] = ha;
                         cache[at + c + half] = hb;
@@ -608,6 +618,10 @@ struct Streamer {
                 qkvb[hs * DH + c + half] = b;
             }
         });
+        // the appended K and V are read by bulk copies (async proxy) of the
+        // lane's later tokens in the same launch
+        fence_proxy_async_global();
+        cons_sync();
         if (!(p.skip_arrive_cta == cta && l == 0)) {
             if (tid == 0 && !S.abort_) {
                 __threadfence();
@@ -646,7 +660,7 @@ struct Streamer {
         const LayerPlan lp = p.lp[(size_t)cta * p.L + l];
         if (tid == 0 && !S.abort_) {
             const uint64_t t0 = p.trace ? global_timer_ns() : 0;
-            while (S.oflag < l + 1) {
+            while (S.oflag < tk * p.L + l + 1) {
                 __nanosleep(64);
                 if (S.abort_) break;
                 if (global_timer_ns() > deadline) { fail(5); break; }
@@ -699,7 +713,7 @@ struct Streamer {
             p.cand_i[cta] = bi;
             __threadfence();
             const uint32_t old = atomicAdd(p.fin, 1u);
-            S.last = (old == p.epoch * (uint32_t)p.n_cta - 1u) ? 1 : 0;
+            S.last = (old == ep() * (uint32_t)p.n_cta - 1u) ? 1 : 0;
             __threadfence();
         }
         cons_sync();
@@ -712,12 +726,48 @@ struct Streamer {
                 if (better(v, i, bv, bi)) { bv = v; bi = i; }
             }
             block_argmax(bv, bi);
-            if (tid == 0) *p.argmax = bi;
+            if (tid == 0) {
+                p.argmax[tk] = bi;
+                if (p.stamps) p.stamps[tk] = global_timer_ns();
+                __threadfence();
+                atomicAdd(p.tok_ready, 1u);  // the next token of this launch may embed it
+            }
         }
     }
 
     // ------------------------------------------------------------------ run
     __device__ void run() {
+        const int ntok = max(p.n_tokens, 1);
+        for (tk = 0; tk < ntok; ++tk) {
+            if (tk > 0) {  // the next token: stop together if any role failed in this one
+                cons_sync();
+                if (tid == 0) S.stop_s = S.abort_;
+                cons_sync();
+                if (S.stop_s) break;
+                pre_u = -1;  // lane-sum indices repeat per token
+                deadline = global_timer_ns() + p.timeout_ns;
+            }
+            run_token();
+        }
+        // After an error: wait (bounded) for the producer to stop and for the
+        // last copy issued into each stage to land before the CTA exits.
+        cons_sync();
+        if (tid == 0 && S.abort_) {
+            const uint64_t dl = global_timer_ns() + 1000000000ull;
+            while (!S.prod_done && global_timer_ns() < dl) {
+            }
+            const uint32_t issued = (uint32_t)S.issued;
+            for (int st = 0; st < C::STAGES; ++st) {
+                if ((uint32_t)st >= issued) break;
+                const uint32_t t = st + ((issued - 1 - st) / C::STAGES) * C::STAGES;
+                const uint32_t par = (t / C::STAGES) & 1u;
+                while (!mbar_try_wait(&S.full[st], par) && global_timer_ns() < dl) {
+                }
+            }
+        }
+    }
+
+    __device__ void run_token() {
         for (int oi = 0; oi < p.n_ops; ++oi) {
             if (tid == 0) S.cur_op = oi;
             const int op = __ldg(p.ops + oi);
@@ -749,22 +799,6 @@ struct Streamer {
                 tr[3] = S.t_tile;
             }
         }
-        // After an error: wait (bounded) for the producer to stop and for the
-        // last copy issued into each stage to land before the CTA exits.
-        cons_sync();
-        if (tid == 0 && S.abort_) {
-            const uint64_t dl = global_timer_ns() + 1000000000ull;
-            while (!S.prod_done && global_timer_ns() < dl) {
-            }
-            const uint32_t issued = (uint32_t)S.issued;
-            for (int st = 0; st < C::STAGES; ++st) {
-                if ((uint32_t)st >= issued) break;
-                const uint32_t t = st + ((issued - 1 - st) / C::STAGES) * C::STAGES;
-                const uint32_t par = (t / C::STAGES) & 1u;
-                while (!mbar_try_wait(&S.full[st], par) && global_timer_ns() < dl) {
-                }
-            }
-        }
     }
 };
 
@@ -792,6 +826,10 @@ struct Attention {
     __device__ bool ok(bool cond, int site, long long index) {
         return in_bounds(p, &S.abort_, cond, site, index, cur_op);
     }
+    // epoch (counter targets) and position of the current token (its index
+    // lives in shared memory, so that no register holds it through the loops)
+    __device__ uint32_t ep() const { return p.epoch + (uint32_t)S.atok; }
+    __device__ int pos() const { return p.pos + S.atok; }
     // a K or V tile of keys [j0, j0 + n) of heads g0 .. g0 + hc - 1
     __device__ bool tile_ok(int lane_id, int g0, int j0, int n) {
         return ok(lane_id < p.NL && g0 >= 0 && g0 + p.hc <= p.HKV_L && j0 >= 0 && n >= 0 && n <= p.kt &&
@@ -1009,7 +1047,7 @@ struct Attention {
         const int S_ = cp.S, GL = p.GL, HC = p.hc, kt = p.kt, NQ = HC * GL, items = NQ * DH;
         constexpr int DP = DH / 2, NG = kAttnThreads / DP;
         int a, b;
-        attn_range(p.pos, p.window[l], cp.k, S_, &a, &b);
+        attn_range(pos(), p.window[l], cp.k, S_, &a, &b);
         const bool last = (cp.k == S_ - 1);
         const int n_prev = b - a, T = (n_prev + kt - 1) / kt, T_eff = (last && T == 0) ? 1 : T;
         // earlier keys do not depend on this step: fetch the first tile before
@@ -1018,7 +1056,7 @@ struct Attention {
             issue_k(l, cp.lane, 0, a, min(kt, n_prev));
             issue_v(l, cp.lane, 0, a, min(kt, n_prev));
         }
-        wait_geq(&p.barA[l * p.NL + cp.lane], p.epoch * (uint32_t)S_);
+        wait_geq(&p.barA[l * p.NL + cp.lane], ep() * (uint32_t)S_);
         const float *qkvb = p.qkv + ((size_t)l * p.NL + cp.lane) * p.qkv_l;
         for (int g0 = 0; g0 < p.HKV_L; g0 += HC) {
             if (g0 > 0 && T > 0) {  // the buffers are free since the previous chunk's last barrier
@@ -1094,7 +1132,7 @@ struct Attention {
         const LayerPlan lp = p.lp[(size_t)cta * p.L + l];
         const CtaPlan cp = p.cta[cta];
         const int S_ = cp.S;
-        wait_geq(&p.barB[l * p.NL + cp.lane], p.epoch * (uint32_t)S_);
+        wait_geq(&p.barB[l * p.NL + cp.lane], ep() * (uint32_t)S_);
         float *ob = S.obuf[l & 1];
         const bool rows_ok =
             lp.o_n <= 0 ||
@@ -1170,11 +1208,37 @@ struct Attention {
         attn_sync();
         if (at == 0) {
             __threadfence_block();
-            S.oflag = l + 1;
+            S.oflag = S.atok * p.L + l + 1;
         }
     }
 
     __device__ void run() {
+        while (true) {
+            run_token();
+            // the next token, unless this was the last or any role failed
+            attn_sync();
+            if (at == 0) {
+                S.stop_a = S.abort_ || S.atok + 1 >= max(p.n_tokens, 1);
+                S.atok = S.atok + 1;
+            }
+            attn_sync();
+            if (S.stop_a) break;
+            deadline = global_timer_ns() + p.timeout_ns;
+        }
+        // after an error, let the last K and V tiles thread 0 issued land
+        // (tiles complete in order, so the last one's phase covers them all)
+        if (at == 0 && S.abort_) {
+            const uint64_t dl = global_timer_ns() + 1000000000ull;
+            if (kiss > 0)
+                while (!mbar_try_wait(&S.abarK, (kiss - 1) & 1u) && global_timer_ns() < dl) {
+                }
+            if (viss > 0)
+                while (!mbar_try_wait(&S.abarV, (viss - 1) & 1u) && global_timer_ns() < dl) {
+                }
+        }
+    }
+
+    __device__ void run_token() {
         for (int oi = 0; oi < p.n_ops; ++oi) {
             const int op = __ldg(p.ops + oi);
             if (op_type(op) != OP_ATTN) continue;
@@ -1193,17 +1257,6 @@ struct Attention {
                 tr[5] = S.a_tpv;
             }
         }
-        // after an error, let the last K and V tiles thread 0 issued land
-        // (tiles complete in order, so the last one's phase covers them all)
-        if (at == 0 && S.abort_) {
-            const uint64_t dl = global_timer_ns() + 1000000000ull;
-            if (kiss > 0)
-                while (!mbar_try_wait(&S.abarK, (kiss - 1) & 1u) && global_timer_ns() < dl) {
-                }
-            if (viss > 0)
-                while (!mbar_try_wait(&S.abarV, (viss - 1) & 1u) && global_timer_ns() < dl) {
-                }
-        }
     }
 };
 
@@ -1215,24 +1268,56 @@ __device__ void produce(const KParams &p, Smem<D, DH> &S, uint8_t *stages, uint6
     const CtaPlan cp = p.cta[cta];
     const uint64_t pol = policy_evict_first();
     uint32_t it = 0;
-    const uint8_t *w = reinterpret_cast<const uint8_t *>(p.wstream) + (size_t)cp.w_row0 * 2 * D;
-    const uint8_t *w_end = w + (size_t)cp.w_rows * 2 * D;
+    const uint8_t *const w0 = reinterpret_cast<const uint8_t *>(p.wstream) + (size_t)cp.w_row0 * 2 * D;
+    const uint8_t *const w_end = w0 + (size_t)cp.w_rows * 2 * D;
+    const uint8_t *w = w0;
     const uint8_t *pf = w;  // the L2 prefetch front of this CTA's weight stream
+    // with a further token in this launch: the prefetch front of that token's
+    // pass over the same stream (the prefetch runs on across the boundary)
+    const uint8_t *pf_next = w0;
+    const int ntok = max(p.n_tokens, 1);
+    int tk = 0;
     bool stop = false;
 
     unsigned long long t_blocked = 0, t_first = 0;  // trace of the current op
+    // While the consumers hold every stage for a while (the drain before the
+    // LM head, a lane barrier), HBM would sit idle: after idle_after_ns the
+    // producer pulls further rows of its own stream into L2, one stage's
+    // worth at a time, at most idle_prefetch_bytes beyond the rows it copies.
+    auto idle_prefetch = [&](uint64_t waited) {
+        if (p.idle_prefetch_bytes == 0 || waited < p.idle_after_ns) return;
+        const size_t lead = (size_t)(pf - w) + (size_t)(pf_next - w0);
+        if (lead >= (size_t)p.idle_prefetch_bytes) return;
+        if (pf < w_end) {
+            const uint32_t nb = (uint32_t)min((size_t)kStageBytes, (size_t)(w_end - pf));
+            bulk_prefetch_l2(pf, nb);
+            pf += nb;
+        } else if (tk + 1 < ntok && pf_next < w_end) {  // the next token's first rows
+            const uint32_t nb = (uint32_t)min((size_t)kStageBytes, (size_t)(w_end - pf_next));
+            bulk_prefetch_l2(pf_next, nb);
+            pf_next += nb;
+        }
+    };
     auto claim = [&](int &stage) -> bool {
         stage = it % C::STAGES;
         if (it >= C::STAGES) {
             const uint32_t par = ((it / C::STAGES) - 1) & 1u;
             if (!mbar_try_wait(&S.empty[stage], par)) {
                 const uint64_t t0 = global_timer_ns();
-                while (!mbar_try_wait(&S.empty[stage], par)) {
+                while (true) {
+                    if (p.idle_prefetch_bytes) {  // short polls, so that the idle time is seen
+                        if (mbar_test_wait(&S.empty[stage], par)) break;
+                        __nanosleep(256);
+                    } else if (mbar_try_wait(&S.empty[stage], par)) {
+                        break;
+                    }
                     if (S.abort_) return false;
-                    if (global_timer_ns() > deadline) {
+                    const uint64_t now = global_timer_ns();
+                    if (now > deadline) {
                         record_error(p, &S.abort_, 3u, -1);
                         return false;
                     }
+                    idle_prefetch(now - t0);
                 }
                 if (p.trace) t_blocked += global_timer_ns() - t0;
             }
@@ -1250,7 +1335,17 @@ __device__ void produce(const KParams &p, Smem<D, DH> &S, uint8_t *stages, uint6
                 return;
             }
             const uint8_t *want = w + bytes + ahead;
-            if (want > w_end) want = w_end;
+            if (want > w_end) {
+                if (tk + 1 < ntok) {  // run on into the next token's pass over the stream
+                    const uint8_t *want2 = w0 + min((size_t)(want - w_end), (size_t)(w_end - w0));
+                    while (pf_next < want2) {
+                        const uint32_t nb = (uint32_t)min((size_t)kStageBytes, (size_t)(want2 - pf_next));
+                        bulk_prefetch_l2(pf_next, nb);
+                        pf_next += nb;
+                    }
+                }
+                want = w_end;
+            }
             while (pf < want) {
                 const uint32_t nb = (uint32_t)min((size_t)kStageBytes, (size_t)(want - pf));
                 bulk_prefetch_l2(pf, nb);
@@ -1264,6 +1359,14 @@ __device__ void produce(const KParams &p, Smem<D, DH> &S, uint8_t *stages, uint6
         }
     };
 
+    for (tk = 0; tk < ntok && !stop; ++tk) {
+    if (tk > 0) {  // the same rows again for the next token
+        if (S.abort_) break;
+        w = w0;
+        pf = pf_next > w0 ? pf_next : w0;
+        pf_next = w0;
+        deadline = global_timer_ns() + p.timeout_ns;
+    }
     for (int oi = 0; oi < p.n_ops && !stop; ++oi) {
         const int op = __ldg(p.ops + oi);
         const int t = op_type(op), l = op_arg(op);
@@ -1280,6 +1383,7 @@ __device__ void produce(const KParams &p, Smem<D, DH> &S, uint8_t *stages, uint6
             tr[5] = t_first;
         }
     }
+    }  // tokens
     S.issued = (int)it;
     __threadfence_block();
     S.prod_done = 1;
@@ -1300,6 +1404,7 @@ __device__ void help(const KParams &p, Smem<D, DH> &S, uint64_t deadline) {
     const CtaPlan cp = p.cta[cta];
     uint32_t nred = 0, issued = 0;
     bool ok = true;
+    uint32_t ep = p.epoch;  // epoch of the current token of this launch
     // lane 0 waits until *ctr reaches target; false after an error or timeout
     auto wait_count = [&](const uint32_t *ctr, uint32_t target, int oi) -> bool {
         bool good = true;
@@ -1337,6 +1442,14 @@ __device__ void help(const KParams &p, Smem<D, DH> &S, uint64_t deadline) {
         if (good) ++nred;
         return good;
     };
+    const int ntok = max(p.n_tokens, 1);
+    for (int tk = 0; tk < ntok && ok; ++tk) {
+    if (tk > 0) {
+        // the next token: stop if this CTA failed in this one (one decision for the warp)
+        if (__shfl_sync(0xffffffffu, S.abort_ ? 1 : 0, 0)) break;
+        ep = p.epoch + (uint32_t)tk;
+        deadline = global_timer_ns() + p.timeout_ns;
+    }
     for (int oi = 0; oi < p.n_ops && ok; ++oi) {
         const int op = __ldg(p.ops + oi);
         const int t = op_type(op), u = op_arg(op);
@@ -1351,7 +1464,7 @@ __device__ void help(const KParams &p, Smem<D, DH> &S, uint64_t deadline) {
             // own-lane reading: this CTA's chunks c = k, k + S, ... of the
             // lane's sum, over the lane's S CTAs in order
             const uint64_t t_w0 = p.trace ? global_timer_ns() : 0;
-            ok = wait_count(&p.lcnt[u * p.NL + cp.lane], p.epoch * (uint32_t)cp.S, oi);
+            ok = wait_count(&p.lcnt[u * p.NL + cp.lane], ep * (uint32_t)cp.S, oi);
             const uint64_t t_w1 = p.trace ? global_timer_ns() : 0;
             float *rl = p.RL + ((size_t)(u % p.pslots) * p.NL + cp.lane) * D;
             for (int c = cp.k; ok && c < p.nch; c += cp.S) {
@@ -1382,7 +1495,7 @@ __device__ void help(const KParams &p, Smem<D, DH> &S, uint64_t deadline) {
         // over the CTAs in order
         uint64_t t_w0 = 0, t_w1 = 0, t_c = 0;
         if (p.trace && lane == 0) t_w0 = global_timer_ns();
-        ok = wait_count(&p.cnt[u], p.epoch * (uint32_t)p.n_cta, oi);
+        ok = wait_count(&p.cnt[u], ep * (uint32_t)p.n_cta, oi);
         if (!ok) break;
         if (p.trace && lane == 0) t_w1 = global_timer_ns();
         const float *src = slot + (size_t)cta * p.n_cta * kRChunk;
@@ -1410,6 +1523,7 @@ __device__ void help(const KParams &p, Smem<D, DH> &S, uint64_t deadline) {
             }
         }
     }
+    }  // tokens
     // after an error, let pieces still in flight land before the CTA exits
     if (lane == 0 && issued > nred) {
         const uint64_t dl = global_timer_ns() + 1000000000ull;
@@ -1440,6 +1554,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         S.issued = 0;
         S.oflag = 0;
         S.last = 0;
+        S.atok = 0;
         fence_barrier_init();
     }
     __syncthreads();

@@ -20,11 +20,20 @@ struct KParams {
     // this step
     int pos, token;
     const int *token_src;  // non-null: the token is read here on the device (chained steps)
-    uint32_t epoch;  // launches since the last reset; counters target epoch * n
+    uint32_t epoch;  // tokens decoded since the last reset, this one included; counters target epoch * n
+    // Several tokens in one launch (greedy generation): token t (epoch + t,
+    // position pos + t) writes its argmax to argmax[t] and then bumps
+    // *tok_ready; token t + 1 embeds argmax[t] once *tok_ready has reached
+    // epoch + t.  stamps (nullable) receives each token's completion time.
+    int n_tokens;
+    uint32_t *tok_ready;
+    unsigned long long *stamps;
     unsigned long long timeout_ns;
     int skip_arrive_cta;
     unsigned l2_prefetch_bytes;  // weight-stream L2 prefetch distance beyond the stage ring
     unsigned lm_prefetch_bytes;  // the same for the LM-head rows (the step's drain is idle HBM time)
+    unsigned idle_prefetch_bytes;  // further prefetch while the producer has waited idle_after_ns for a stage
+    unsigned idle_after_ns;
     int window[LF_MAX_LAYERS];
     // plan
     const int *ops;

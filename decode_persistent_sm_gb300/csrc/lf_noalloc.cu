@@ -157,10 +157,13 @@ extern "C" lf_status lf_decode_step_static_scratch(lf_engine *e, int32_t token,
     k.pos = e->pos;
     k.token = token;
     k.epoch = 1;  // counters were just cleared
+    k.n_tokens = 1;
     k.timeout_ns = e->timeout_ns;
     k.skip_arrive_cta = -1;
     k.l2_prefetch_bytes = e->l2_prefetch_bytes;
     k.lm_prefetch_bytes = e->lm_prefetch_bytes;
+    k.idle_prefetch_bytes = e->idle_prefetch_bytes;
+    k.idle_after_ns = e->idle_after_ns;
     for (int l = 0; l < s.L; ++l) k.window[l] = e->cfg.swa_window[l];
     k.ops = e->d_ops; k.cta = e->d_cta; k.lp = e->d_lp;
     k.wstream = e->wstream; k.emb = e->emb; k.gains = e->gains; k.rope = e->rope;
@@ -177,6 +180,7 @@ extern "C" lf_status lf_decode_step_static_scratch(lf_engine *e, int32_t token,
     k.cnt = q; q += 2 * s.L;
     k.ready = q; q += 2 * s.L;
     k.fin = q;
+    k.tok_ready = q + 1;
     k.err = ctr + e->n_ctr + 4;
     k.logits = logits_device;
     k.argmax = argmax_device;

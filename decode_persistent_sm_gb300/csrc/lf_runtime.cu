@@ -273,7 +273,8 @@ lf_status lf_create(const lf_config *cfg, lf_engine **out) {
     const lf::Plan &P = e->plan;
     const lf::Shape &s = P.sh;
     const int L = s.L, NC = P.n_cta;
-    e->n_ctr = (size_t)L * s.NL * 2 + (size_t)4 * L + 1 + (size_t)4 * L * s.NL;  // + own-lane counters
+    // barA, barB | cnt, ready | fin, tok_ready | own-lane counters
+    e->n_ctr = (size_t)L * s.NL * 2 + (size_t)4 * L + 2 + (size_t)4 * L * s.NL;
     const size_t kv_elems = (size_t)s.NL * L * s.HKV_L * s.ctx * s.DH;
     const int qkv_l = (s.HQ_L + 2 * s.HKV_L) * s.DH;
     cudaError_t err = cudaSuccess;
@@ -293,6 +294,7 @@ lf_status lf_create(const lf_config *cfg, lf_engine **out) {
     ALLOC(ctr, e->n_ctr);
     ALLOC(status, 8);
     ALLOC(gen, s.ctx);
+    ALLOC(stamps, s.ctx);
     ALLOC(pf_err, 1);
     ALLOC(cand_v, NC);
     ALLOC(cand_i, NC);
@@ -441,10 +443,13 @@ static lf_status read_status(lf_engine *e, float *logits, int32_t *argmax) {
     return LF_OK;
 }
 
-// Enqueues one decode step at the current position (checked by the caller).
-// The input token is `token`, or *token_src read on the device when non-null;
-// the argmax goes to *argmax_dst (device).
-static lf_status enqueue_step(lf_engine *e, int32_t token, const int32_t *token_src, int32_t *argmax_dst) {
+// Enqueues n_tokens decode steps from the current position in one launch
+// (checked by the caller).  The first step's token is `token`, or *token_src
+// read on the device when non-null; step t's argmax goes to argmax_dst[t]
+// (device), and step t + 1 embeds it.  stamps (device, nullable): each step's
+// completion time.
+static lf_status enqueue_steps(lf_engine *e, int32_t token, const int32_t *token_src, int32_t *argmax_dst,
+                               int n_tokens, unsigned long long *stamps) {
     const lf::Plan &P = e->plan;
     const lf::Shape &s = P.sh;
     lf::KParams k{};
@@ -463,10 +468,14 @@ static lf_status enqueue_step(lf_engine *e, int32_t token, const int32_t *token_
     k.token = token;
     k.token_src = token_src;
     k.epoch = e->epoch + 1;
+    k.n_tokens = n_tokens;
+    k.stamps = stamps;
     k.timeout_ns = e->timeout_ns;
     k.skip_arrive_cta = e->skip_cta;
     k.l2_prefetch_bytes = e->l2_prefetch_bytes;
     k.lm_prefetch_bytes = e->lm_prefetch_bytes;
+    k.idle_prefetch_bytes = e->idle_prefetch_bytes;
+    k.idle_after_ns = e->idle_after_ns;
     for (int l = 0; l < s.L; ++l) k.window[l] = e->cfg.swa_window[l];
     k.ops = e->d_ops; k.cta = e->d_cta; k.lp = e->d_lp;
     k.wstream = e->wstream; k.emb = e->emb; k.gains = e->gains; k.rope = e->rope;
@@ -477,20 +486,25 @@ static lf_status enqueue_step(lf_engine *e, int32_t token, const int32_t *token_
     k.cnt = c; c += 2 * s.L;
     k.ready = c; c += 2 * s.L;
     k.fin = c; c += 1;
+    k.tok_ready = c; c += 1;
     k.lcnt = c; c += (size_t)2 * s.L * s.NL;
     k.lready = c;
     k.cand_v = e->cand_v; k.cand_i = e->cand_i; k.logits = e->logits;
     k.argmax = argmax_dst;
     k.err = e->status + 4;
-    k.trace = e->trace;
+    k.trace = n_tokens == 1 ? e->trace : nullptr;  // the trace records one step
 
     cudaError_t err = lf::launch_decode(k, e->stream);
     e->skip_cta = -1;
     if (err != cudaSuccess) return cuda_fail(e, err);
-    e->epoch += 1;
-    e->pos += 1;
+    e->epoch += (uint32_t)n_tokens;
+    e->pos += n_tokens;
     e->launches += 1;
     return LF_OK;
+}
+
+static lf_status enqueue_step(lf_engine *e, int32_t token, const int32_t *token_src, int32_t *argmax_dst) {
+    return enqueue_steps(e, token, token_src, argmax_dst, 1, nullptr);
 }
 
 lf_status lf_decode_step(lf_engine *e, int32_t token, float *logits, int32_t *argmax) {
@@ -559,14 +573,23 @@ lf_status lf_generate(lf_engine *e, int32_t first_token, int n, int32_t *tokens_
     const lf::Shape &s = e->plan.sh;
     if (first_token < 0 || first_token >= s.V) return LF_ERR_INVALID_ARG;
     if ((long long)e->pos + n > s.ctx) return LF_ERR_CTX_OVERFLOW;
-    for (int i = 0; i < n; ++i) {
-        lf_status st = enqueue_step(e, first_token, i ? e->gen + i - 1 : nullptr, e->gen + i);
-        if (st != LF_OK) return st;
-    }
+    // all n steps in one launch: each CTA's weight copies run on into the next
+    // step while this one drains, and step t + 1 embeds step t's argmax
+    lf_status st = enqueue_steps(e, first_token, nullptr, e->gen, n, e->stamps);
+    if (st != LF_OK) return st;
+    e->gen_n = n;
     cudaError_t err = cudaMemcpyAsync(tokens_out, e->gen, (size_t)n * sizeof(int32_t), cudaMemcpyDeviceToHost,
                                       e->stream);
     if (err != cudaSuccess) return cuda_fail(e, err);
     return read_status(e, logits, nullptr);
+}
+
+lf_status lf_generate_stamps(lf_engine *e, uint64_t *ns, int n) {
+    if (!e || !ns || n < 1 || n > e->gen_n) return LF_ERR_INVALID_ARG;
+    if (e->poisoned != LF_OK) return e->poisoned;
+    cudaError_t err = cudaMemcpyAsync(ns, e->stamps, (size_t)n * sizeof(uint64_t), cudaMemcpyDeviceToHost, e->stream);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(e->stream);
+    return err == cudaSuccess ? LF_OK : cuda_fail(e, err);
 }
 
 lf_status lf_synchronize(lf_engine *e) {
@@ -675,6 +698,13 @@ lf_status lf_set_l2_prefetch(lf_engine *e, uint32_t bytes_per_sm, uint32_t lm_by
         return LF_ERR_INVALID_ARG;
     e->l2_prefetch_bytes = bytes_per_sm;
     e->lm_prefetch_bytes = lm_bytes_per_sm;
+    return LF_OK;
+}
+
+lf_status lf_set_idle_prefetch(lf_engine *e, uint32_t bytes_per_sm, uint32_t after_ns) {
+    if (!e || (bytes_per_sm % 16) != 0 || bytes_per_sm > (64u << 20)) return LF_ERR_INVALID_ARG;
+    e->idle_prefetch_bytes = bytes_per_sm;
+    e->idle_after_ns = after_ns;
     return LF_OK;
 }
 

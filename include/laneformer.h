@@ -120,12 +120,22 @@ lf_status lf_decode_step(lf_engine *e, int32_t token, float *logits, int32_t *ar
  * infrastructure", quotes, decoded greedily as in its "Training and data
  * specialisation" section.  Runs n >= 1 decode steps from the current
  * position: step 0 reads `first_token`, step i > 0 reads the argmax of step
- * i - 1 straight from device memory.  tokens_out (host, n int32, required)
- * receives the n argmax tokens; logits (host, vocab floats, nullable) those
- * of the last step.  Advances the position by n.  Synchronous.
+ * i - 1 straight from device memory.  All n steps run in one launch of the
+ * persistent kernel: each SM's weight copies run on into step i + 1 while
+ * step i drains its last lane sums and its LM head, and step i + 1 embeds
+ * step i's argmax as soon as it is published.  The results are those of n
+ * lf_decode_step calls.  tokens_out (host, n int32, required) receives the n
+ * argmax tokens; logits (host, vocab floats, nullable) those of the last
+ * step.  Advances the position by n.  Synchronous.
  * LF_ERR_INVALID_ARG for n < 1, a NULL tokens_out or first_token outside
  * [0, vocab); LF_ERR_CTX_OVERFLOW if position + n > ctx_cap (nothing run). */
 lf_status lf_generate(lf_engine *e, int32_t first_token, int n, int32_t *tokens_out, float *logits);
+
+/* Completion time of each of the first n steps of the last lf_generate call
+ * (the device's global timer, ns, taken when the step's argmax is
+ * published) into ns (host, n uint64).  Differences give per-token latency.
+ * LF_ERR_INVALID_ARG if n exceeds that call's step count. */
+lf_status lf_generate_stamps(lf_engine *e, uint64_t *ns, int n);
 
 /* Stochastic decoding for pass@N (News (asector), "Performance and
  * infrastructure": several sampled solutions per prompt are affordable
@@ -209,6 +219,14 @@ lf_status lf_set_timeout_ns(lf_engine *e, uint64_t ns);
  * reached while the step drains its last lane sums (default 128 KiB).  0 turns
  * a prefetch off. */
 lf_status lf_set_l2_prefetch(lf_engine *e, uint32_t bytes_per_sm, uint32_t lm_bytes_per_sm);
+
+/* Tuning: when an SM's weight copies have waited after_ns for a free stage
+ * (its consumers are held up, e.g. by the last lane sums before the LM head),
+ * the SM prefetches further rows of its stream into L2, 32 KiB at a time,
+ * until it is bytes_per_sm (a multiple of 16) ahead of its copies; HBM then
+ * works during the wait (default 768 KiB after 4000 ns).  0 bytes turns it
+ * off. */
+lf_status lf_set_idle_prefetch(lf_engine *e, uint32_t bytes_per_sm, uint32_t after_ns);
 
 /* Test hook: in the next decode step, CTA `cta` skips its first lane-barrier
  * arrival (-1 = off), so that the lane's other CTAs time out.  Proves that the

@@ -140,3 +140,53 @@ def test_out_of_vocabulary_device_token_poisons_until_reset():
             ref = orc.step(int(t))
             assert note(got, ref, am) <= REL_L2
             assert am == oracle.argmax(ref)
+
+
+@pytest.mark.parametrize("lanes,delay,own", [(8, 0, 0), (8, 1, 0), (1, 2, 0), (4, 3, 0), (8, 2, 1), (2, 1, 1)])
+def test_generate_in_one_launch_equals_separate_steps(lanes, delay, own):
+    # lf_generate runs all steps in one launch of the persistent kernel; the
+    # tokens and the last logits must be those of one launch per step
+    from decode_persistent_sm_gb300 import Engine
+    shape = synth.TINY.replace(n_layers=6, swa_window=(64, 0, 16, 0, 8, 0), n_lanes=lanes, dtp_delay=delay,
+                               own_lane_immediate=own)
+    blob = synth.make_weights(shape, 60 + lanes + delay, gain_std=0.1)
+    prompt = synth.make_tokens(60, 10, shape.vocab)
+    with Engine.from_shape(shape) as a, Engine.from_shape(shape) as b:
+        a.load_weights(blob)
+        b.load_weights(blob)
+        a.prefill(prompt[:-1], logits=False)
+        b.prefill(prompt[:-1], logits=False)
+        gen, last = a.generate(int(prompt[-1]), 40, logits=True)
+        ref, ref_last = host_loop(b, prompt[-1], 40)
+        assert np.array_equal(gen, ref) and np.array_equal(last, ref_last)
+        stamps = a.generate_stamps(40).astype(np.int64)
+        assert np.all(np.diff(stamps) > 0)
+        # and the next call continues the same sequence
+        gen2, _ = a.generate(int(gen[-1]), 5)
+        ref2, _ = host_loop(b, gen[-1], 5)
+        assert np.array_equal(gen2, ref2)
+
+
+@pytest.mark.slow
+def test_full_generate_in_one_launch_across_the_window():
+    # 40 tokens from position 1000: the sliding-window layers cross their
+    # 1024-key window inside the launch, and each step's attention reads the
+    # keys the launch's earlier steps appended
+    from decode_persistent_sm_gb300 import Engine
+    shape = synth.FULL
+    blob = synth.make_weights(shape, 1)
+    kv = synth.make_kv(shape, 1, 1000)
+    first = int(synth.make_tokens(42, 1, shape.vocab)[0])
+    with Engine.from_shape(shape) as eng:
+        eng.load_weights(blob)
+        eng.load_kv(kv, 1000)
+        gen, last = eng.generate(first, 40, logits=True)
+        stamps = eng.generate_stamps(40).astype(np.int64)
+        eng.set_position(1000)
+        ref, ref_last = host_loop(eng, first, 40)
+    assert np.array_equal(gen, ref) and np.array_equal(last, ref_last)
+    per_token_ms = np.diff(stamps) / 1e6
+    assert 0.2 < np.median(per_token_ms) < 5.0
+    orc = oracle.Oracle(shape, blob)
+    orc.load_kv(kv, 1000)
+    assert oracle_agreement(orc, first, gen) >= 39 / 40
