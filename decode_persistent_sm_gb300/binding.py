@@ -28,6 +28,7 @@ _SIGS = {
     "lf_prefill": (_ci, [_vp, _vp, _ci, _vp, _vp]),
     "lf_decode_step": (_ci, [_vp, _i32, _vp, _vp]),
     "lf_matmul_f16": (_ci, [_vp, _vp, _vp, _ci, _ci, _ci, _vp]),
+    "lf_matmul_f16_async": (_ci, [_vp, _vp, _vp, _ci, _ci, _ci, _vp, _vp]),
     "lf_prefill_batched": (_ci, [_vp, _vp, _ci, _vp, _vp]),
     "lf_set_prefill_attention": (_ci, [_vp, _ci]),
     "lf_generate": (_ci, [_vp, _i32, _ci, _vp, _vp]),
@@ -135,6 +136,14 @@ def matmul_f16(a_ptr: int, b_ptr: int, c_ptr: int, m: int, n: int, k: int, strea
     FP16 a, b row-major, fp32 c); waits for the stream."""
     lib = load_library()
     _check("lf_matmul_f16", lib.lf_matmul_f16(a_ptr, b_ptr, c_ptr, int(m), int(n), int(k), stream))
+
+
+def matmul_f16_async(a_ptr: int, b_ptr: int, c_ptr: int, m: int, n: int, k: int, err_ptr: int,
+                     stream: Optional[int] = None):
+    """lf_matmul_f16_async: enqueue c = a . b^T; *err_ptr (device) flags a timeout."""
+    lib = load_library()
+    _check("lf_matmul_f16_async",
+           lib.lf_matmul_f16_async(a_ptr, b_ptr, c_ptr, int(m), int(n), int(k), err_ptr, stream))
 
 
 def gemv_f16(w_ptr: int, x_ptr: int, y_ptr: int, n: int, k: int, batch: int, stream: Optional[int] = None):

@@ -154,6 +154,15 @@ extern "C" lf_status lf_matmul_f16(const void *a_device, const void *b_device, f
     return h ? LF_ERR_TIMEOUT : LF_OK;
 }
 
+extern "C" lf_status lf_matmul_f16_async(const void *a_device, const void *b_device, float *c_device, int m, int n,
+                                         int k, uint32_t *err_device, void *cuda_stream) {
+    if (!a_device || !b_device || !c_device || !err_device || m < 1 || n < 1 || k < 64 || k % 64 ||
+        (reinterpret_cast<uintptr_t>(err_device) & 3u))
+        return LF_ERR_INVALID_ARG;
+    return lf::tc_gemm_f16(static_cast<const __half *>(a_device), static_cast<const __half *>(b_device), c_device,
+                           m, n, k, n, err_device, kGemmTimeoutNs, static_cast<cudaStream_t>(cuda_stream));
+}
+
 namespace {
 
 __device__ __forceinline__ void pf_h8(uint4 w, float *f) {

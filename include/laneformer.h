@@ -337,6 +337,14 @@ lf_status lf_set_prefill_attention(lf_engine *e, int tensor_cores);
 lf_status lf_matmul_f16(const void *a_device, const void *b_device, float *c_device, int m, int n, int k,
                         void *cuda_stream);
 
+/* The same product, only enqueued on `cuda_stream` (no wait, no status read
+ * back): for callers that chain several products, and for timing the kernel
+ * alone.  *err_device (device word, 4-byte aligned, cleared by the caller)
+ * becomes non-zero if a device-side wait ran out.  LF_ERR_INVALID_ARG for bad
+ * sizes or pointers, LF_ERR_CUDA if the launch failed. */
+lf_status lf_matmul_f16_async(const void *a_device, const void *b_device, float *c_device, int m, int n, int k,
+                              uint32_t *err_device, void *cuda_stream);
+
 /* Batched decode for pass@N (News, "Performance and infrastructure":
  * several sampled solutions per prompt): n_batch samples (1..16) continue
  * the engine's current sequence together, one position per step, each with

@@ -54,3 +54,18 @@ def test_matmul_rejects_bad_sizes():
     lib = load_library()
     assert lib.lf_matmul_f16(None, None, None, 1, 1, 64, None) == 1
     assert lib.lf_matmul_f16(ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16), 1, 1, 65, None) == 1
+
+
+def test_async_matmul_equals_the_synchronous_call():
+    import torch
+    from decode_persistent_sm_gb300 import matmul_f16, matmul_f16_async
+    a, b, c = run(300, 520, 256, 5)
+    ta = torch.from_numpy(a).cuda()
+    tb = torch.from_numpy(b).cuda()
+    tc = torch.full((300, 520), float("nan"), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(3):  # chained on one stream, no wait in between
+        matmul_f16_async(ta.data_ptr(), tb.data_ptr(), tc.data_ptr(), 300, 520, 256, err.data_ptr())
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(tc.cpu().numpy(), c)  # same kernel, same summation order
