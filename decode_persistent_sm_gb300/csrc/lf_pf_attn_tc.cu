@@ -105,7 +105,13 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     uint8_t *t = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(at_raw) + 1023) & ~uintptr_t(1023));
     AttnShared &S = *reinterpret_cast<AttnShared *>(t + A_TILES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qt = blockIdx.x, h0 = blockIdx.y * nh, i0 = qt * AQ;
+    // CTAs are dispatched in index order; the causal triangle gives the last
+    // query tiles the most key tiles, so index i takes query tile
+    // n_qt - 1 - i / n_pairs: the longest CTAs start first and the short ones
+    // fill the SMs at the end (with the smallest first, the longest started
+    // last and set a long tail)
+    const int n_qt = (a.M + AQ - 1) / AQ, n_pairs = a.NQ / nh;
+    const int qt = n_qt - 1 - (int)(blockIdx.x / n_pairs), h0 = (int)(blockIdx.x % n_pairs) * nh, i0 = qt * AQ;
     const int rows = min(AQ, a.M - i0);
     const int p_first = a.p0 + i0, p_last = a.p0 + i0 + rows - 1;
     const int lo = a.window > 0 ? max(0, p_first - a.window + 1) : 0, hi = p_last;
@@ -423,7 +429,7 @@ lf_status pf_attention_tc(const __half *q16, const __half *kc, const __half *vt,
     if (attr_err != cudaSuccess) return LF_ERR_CUDA;
     // two q heads per CTA when consecutive q heads pair up on one lane-local KV head
     const int nh = (a.GL % 2 == 0 && a.HQ_L % 2 == 0) ? 2 : 1;
-    const dim3 grid((a.M + AQ - 1) / AQ, a.NQ / nh);
+    const dim3 grid((unsigned)(((a.M + AQ - 1) / AQ) * (a.NQ / nh)));
     pf_attn_tc_kernel<<<grid, A_THREADS, A_SMEM, stream>>>(mq, mk, mv, a, nh, err, timeout_ns);
     return cudaGetLastError() == cudaSuccess ? LF_OK : LF_ERR_CUDA;
 }
