@@ -436,7 +436,9 @@ def run_ours(args, world, rank, local):
     achieved = nbytes / (ms / 1e3) / 1e9
     read_gbs = read_stream_gbs(nbytes, stream)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": profile_traffic() if POS == 512 else None,
+                "frac": achieved / peak,
+                # the committed capture covers the full-shape launch at position 512 only
+                "traffic": profile_traffic() if POS == 512 and not args.layers else None,
                 "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                 "algorithmic_bytes_per_launch": nbytes,
                 # the copy figure counts a read and a write; a read-only stream in
