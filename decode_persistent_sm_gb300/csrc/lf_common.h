@@ -48,7 +48,12 @@ constexpr int kAttnThreads = kAttnWarps * 32;
 constexpr int kThreads = kConsThreads + kAttnThreads + 64;
 constexpr int kStageBytes = 32768;
 constexpr int kStages = 4;
-constexpr int kAttnBuf = 32768;    // attention group's KV tile buffer
+// Attention KV tiles: per attention warp (one KV head each) a K and a V tile
+// of kAttnKT keys, every key row padded by 16 bytes so that the eight rows of
+// an 8x8 matrix load fall in eight different bank groups.
+constexpr int kAttnKT = 32;
+LF_HD constexpr int attn_row_bytes(int dh) { return 2 * dh + 16; }
+constexpr int kAttnBuf = 2 * kAttnWarps * kAttnKT * (2 * 128 + 16);  // K tiles, then V tiles
 constexpr int kMaxCtas = 160;      // helper buffer rows (one 128-byte piece per CTA)
 constexpr int kRChunk = 32;        // floats per chunk of the delayed lane sum
 constexpr int kMaxUnitsPerCta = 256;
@@ -56,11 +61,6 @@ constexpr int kMaxORowsPerCta = 256;
 constexpr int kMaxGroup = 4;       // q heads per KV head inside one lane
 constexpr int kMaxLaneCtas = 160;  // CTAs per lane (attention merge weights)
 constexpr int kRedRows = 128;      // GEMV rows reduced per epilogue block
-constexpr int kAttnScores = 640;   // scores per attention tile (q heads x attn_ldk(keys))
-// Row stride of the attention score rows: room for the current key and a
-// float4 read past the last key, 16-byte aligned rows.
-LF_HD constexpr int attn_ldk(int kt) { return (kt + 7) & ~3; }
-constexpr int kMaxChunkHeads = 16; // q heads per attention chunk
 
 // Op list: every CTA walks the same list; an op's data differs per CTA.
 enum OpType : int {

@@ -43,14 +43,12 @@ struct Cfg {
     static_assert(!kBlockRow || RPT == 4, "block-row GEMV assumes 4 rows per tile");
     static_assert(kRedRows % RPT == 0, "reduction block");
     static constexpr int GLMAX = 256 / DH < kMaxGroup ? 256 / DH : kMaxGroup;
-    // attention q in shared memory: 8-float chunks at a stride of 12 floats,
-    // so that 8 threads reading 8 different chunks hit 8 different bank groups
-    static constexpr int QCH = DH / 8;
-    static constexpr int QST = QCH * 12;  // floats per q head
-    static_assert((QCH & (QCH - 1)) == 0, "head_dim chunks");
-    // attention: P.V by dimension pairs, at most 4 q heads per thread
-    static_assert((DH / 2 & (DH / 2 - 1)) == 0 && kAttnThreads % (DH / 2) == 0, "head_dim layout");
-    static_assert(512 / DH <= 4 * (kAttnThreads / (DH / 2)), "q heads per attention thread");
+    // attention: head_dim in 16-wide MMA steps; per warp a K and a V tile of
+    // kAttnKT padded key rows
+    static constexpr int KS = DH / 16;
+    static constexpr int RB = attn_row_bytes(DH);
+    static_assert(DH % 16 == 0 && kAttnKT == 32, "attention MMA tiling");
+    static_assert(2 * kAttnWarps * kAttnKT * RB <= kAttnBuf && RB % 16 == 0, "attention tile buffer");
 };
 
 template <int D, int DH>
@@ -58,7 +56,7 @@ struct Smem {
     using C = Cfg<D, DH>;
     uint64_t full[C::STAGES];
     uint64_t empty[C::STAGES];
-    uint64_t abarK, abarV;            // attention K / V tile arrival
+    uint64_t abarK[kAttnWarps], abarV[kAttnWarps];  // attention K / V tile arrival, per warp
     uint64_t hbar;                    // helper: partial pieces arrival
     // streaming warps
     float red[kConsWarps][kRedRows];  // GEMV row partials per warp (row sums in red[0] if warp-per-row)
@@ -69,12 +67,9 @@ struct Smem {
     float axbuf[kConsWarps][C::kBlockRow ? 1 : D];
     float amv[kConsWarps];
     int ami[kConsWarps];
-    // attention warps
-    __align__(16) float qs[512 / DH * C::QST];  // q of the current head chunk, padded chunks
-    __align__(16) float sc[kAttnScores];       // scores / probabilities, [q head][attn_ldk(kt)]
-    float am[kMaxChunkHeads], al[kMaxChunkHeads], alpha[kMaxChunkHeads];
-    __align__(16) __half curk[kConsThreads];   // this step's key / value, per chunk head
-    __align__(16) __half curv[kConsThreads];
+    // attention warps: per warp, the q fragments of its KV head's q heads for
+    // every 16-wide step of head_dim, (hi b0, hi b1, lo b0, lo b1) per lane
+    __align__(16) uint4 qf[kAttnWarps][C::KS * 32];
     float2 ml[4][kMaxLaneCtas];                // merge: (m, l) per lane CTA, then (weight, l)
     // helper warp: one 32-float piece of every CTA's partial
     __align__(16) float hbuf[kMaxCtas][kRChunk];
@@ -806,13 +801,14 @@ struct Streamer {
 template <int D, int DH>
 struct Attention {
     using C = Cfg<D, DH>;
+    static constexpr int KT = kAttnKT, RB = C::RB, KS = C::KS, MD = DH / 16;
     const KParams &p;
     Smem<D, DH> &S;
     uint8_t *abuf;
     int at, awarp, lane, cta, cur_op;
     uint64_t deadline;
-    uint32_t kwait, vwait;  // K / V tiles waited for (every attention thread keeps the counts)
-    uint32_t kiss, viss;    // K / V tiles whose copies thread 0 issued
+    uint32_t kwait, vwait;  // this warp's K / V tiles waited for (every lane keeps the counts)
+    uint32_t kiss, viss;    // this warp's K / V tiles issued
 
     __device__ Attention(const KParams &p_, Smem<D, DH> &S_, uint8_t *ab, uint64_t dl)
         : p(p_), S(S_), abuf(ab), deadline(dl), cur_op(0), kwait(0), vwait(0), kiss(0), viss(0) {
@@ -830,12 +826,6 @@ struct Attention {
     // lives in shared memory, so that no register holds it through the loops)
     __device__ uint32_t ep() const { return p.epoch + (uint32_t)S.atok; }
     __device__ int pos() const { return p.pos + S.atok; }
-    // a K or V tile of keys [j0, j0 + n) of heads g0 .. g0 + hc - 1
-    __device__ bool tile_ok(int lane_id, int g0, int j0, int n) {
-        return ok(lane_id < p.NL && g0 >= 0 && g0 + p.hc <= p.HKV_L && j0 >= 0 && n >= 0 && n <= p.kt &&
-                      j0 + n <= p.ctx && p.hc * p.kt * DH * 2 <= kAttnBuf / 2,
-                  SITE_KV_TILE, j0);
-    }
 
     __device__ void wait_geq(const uint32_t *ptr, uint32_t target) {
         if (at == 0 && !S.abort_) {
@@ -850,36 +840,29 @@ struct Attention {
         attn_sync();
     }
 
-    // Bulk-loads keys [j0, j0 + n) of the chunk's HC KV heads: K into the
-    // first half of the tile buffer (head g at g*kt keys), V into the second.
-    // K and V have their own barriers, so the next tile's K can load while
-    // this tile's P.V runs and its V while the next scores run.  Only thread 0
-    // issues, at most one tile ahead of the waits.
-    __device__ void issue_k(int l, int lane_id, int g0, int j0, int n) {
-        if (at == 0 && !S.abort_ && kiss == kwait && tile_ok(lane_id, g0, j0, n)) {
-            const uint32_t bytes = (uint32_t)n * DH * 2;
-            mbar_arrive_expect_tx(&S.abarK, (uint32_t)p.hc * bytes);
-            for (int g = 0; g < p.hc; ++g) {
-                const size_t head = (((size_t)lane_id * p.L + l) * p.HKV_L + g0 + g) * p.ctx;
-                bulk_g2s(abuf + (size_t)g * p.kt * DH * 2, p.kc + (head + j0) * DH, bytes, &S.abarK);
-            }
-            ++kiss;
-        }
-    }
-    __device__ void issue_v(int l, int lane_id, int g0, int j0, int n) {
-        if (at == 0 && !S.abort_ && viss == vwait && tile_ok(lane_id, g0, j0, n)) {
-            const uint32_t bytes = (uint32_t)n * DH * 2;
-            mbar_arrive_expect_tx(&S.abarV, (uint32_t)p.hc * bytes);
-            for (int g = 0; g < p.hc; ++g) {
-                const size_t head = (((size_t)lane_id * p.L + l) * p.HKV_L + g0 + g) * p.ctx;
-                bulk_g2s(abuf + kAttnBuf / 2 + (size_t)g * p.kt * DH * 2, p.vc + (head + j0) * DH, bytes,
-                         &S.abarV);
-            }
-            ++viss;
-        }
+    // This warp's K (or V) tile: keys [j0, j0 + n) of lane-local KV head g
+    // of layer l, key j0 + i copied by lane i into padded row i.  The warp's
+    // barrier counts the bytes; at most one tile of each kind is in flight.
+    __device__ void issue(bool v, int l, int lane_id, int g, int j0, int n) {
+        uint32_t &iss = v ? viss : kiss;
+        const uint32_t waited = v ? vwait : kwait;
+        const bool go = __shfl_sync(0xffffffffu,
+                                    !S.abort_ && iss == waited &&
+                                        ok(lane_id < p.NL && g >= 0 && g < p.HKV_L && j0 >= 0 && n > 0 && n <= KT &&
+                                               j0 + n <= p.ctx,
+                                           SITE_KV_TILE, j0),
+                                    0);
+        if (!go) return;
+        uint64_t *bar = v ? &S.abarV[awarp] : &S.abarK[awarp];
+        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)n * DH * 2);
+        __syncwarp();
+        const size_t head = (((size_t)lane_id * p.L + l) * p.HKV_L + g) * p.ctx;
+        uint8_t *dst = abuf + (v ? kAttnBuf / 2 : 0) + (size_t)awarp * KT * RB;
+        if (lane < n) bulk_g2s(dst + lane * RB, (v ? p.vc : p.kc) + (head + j0 + lane) * DH, DH * 2, bar);
+        ++iss;
     }
 
-    // Waits for the K (or V) tile issued last (tile i completes phase i).
+    // Waits for the warp's K (or V) tile issued last (tile i completes phase i).
     __device__ void wait_kv(uint64_t *bar, uint32_t &count) {
         const uint64_t t0 = (p.trace && at == 0) ? global_timer_ns() : 0;
         // (in abort mode nothing may have been issued: the loop then stops at once)
@@ -890,235 +873,246 @@ struct Attention {
         ++count;
     }
 
-    // Scores of keys [0, n) of the tile plus (has_cur) the current key from
-    // S.curk at index n, for all q heads of the chunk: one (KV head, key)
-    // pair per thread over the whole head dimension, 8 dimensions per step.
-    // The chunk order is rotated by the key, so the 8 threads of a quarter
-    // warp read 8 different bank groups of K (rows 256 B apart) and of q.
-    template <int GL>
-    __device__ void scores_t(int n, bool has_cur) {
-        const int HC = p.hc, kt = p.kt, ldk = attn_ldk(kt), nt = n + (has_cur ? 1 : 0);
-        const __half *kbase = reinterpret_cast<const __half *>(abuf);
-        for (int pi = at; pi < HC * nt; pi += kAttnThreads) {
-            const int g = pi / nt, j = pi - g * nt;
-            const uint4 *kr =
-                reinterpret_cast<const uint4 *>(j < n ? kbase + ((size_t)g * kt + j) * DH : S.curk + g * DH);
-            const float *qb = S.qs + (size_t)g * GL * C::QST;
-            float s0[GL], s1[GL];
-#pragma unroll
-            for (int gq = 0; gq < GL; ++gq) s0[gq] = s1[gq] = 0.f;
-#pragma unroll 4
-            for (int cs = 0; cs < C::QCH; ++cs) {
-                const int c = (cs + j) & (C::QCH - 1);
-                float kf[8];
-                h8_to_f(kr[c], kf);
-#pragma unroll
-                for (int gq = 0; gq < GL; ++gq) {
-                    const float4 qa = *reinterpret_cast<const float4 *>(qb + gq * C::QST + c * 12);
-                    const float4 qc = *reinterpret_cast<const float4 *>(qb + gq * C::QST + c * 12 + 4);
-                    s0[gq] = fmaf(qa.x, kf[0], s0[gq]);
-                    s1[gq] = fmaf(qc.x, kf[4], s1[gq]);
-                    s0[gq] = fmaf(qa.y, kf[1], s0[gq]);
-                    s1[gq] = fmaf(qc.y, kf[5], s1[gq]);
-                    s0[gq] = fmaf(qa.z, kf[2], s0[gq]);
-                    s1[gq] = fmaf(qc.z, kf[6], s1[gq]);
-                    s0[gq] = fmaf(qa.w, kf[3], s0[gq]);
-                    s1[gq] = fmaf(qc.w, kf[7], s1[gq]);
-                }
-            }
-#pragma unroll
-            for (int gq = 0; gq < GL; ++gq) S.sc[(g * GL + gq) * ldk + j] = (s0[gq] + s1[gq]) * p.attn_scale;
-        }
-    }
-    __device__ void scores(int n, bool has_cur) {
-        if (p.GL == 1) scores_t<1>(n, has_cur);
-        else if (p.GL == 2) scores_t<2>(n, has_cur);
-        else scores_t<4>(n, has_cur);
-    }
-
-    // Online softmax update over the tile's nt scores: each warp takes two q
-    // heads at a time (independent reductions interleaved); scores become
-    // probabilities, S.alpha the rescale of the older terms.
-    __device__ void softmax(int nt) {
-        const int NQ = p.hc * p.GL, ldk = attn_ldk(p.kt);
-        for (int a0 = awarp; a0 < NQ; a0 += 2 * kAttnWarps) {
-            const bool two = a0 + kAttnWarps < NQ;
-            const int a1 = two ? a0 + kAttnWarps : a0;  // (a lone head is reduced twice, written once)
-            float *s0 = S.sc + a0 * ldk, *s1 = S.sc + a1 * ldk;
-            const float mo0 = S.am[a0], mo1 = S.am[a1];
-            float m0 = -FLT_MAX, m1 = -FLT_MAX;
-            for (int j = lane; j < nt; j += 32) {
-                m0 = fmaxf(m0, s0[j]);
-                m1 = fmaxf(m1, s1[j]);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-                m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
-            }
-            const float mn0 = fmaxf(mo0, m0), mn1 = fmaxf(mo1, m1);
-            float sum0 = 0.f, sum1 = 0.f;
-            for (int j = lane; j < nt; j += 32) {
-                const float p0 = expf(s0[j] - mn0), p1 = expf(s1[j] - mn1);
-                s0[j] = p0;
-                if (two) s1[j] = p1;
-                sum0 += p0;
-                sum1 += p1;
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                sum0 += __shfl_xor_sync(0xffffffffu, sum0, o);
-                sum1 += __shfl_xor_sync(0xffffffffu, sum1, o);
-            }
-            if (lane == 0) {
-                const float al0 = (mo0 == -INFINITY) ? 0.f : expf(mo0 - mn0);
-                S.am[a0] = mn0;
-                S.al[a0] = S.al[a0] * al0 + sum0;
-                S.alpha[a0] = al0;
-                if (two) {
-                    const float al1 = (mo1 == -INFINITY) ? 0.f : expf(mo1 - mn1);
-                    S.am[a1] = mn1;
-                    S.al[a1] = S.al[a1] * al1 + sum1;
-                    S.alpha[a1] = al1;
-                }
-            }
-        }
-    }
-
-    // o = alpha * o + sum_j p_j V_j.  Thread layout: dimension pair dp =
-    // at % (DH/2) of q heads grp + NG*r (r < 4), NG = threads / (DH/2); keys
-    // outer (probabilities as float4 over 4 keys), heads inner.  With one
-    // thread group (NG = 1) the GLT q heads of a KV head share its V loads.
-    template <int GLT>
-    __device__ void pv_t(int n, bool has_cur, float2 *o) {
-        constexpr int DP = DH / 2, NG = kAttnThreads / DP;
-        const int kt = p.kt, NQ = p.hc * GLT, ldk = attn_ldk(kt);
-        const int dp = at % DP, grp = at / DP;
-        const __half2 *vb = reinterpret_cast<const __half2 *>(abuf + kAttnBuf / 2);
-        int soff[4], voff[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int a = min(grp + NG * r, NQ - 1);
-            soff[r] = a * ldk;
-            voff[r] = (a / GLT) * kt * DP + dp;
-            const float al = S.alpha[a];
-            o[r].x *= al;
-            o[r].y *= al;
-        }
+    // Split-K attention of lane-local KV head g over keys [a, a + n_prev)
+    // (plus, when cur, this step's own key and value), for its GL q heads:
+    // the warp's (acc, m, l) partial per q head goes to p.apart.
+    //
+    // Scores: S^T = K_tile q^T on the MMA, keys as M (two 16-key row blocks),
+    // the q heads as N (zero columns past GL), head_dim as K; q enters as
+    // FP16 hi + lo so that the products keep about fp32 precision (the keys
+    // are FP16 in the cache).  P.V: O^T += V^T P^T, head_dim as M (MD blocks
+    // of 16), the q heads as N, keys as K, P again as hi + lo.  Online softmax
+    // over the tiles in registers: lane 4g + t holds q heads 2t and 2t + 1
+    // of every score and accumulator fragment.
+    __device__ void head(int l, int lane_id, int g, int a, int n_prev, int T, int T_eff, bool cur) {
+        const int GL = p.GL, gq = lane >> 2, t4 = lane & 3;
+        const bool hv0 = 2 * t4 < GL, hv1 = 2 * t4 + 1 < GL;
+        const float *qkvb = p.qkv + ((size_t)l * p.NL + lane_id) * p.qkv_l;
+        // q fragments of this warp's heads (lane: q head gq, dims 2t..2t+1 and
+        // 2t+8..2t+9 of each step) and the partial dot products with this
+        // step's key (FP16-rounded, as the cache holds it)
+        float scp = 0.f;
+        uint4 *qf = S.qf[awarp];
 #pragma unroll 2
-        for (int j0 = 0; j0 < n; j0 += 4) {
-            float4 pr[4];
+        for (int ks = 0; ks < KS; ++ks) {
+            float2 x = make_float2(0.f, 0.f), y = x;
+            if (gq < GL) {
+                const float *qh = qkvb + ((size_t)g * GL + gq) * DH + 16 * ks + 2 * t4;
+                x = __ldcg(reinterpret_cast<const float2 *>(qh));
+                y = __ldcg(reinterpret_cast<const float2 *>(qh + 8));
+                if (cur) {
+                    const float *kh = qkvb + ((size_t)p.HQ_L + g) * DH + 16 * ks + 2 * t4;
+                    const float2 k0 = __ldcg(reinterpret_cast<const float2 *>(kh));
+                    const float2 k1 = __ldcg(reinterpret_cast<const float2 *>(kh + 8));
+                    scp = fmaf(x.x, __half2float(__float2half_rn(k0.x)), scp);
+                    scp = fmaf(x.y, __half2float(__float2half_rn(k0.y)), scp);
+                    scp = fmaf(y.x, __half2float(__float2half_rn(k1.x)), scp);
+                    scp = fmaf(y.y, __half2float(__float2half_rn(k1.y)), scp);
+                }
+            }
+            uint4 f;
+            split_h2(x.x, x.y, f.x, f.z);
+            split_h2(y.x, y.y, f.y, f.w);
+            qf[ks * 32 + lane] = f;
+        }
+        // this step's scores of q heads 2t and 2t + 1 (lanes 8t and 8t + 4 hold them)
+        scp += __shfl_xor_sync(0xffffffffu, scp, 1);
+        scp += __shfl_xor_sync(0xffffffffu, scp, 2);
+        const float sc0 = __shfl_sync(0xffffffffu, scp, 8 * t4) * p.attn_scale;
+        const float sc1 = __shfl_sync(0xffffffffu, scp, (8 * t4 + 4) & 31) * p.attn_scale;
+        __syncwarp();
+
+        float acc[MD][4];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) pr[r] = *reinterpret_cast<const float4 *>(S.sc + soff[r] + j0);
+        for (int md = 0; md < MD; ++md) acc[md][0] = acc[md][1] = acc[md][2] = acc[md][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        const uint32_t kb = smem_u32(abuf + (size_t)awarp * KT * RB);
+        const uint32_t vb = smem_u32(abuf + kAttnBuf / 2 + (size_t)awarp * KT * RB);
+        // ldmatrix row addresses: K as A (key rows, 8 dims per matrix), V as A^T
+        const uint32_t ka = kb + (uint32_t)(((lane & 7) + ((lane >> 3) & 1) * 8) * RB + (lane >> 4) * 16);
+        const uint32_t va = vb + (uint32_t)(((lane & 7) + (lane >> 4) * 8) * RB + ((lane >> 3) & 1) * 16);
+
+        for (int t = 0; t < T_eff; ++t) {
+            const int n = t < T ? min(KT, n_prev - t * KT) : 0;
+            const int nn = t + 1 < T ? min(KT, n_prev - (t + 1) * KT) : 0;
+            const bool has_cur = cur && t == T_eff - 1;
+            if (t < T) wait_kv(&S.abarK[awarp], kwait);
+            const uint64_t t_sc = (p.trace && at == 0) ? global_timer_ns() : 0;
+            float sh[2][4], sl[2][4];
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                if (j0 + jj < n) {
-                    float2 v;
+            for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        if (NG > 1 || r % GLT == 0) v = __half22float2(vb[voff[r] + (j0 + jj) * DP]);
-                        const float pj = jj == 0 ? pr[r].x : jj == 1 ? pr[r].y : jj == 2 ? pr[r].z : pr[r].w;
-                        o[r].x = fmaf(pj, v.x, o[r].x);
-                        o[r].y = fmaf(pj, v.y, o[r].y);
+                for (int r = 0; r < 4; ++r) sh[mt][r] = sl[mt][r] = 0.f;
+            if (n > 0) {
+#pragma unroll 2
+                for (int ks = 0; ks < KS; ++ks) {
+                    const uint4 f = qf[ks * 32 + lane];
+                    uint32_t fa[4];
+                    ldsm_x4(ka + ks * 32, fa);
+                    mma_16816(sh[0], fa, f.x, f.y);
+                    mma_16816(sl[0], fa, f.z, f.w);
+                    if (n > 16) {
+                        ldsm_x4(ka + 16 * RB + ks * 32, fa);
+                        mma_16816(sh[1], fa, f.x, f.y);
+                        mma_16816(sl[1], fa, f.z, f.w);
                     }
                 }
             }
-        }
-        if (has_cur) {
-            const __half2 *cv = reinterpret_cast<const __half2 *>(S.curv);
+            __syncwarp();  // every lane's K reads are done: the buffer may refill
+            if (p.trace && at == 0) S.a_tsc += global_timer_ns() - t_sc;
+            if (nn > 0) issue(false, l, lane_id, g, a + (t + 1) * KT, nn);
+
+            // online softmax: s[mt][r] is key 16 mt + gq + 8 (r / 2), q head 2t + r % 2
+            float s[2][4];
+            float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int a = min(grp + NG * r, NQ - 1);
-                const float pj = S.sc[soff[r] + n];
-                const float2 v = __half22float2(cv[(a / GLT) * DP + dp]);
-                o[r].x = fmaf(pj, v.x, o[r].x);
-                o[r].y = fmaf(pj, v.y, o[r].y);
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const bool valid = 16 * mt + gq + 8 * (r >> 1) < n && ((r & 1) ? hv1 : hv0);
+                    s[mt][r] = valid ? (sh[mt][r] + sl[mt][r]) * p.attn_scale : -INFINITY;
+                    if (r & 1) mx1 = fmaxf(mx1, s[mt][r]);
+                    else mx0 = fmaxf(mx0, s[mt][r]);
+                }
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            if (has_cur) {
+                if (hv0) mx0 = fmaxf(mx0, sc0);
+                if (hv1) mx1 = fmaxf(mx1, sc1);
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float ms0 = (mn0 == -INFINITY) ? 0.f : mn0, ms1 = (mn1 == -INFINITY) ? 0.f : mn1;
+            const float al0 = expf(m0 - ms0), al1 = expf(m1 - ms1);
+            float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    s[mt][r] = expf(s[mt][r] - ((r & 1) ? ms1 : ms0));
+                    if (r & 1) sum1 += s[mt][r];
+                    else sum0 += s[mt][r];
+                }
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                sum0 += __shfl_xor_sync(0xffffffffu, sum0, o);
+                sum1 += __shfl_xor_sync(0xffffffffu, sum1, o);
+            }
+            const float pc0 = (has_cur && hv0) ? expf(sc0 - ms0) : 0.f;
+            const float pc1 = (has_cur && hv1) ? expf(sc1 - ms1) : 0.f;
+            l0 = l0 * al0 + sum0 + pc0;
+            l1 = l1 * al1 + sum1 + pc1;
+            m0 = mn0;
+            m1 = mn1;
+#pragma unroll
+            for (int md = 0; md < MD; ++md) {
+                acc[md][0] *= al0;
+                acc[md][2] *= al0;
+                acc[md][1] *= al1;
+                acc[md][3] *= al1;
+            }
+
+            if (t < T) wait_kv(&S.abarV[awarp], vwait);
+            const uint64_t t_pv = (p.trace && at == 0) ? global_timer_ns() : 0;
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                if (16 * kk < n) {
+                    // P^T fragment of keys 16 kk + (2t, 2t + 1, 2t + 8, 2t + 9), q head gq:
+                    // key 16 kk + r, head h sits in lane 4 (r % 8) + h / 2, s[kk][2 (r / 8) + h % 2]
+                    const int src0 = 8 * t4 + (gq >> 1), src1 = src0 + 4;
+                    const bool odd = gq & 1, hv = gq < GL;
+                    const float x0 = __shfl_sync(0xffffffffu, s[kk][0], src0);
+                    const float x1 = __shfl_sync(0xffffffffu, s[kk][1], src0);
+                    const float x2 = __shfl_sync(0xffffffffu, s[kk][0], src1);
+                    const float x3 = __shfl_sync(0xffffffffu, s[kk][1], src1);
+                    const float y0 = __shfl_sync(0xffffffffu, s[kk][2], src0);
+                    const float y1 = __shfl_sync(0xffffffffu, s[kk][3], src0);
+                    const float y2 = __shfl_sync(0xffffffffu, s[kk][2], src1);
+                    const float y3 = __shfl_sync(0xffffffffu, s[kk][3], src1);
+                    const float p00 = hv ? (odd ? x1 : x0) : 0.f, p01 = hv ? (odd ? x3 : x2) : 0.f;
+                    const float p10 = hv ? (odd ? y1 : y0) : 0.f, p11 = hv ? (odd ? y3 : y2) : 0.f;
+                    uint32_t b0h, b0l, b1h, b1l;
+                    split_h2(p00, p01, b0h, b0l);
+                    split_h2(p10, p11, b1h, b1l);
+#pragma unroll
+                    for (int md = 0; md < MD; ++md) {
+                        uint32_t fa[4];
+                        ldsm_x4_trans(va + kk * 16 * RB + md * 32, fa);
+                        mma_16816(acc[md], fa, b0h, b1h);
+                        mma_16816(acc[md], fa, b0l, b1l);
+                    }
+                }
+            }
+            if (has_cur) {  // this step's value, FP16-rounded as the cache holds it
+                const float *vh = qkvb + ((size_t)p.HQ_L + p.HKV_L + g) * DH + gq;
+#pragma unroll
+                for (int md = 0; md < MD; ++md) {
+                    const float v0 = __half2float(__float2half_rn(__ldcg(vh + 16 * md)));
+                    const float v8 = __half2float(__float2half_rn(__ldcg(vh + 16 * md + 8)));
+                    acc[md][0] = fmaf(pc0, v0, acc[md][0]);
+                    acc[md][1] = fmaf(pc1, v0, acc[md][1]);
+                    acc[md][2] = fmaf(pc0, v8, acc[md][2]);
+                    acc[md][3] = fmaf(pc1, v8, acc[md][3]);
+                }
+            }
+            __syncwarp();  // every lane's V reads are done
+            if (p.trace && at == 0) S.a_tpv += global_timer_ns() - t_pv;
+            if (nn > 0) issue(true, l, lane_id, g, a + (t + 1) * KT, nn);
+        }
+        // scratch read back within this layer: kept in L2 ahead of the weight stream
+        float *dst = p.apart + (((size_t)l * p.n_cta + cta) * p.HQ_L + (size_t)g * GL) * (DH + 2);
+        const uint64_t keep = policy_evict_last();
+        if (ok(l < p.L && (g + 1) * GL <= p.HQ_L, SITE_ATTN_PART, g)) {
+            float *d0 = dst + (size_t)(2 * t4) * (DH + 2), *d1 = d0 + (DH + 2);
+#pragma unroll
+            for (int md = 0; md < MD; ++md) {
+                if (hv0) {
+                    st_hint(d0 + 16 * md + gq, acc[md][0], keep);
+                    st_hint(d0 + 16 * md + gq + 8, acc[md][2], keep);
+                }
+                if (hv1) {
+                    st_hint(d1 + 16 * md + gq, acc[md][1], keep);
+                    st_hint(d1 + 16 * md + gq + 8, acc[md][3], keep);
+                }
+            }
+            if (gq == 0) {
+                if (hv0) {
+                    st_hint(d0 + DH, m0, keep);
+                    st_hint(d0 + DH + 1, l0, keep);
+                }
+                if (hv1) {
+                    st_hint(d1 + DH, m1, keep);
+                    st_hint(d1 + DH + 1, l1, keep);
+                }
             }
         }
-    }
-    __device__ void pv(int n, bool has_cur, float2 *o) {
-        if (p.GL == 1) pv_t<1>(n, has_cur, o);
-        else if (p.GL == 2) pv_t<2>(n, has_cur, o);
-        else pv_t<4>(n, has_cur, o);
     }
 
     __device__ void attention(int l) {
         const CtaPlan cp = p.cta[cta];
-        const int S_ = cp.S, GL = p.GL, HC = p.hc, kt = p.kt, NQ = HC * GL, items = NQ * DH;
-        constexpr int DP = DH / 2, NG = kAttnThreads / DP;
+        const int S_ = cp.S, HC = p.hc;
         int a, b;
         attn_range(pos(), p.window[l], cp.k, S_, &a, &b);
         const bool last = (cp.k == S_ - 1);
-        const int n_prev = b - a, T = (n_prev + kt - 1) / kt, T_eff = (last && T == 0) ? 1 : T;
-        // earlier keys do not depend on this step: fetch the first tile before
+        const int n_prev = b - a, T = (n_prev + KT - 1) / KT, T_eff = (last && T == 0) ? 1 : T;
+        const bool mine = awarp < HC;  // this warp has a KV head in every chunk
+        // earlier keys do not depend on this step: fetch the first tiles before
         // waiting for the lane's QKV rows
-        if (T > 0) {
-            issue_k(l, cp.lane, 0, a, min(kt, n_prev));
-            issue_v(l, cp.lane, 0, a, min(kt, n_prev));
+        if (mine && T > 0) {
+            issue(false, l, cp.lane, awarp, a, min(KT, n_prev));
+            issue(true, l, cp.lane, awarp, a, min(KT, n_prev));
         }
         wait_geq(&p.barA[l * p.NL + cp.lane], ep() * (uint32_t)S_);
-        const float *qkvb = p.qkv + ((size_t)l * p.NL + cp.lane) * p.qkv_l;
-        for (int g0 = 0; g0 < p.HKV_L; g0 += HC) {
-            if (g0 > 0 && T > 0) {  // the buffers are free since the previous chunk's last barrier
-                issue_k(l, cp.lane, g0, a, min(kt, n_prev));
-                issue_v(l, cp.lane, g0, a, min(kt, n_prev));
+        for (int g0 = 0; g0 < p.HKV_L && mine; g0 += HC) {
+            if (g0 > 0 && T > 0) {  // the warp's buffers are free since its previous head
+                issue(false, l, cp.lane, g0 + awarp, a, min(KT, n_prev));
+                issue(true, l, cp.lane, g0 + awarp, a, min(KT, n_prev));
             }
-            // one round trip: q of the chunk's heads and (last CTA) this step's k, v
-            if (at < NQ) {
-                S.am[at] = -INFINITY;
-                S.al[at] = 0.f;
-            }
-            for (int o = at; o < items; o += kAttnThreads)
-                S.qs[(o / DH) * C::QST + (o % DH) / 8 * 12 + o % 8] = __ldcg(qkvb + (size_t)g0 * GL * DH + o);
-            if (last) {
-                for (int o = at; o < HC * DH; o += kAttnThreads) {
-                    S.curk[o] = __float2half_rn(__ldcg(qkvb + (size_t)(p.HQ_L + g0) * DH + o));
-                    S.curv[o] = __float2half_rn(__ldcg(qkvb + (size_t)(p.HQ_L + p.HKV_L + g0) * DH + o));
-                }
-            }
-            attn_sync();
-            float2 acc[4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r) acc[r] = make_float2(0.f, 0.f);
-            for (int t = 0; t < T_eff; ++t) {
-                const int n = t < T ? min(kt, n_prev - t * kt) : 0, nn = t + 1 < T ? min(kt, n_prev - (t + 1) * kt) : 0;
-                const bool has_cur = last && t == T_eff - 1;
-                if (t < T) wait_kv(&S.abarK, kwait);
-                const uint64_t t_sc = (p.trace && at == 0) ? global_timer_ns() : 0;
-                scores(n, has_cur);
-                attn_sync();  // scores visible; the K half of the buffer is free
-                if (p.trace && at == 0) S.a_tsc += global_timer_ns() - t_sc;
-                if (nn > 0) issue_k(l, cp.lane, g0, a + (t + 1) * kt, nn);
-                softmax(n + (has_cur ? 1 : 0));
-                attn_sync();  // probabilities and rescale factors visible
-                if (t < T) wait_kv(&S.abarV, vwait);
-                const uint64_t t_pv = (p.trace && at == 0) ? global_timer_ns() : 0;
-                pv(n, has_cur, acc);
-                attn_sync();  // the V half and the scores are free again
-                if (p.trace && at == 0) S.a_tpv += global_timer_ns() - t_pv;
-                if (nn > 0) issue_v(l, cp.lane, g0, a + (t + 1) * kt, nn);
-            }
-            // scratch read back within this layer: kept in L2 ahead of the weight stream
-            float *dst = p.apart + (((size_t)l * p.n_cta + cta) * p.HQ_L + (size_t)g0 * GL) * (DH + 2);
-            const uint64_t keep = policy_evict_last();
-            const bool part_ok = ok(l < p.L && g0 * GL + NQ <= p.HQ_L && NQ <= kMaxChunkHeads, SITE_ATTN_PART, g0);
-            if (part_ok) {
-                const int dp = at % DP, grp = at / DP;
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int ah = grp + NG * r;
-                    if (ah < NQ) {
-                        st_hint(dst + ah * (DH + 2) + 2 * dp, acc[r].x, keep);
-                        st_hint(dst + ah * (DH + 2) + 2 * dp + 1, acc[r].y, keep);
-                    }
-                }
-            }
-            if (at < NQ && part_ok) {
-                st_hint(dst + at * (DH + 2) + DH, S.am[at], keep);
-                st_hint(dst + at * (DH + 2) + DH + 1, S.al[at], keep);
-            }
-            attn_sync();
+            head(l, cp.lane, g0 + awarp, a, n_prev, T, T_eff, last);
         }
+        attn_sync();
         if (at == 0 && !S.abort_) {
             __threadfence();
             atomicAdd(&p.barB[l * p.NL + cp.lane], 1u);
@@ -1225,15 +1219,15 @@ struct Attention {
             if (S.stop_a) break;
             deadline = global_timer_ns() + p.timeout_ns;
         }
-        // after an error, let the last K and V tiles thread 0 issued land
+        // after an error, let the last K and V tiles this warp issued land
         // (tiles complete in order, so the last one's phase covers them all)
-        if (at == 0 && S.abort_) {
+        if (lane == 0 && S.abort_) {
             const uint64_t dl = global_timer_ns() + 1000000000ull;
             if (kiss > 0)
-                while (!mbar_try_wait(&S.abarK, (kiss - 1) & 1u) && global_timer_ns() < dl) {
+                while (!mbar_try_wait(&S.abarK[awarp], (kiss - 1) & 1u) && global_timer_ns() < dl) {
                 }
             if (viss > 0)
-                while (!mbar_try_wait(&S.abarV, (viss - 1) & 1u) && global_timer_ns() < dl) {
+                while (!mbar_try_wait(&S.abarV[awarp], (viss - 1) & 1u) && global_timer_ns() < dl) {
                 }
         }
     }
@@ -1541,13 +1535,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     uint8_t *abuf = base + (size_t)C::STAGES * kStageBytes;
     Smem<D, DH> &S = *reinterpret_cast<Smem<D, DH> *>(abuf + kAttnBuf);
     const uint64_t deadline = global_timer_ns() + p.timeout_ns;
+    // KV tile rows past a tile's keys enter the MMAs with zero weights: start
+    // them finite (later they hold earlier keys of the cache)
+    for (int i = threadIdx.x; i < kAttnBuf / 16; i += kThreads)
+        reinterpret_cast<uint4 *>(abuf)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_shared();
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::STAGES; ++i) {
             mbar_init(&S.full[i], 1);
             mbar_init(&S.empty[i], kConsWarps);
         }
-        mbar_init(&S.abarK, 1);
-        mbar_init(&S.abarV, 1);
+        for (int w = 0; w < kAttnWarps; ++w) {
+            mbar_init(&S.abarK[w], 1);
+            mbar_init(&S.abarV[w], 1);
+        }
         mbar_init(&S.hbar, 1);
         S.abort_ = 0;
         S.prod_done = 0;

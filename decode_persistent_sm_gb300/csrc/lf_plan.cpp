@@ -58,19 +58,19 @@ lf_status derive_shape(const lf_config &c, Shape *sh) {
     // summed with the others at once); the own-lane path is used for d > 0.
     s.own = c.own_lane_immediate != 0 && c.dtp_delay > 0;
     const bool kern = (s.D == 4096 && s.DH == 128) || (s.D == 256 && s.DH == 32);
-    // Attention: the q heads of a lane-local KV head times head_dim must tile
-    // the 256 consumer threads.
-    const bool gl_ok = (s.GL == 1 || s.GL == 2 || s.GL == 4) && s.GL * s.DH <= 256;
+    // Attention: each attention warp takes one lane-local KV head of a chunk
+    // (its q heads are the N = 8 side of the warp's MMAs, its keys the M side
+    // in tiles of kAttnKT), so a chunk is two KV heads, or one when the lane's
+    // count is odd.
+    const bool gl_ok = (s.GL == 1 || s.GL == 2 || s.GL == 4) && s.GL * s.DH <= 256 && s.DH % 16 == 0;
     if (!kern || !gl_ok) return LF_ERR_UNSUPPORTED;
-    s.HC = s.HKV_L;
-    while (s.HC * s.GL * s.DH > kConsThreads) s.HC /= 2;
-    if (s.HC < 1 || s.HKV_L % s.HC) return LF_ERR_UNSUPPORTED;
-    s.KT = (kAttnBuf / 2) / (s.HC * s.DH * 2);
+    s.HC = (s.HKV_L % kAttnWarps == 0) ? kAttnWarps : 1;
+    s.KT = kAttnKT;
+    if (2 * kAttnWarps * s.KT * attn_row_bytes(s.DH) > kAttnBuf) return LF_ERR_UNSUPPORTED;
     // Slot u % PS may be rewritten by sub-block u + PS once every CTA has
     // added R[u], which happens before sub-block u + 1 + 2d; PS = 2d + 4
     // keeps the partials few enough to stay in L2.
     s.PS = std::min(2 * s.L, 2 * s.delay + 4);
-    if (s.KT < 1 || s.HC * s.GL * attn_ldk(s.KT) > kAttnScores) return LF_ERR_UNSUPPORTED;
     return LF_OK;
 }
 

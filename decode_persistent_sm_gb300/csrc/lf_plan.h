@@ -18,8 +18,8 @@ struct Shape {
     int F_L;    // FFN units per lane
     int NP;     // QKV row pairs per lane: (HQ_L + 2*HKV_L) * DH/2
     int NO;     // o_proj input columns per lane: HQ_L * DH
-    int HC;     // KV heads processed together in attention (HC * GL * DH <= 512)
-    int KT;     // keys per attention tile: K and V of HC heads fill one stage
+    int HC;     // KV heads processed together in attention: one per attention warp (1 or 2)
+    int KT;     // keys per attention tile (kAttnKT)
     int PS;     // lane-sum partial slots (sub-block u uses slot u % PS)
     bool own;   // own-lane-immediate reading (with a delay > 0)
     std::vector<int> kv_first;  // per lane: first global KV head it reads
