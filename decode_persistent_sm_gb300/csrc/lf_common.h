@@ -49,11 +49,13 @@ constexpr int kThreads = kConsThreads + kAttnThreads + 64;
 constexpr int kStageBytes = 32768;
 constexpr int kStages = 4;
 // Attention KV tiles: per attention warp (one KV head each) a K and a V tile
-// of kAttnKT keys, every key row padded by 16 bytes so that the eight rows of
-// an 8x8 matrix load fall in eight different bank groups.
+// of kAttnKT keys in kAttnGroups groups of 4 consecutive keys, one bulk copy
+// per group, group q at q * attn_group_bytes: the 16-byte skew puts the 8
+// rows of an 8x8 matrix load, one key from each group, in 8 bank groups.
 constexpr int kAttnKT = 32;
-LF_HD constexpr int attn_row_bytes(int dh) { return 2 * dh + 16; }
-constexpr int kAttnBuf = 2 * kAttnWarps * kAttnKT * (2 * 128 + 16);  // K tiles, then V tiles
+constexpr int kAttnGroups = kAttnKT / 4;
+LF_HD constexpr int attn_group_bytes(int dh) { return 4 * 2 * dh + 16; }
+constexpr int kAttnBuf = 2 * kAttnWarps * kAttnGroups * (4 * 2 * 128 + 16);  // K tiles, then V tiles
 constexpr int kMaxCtas = 160;      // helper buffer rows (one 128-byte piece per CTA)
 constexpr int kRChunk = 32;        // floats per chunk of the delayed lane sum
 constexpr int kMaxUnitsPerCta = 256;

@@ -44,11 +44,12 @@ struct Cfg {
     static_assert(kRedRows % RPT == 0, "reduction block");
     static constexpr int GLMAX = 256 / DH < kMaxGroup ? 256 / DH : kMaxGroup;
     // attention: head_dim in 16-wide MMA steps; per warp a K and a V tile of
-    // kAttnKT padded key rows
+    // kAttnGroups skewed groups of 4 key rows
     static constexpr int KS = DH / 16;
-    static constexpr int RB = attn_row_bytes(DH);
-    static_assert(DH % 16 == 0 && kAttnKT == 32, "attention MMA tiling");
-    static_assert(2 * kAttnWarps * kAttnKT * RB <= kAttnBuf && RB % 16 == 0, "attention tile buffer");
+    static constexpr int GB = attn_group_bytes(DH);
+    static constexpr int TB = kAttnGroups * GB;  // bytes of one tile
+    static_assert(DH % 16 == 0 && kAttnKT == 32 && kAttnGroups == 8, "attention MMA tiling");
+    static_assert(2 * kAttnWarps * TB <= kAttnBuf && GB % 128 == 16, "attention tile buffer");
 };
 
 template <int D, int DH>
@@ -801,7 +802,7 @@ struct Streamer {
 template <int D, int DH>
 struct Attention {
     using C = Cfg<D, DH>;
-    static constexpr int KT = kAttnKT, RB = C::RB, KS = C::KS, MD = DH / 16;
+    static constexpr int KT = kAttnKT, GB = C::GB, TB = C::TB, KS = C::KS, MD = DH / 16, RW = 2 * DH;
     const KParams &p;
     Smem<D, DH> &S;
     uint8_t *abuf;
@@ -841,8 +842,9 @@ struct Attention {
     }
 
     // This warp's K (or V) tile: keys [j0, j0 + n) of lane-local KV head g
-    // of layer l, key j0 + i copied by lane i into padded row i.  The warp's
-    // barrier counts the bytes; at most one tile of each kind is in flight.
+    // of layer l, keys j0 + 4q .. j0 + 4q + 3 copied by lane q into group q.
+    // The warp's barrier counts the bytes; at most one tile of each kind is
+    // in flight.
     __device__ void issue(bool v, int l, int lane_id, int g, int j0, int n) {
         uint32_t &iss = v ? viss : kiss;
         const uint32_t waited = v ? vwait : kwait;
@@ -857,8 +859,10 @@ struct Attention {
         if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)n * DH * 2);
         __syncwarp();
         const size_t head = (((size_t)lane_id * p.L + l) * p.HKV_L + g) * p.ctx;
-        uint8_t *dst = abuf + (v ? kAttnBuf / 2 : 0) + (size_t)awarp * KT * RB;
-        if (lane < n) bulk_g2s(dst + lane * RB, (v ? p.vc : p.kc) + (head + j0 + lane) * DH, DH * 2, bar);
+        uint8_t *dst = abuf + (v ? kAttnBuf / 2 : 0) + (size_t)awarp * TB;
+        const int cnt = min(4, n - 4 * lane);
+        if (lane < kAttnGroups && cnt > 0)
+            bulk_g2s(dst + lane * GB, (v ? p.vc : p.kc) + (head + j0 + 4 * lane) * DH, (uint32_t)cnt * RW, bar);
         ++iss;
     }
 
@@ -877,7 +881,9 @@ struct Attention {
     // (plus, when cur, this step's own key and value), for its GL q heads:
     // the warp's (acc, m, l) partial per q head goes to p.apart.
     //
-    // Scores: S^T = K_tile q^T on the MMA, keys as M (two 16-key row blocks),
+    // Scores: S^T = K_tile q^T on the MMA, keys as M (two 16-row blocks: row
+    // r of block b is key 4 (r % 8) + 2 b + r / 8 of the tile, so that the 8
+    // rows of a matrix load come from the 8 key groups),
     // the q heads as N (zero columns past GL), head_dim as K; q enters as
     // FP16 hi + lo so that the products keep about fp32 precision (the keys
     // are FP16 in the cache).  P.V: O^T += V^T P^T, head_dim as M (MD blocks
@@ -926,11 +932,13 @@ struct Attention {
 #pragma unroll
         for (int md = 0; md < MD; ++md) acc[md][0] = acc[md][1] = acc[md][2] = acc[md][3] = 0.f;
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-        const uint32_t kb = smem_u32(abuf + (size_t)awarp * KT * RB);
-        const uint32_t vb = smem_u32(abuf + kAttnBuf / 2 + (size_t)awarp * KT * RB);
-        // ldmatrix row addresses: K as A (key rows, 8 dims per matrix), V as A^T
-        const uint32_t ka = kb + (uint32_t)(((lane & 7) + ((lane >> 3) & 1) * 8) * RB + (lane >> 4) * 16);
-        const uint32_t va = vb + (uint32_t)(((lane & 7) + (lane >> 4) * 8) * RB + ((lane >> 3) & 1) * 16);
+        const uint32_t kb = smem_u32(abuf + (size_t)awarp * TB);
+        const uint32_t vb = smem_u32(abuf + kAttnBuf / 2 + (size_t)awarp * TB);
+        // ldmatrix row addresses: K as A (key rows, 8 dims per matrix), V as
+        // A^T (8 keys per matrix); the lane's key is 4 (lane % 8) + its block
+        // offset (row / 8 for K, the k half for V), + 2 per further block
+        const uint32_t ka = kb + (uint32_t)((lane & 7) * GB + ((lane >> 3) & 1) * RW + (lane >> 4) * 16);
+        const uint32_t va = vb + (uint32_t)((lane & 7) * GB + (lane >> 4) * RW + ((lane >> 3) & 1) * 16);
 
         for (int t = 0; t < T_eff; ++t) {
             const int n = t < T ? min(KT, n_prev - t * KT) : 0;
@@ -951,8 +959,8 @@ struct Attention {
                     ldsm_x4(ka + ks * 32, fa);
                     mma_16816(sh[0], fa, f.x, f.y);
                     mma_16816(sl[0], fa, f.z, f.w);
-                    if (n > 16) {
-                        ldsm_x4(ka + 16 * RB + ks * 32, fa);
+                    if (n > 2) {  // (block 1 starts at key 2)
+                        ldsm_x4(ka + 2 * RW + ks * 32, fa);
                         mma_16816(sh[1], fa, f.x, f.y);
                         mma_16816(sl[1], fa, f.z, f.w);
                     }
@@ -962,14 +970,14 @@ struct Attention {
             if (p.trace && at == 0) S.a_tsc += global_timer_ns() - t_sc;
             if (nn > 0) issue(false, l, lane_id, g, a + (t + 1) * KT, nn);
 
-            // online softmax: s[mt][r] is key 16 mt + gq + 8 (r / 2), q head 2t + r % 2
+            // online softmax: s[mt][r] is key 4 gq + 2 mt + r / 2, q head 2t + r % 2
             float s[2][4];
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
-                    const bool valid = 16 * mt + gq + 8 * (r >> 1) < n && ((r & 1) ? hv1 : hv0);
+                    const bool valid = 4 * gq + 2 * mt + (r >> 1) < n && ((r & 1) ? hv1 : hv0);
                     s[mt][r] = valid ? (sh[mt][r] + sl[mt][r]) * p.attn_scale : -INFINITY;
                     if (r & 1) mx1 = fmaxf(mx1, s[mt][r]);
                     else mx0 = fmaxf(mx0, s[mt][r]);
@@ -1018,9 +1026,10 @@ struct Attention {
             const uint64_t t_pv = (p.trace && at == 0) ? global_timer_ns() : 0;
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
-                if (16 * kk < n) {
-                    // P^T fragment of keys 16 kk + (2t, 2t + 1, 2t + 8, 2t + 9), q head gq:
-                    // key 16 kk + r, head h sits in lane 4 (r % 8) + h / 2, s[kk][2 (r / 8) + h % 2]
+                if (2 * kk < n) {
+                    // P^T fragment of block kk's rows 2t, 2t + 1, 2t + 8, 2t + 9 (the same
+                    // keys as the scores' row block kk), q head gq: row r, head h sits in
+                    // lane 4 (r % 8) + h / 2, s[kk][2 (r / 8) + h % 2]
                     const int src0 = 8 * t4 + (gq >> 1), src1 = src0 + 4;
                     const bool odd = gq & 1, hv = gq < GL;
                     const float x0 = __shfl_sync(0xffffffffu, s[kk][0], src0);
@@ -1039,7 +1048,7 @@ struct Attention {
 #pragma unroll
                     for (int md = 0; md < MD; ++md) {
                         uint32_t fa[4];
-                        ldsm_x4_trans(va + kk * 16 * RB + md * 32, fa);
+                        ldsm_x4_trans(va + kk * 2 * RW + md * 32, fa);
                         mma_16816(acc[md], fa, b0h, b1h);
                         mma_16816(acc[md], fa, b0l, b1l);
                     }

@@ -66,7 +66,7 @@ lf_status derive_shape(const lf_config &c, Shape *sh) {
     if (!kern || !gl_ok) return LF_ERR_UNSUPPORTED;
     s.HC = (s.HKV_L % kAttnWarps == 0) ? kAttnWarps : 1;
     s.KT = kAttnKT;
-    if (2 * kAttnWarps * s.KT * attn_row_bytes(s.DH) > kAttnBuf) return LF_ERR_UNSUPPORTED;
+    if (2 * kAttnWarps * kAttnGroups * attn_group_bytes(s.DH) > kAttnBuf) return LF_ERR_UNSUPPORTED;
     // Slot u % PS may be rewritten by sub-block u + PS once every CTA has
     // added R[u], which happens before sub-block u + 1 + 2d; PS = 2d + 4
     // keeps the partials few enough to stay in L2.
