@@ -492,7 +492,7 @@ static lf_status enqueue_steps(lf_engine *e, int32_t token, const int32_t *token
     k.cand_v = e->cand_v; k.cand_i = e->cand_i; k.logits = e->logits;
     k.argmax = argmax_dst;
     k.err = e->status + 4;
-    k.trace = n_tokens == 1 ? e->trace : nullptr;  // the trace records one step
+    k.trace = e->trace;  // (with several tokens, the last one's record remains)
 
     cudaError_t err = lf::launch_decode(k, e->stream);
     e->skip_cta = -1;

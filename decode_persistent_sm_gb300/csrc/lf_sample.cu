@@ -10,12 +10,17 @@
 // kept index, in index order, whose running kept mass exceeds u times the
 // kept mass.  T == 0 is greedy (lowest index among equal maxima).
 //
-// One CTA of 1024 threads: the probabilities live in shared memory; tau is
-// found by bisection on the fp32 bit pattern (the mass above a threshold only
-// changes at the p values, and positive floats order like their bits), each
-// step one pass over the vocabulary and a block sum by a fixed tree (the same
-// order every time); the crossing is found by the warp that owns it, walking
-// its contiguous index range 32 tokens at a time with a warp scan.
+// One CTA of 1024 threads: the probabilities live in shared memory (and in
+// registers, 32 per thread, when the vocabulary fits); tau is found by
+// bisection on the fp32 bit pattern (the mass above a threshold only changes
+// at the p values, and positive floats order like their bits).  Each mass is
+// a per-thread sum in index order and a block sum by a fixed tree (the same
+// order every time), so the masses grow monotonically with the kept set and
+// the bisection's path is fixed; one pass over the values evaluates two
+// steps at once (the midpoint and both candidates for the next midpoint, one
+// block reduction of three sums).  The crossing is found by the warp that
+// owns it, walking its contiguous index range 32 tokens at a time with a
+// warp scan.
 #include <cuda_runtime.h>
 
 #include <cfloat>
@@ -28,6 +33,7 @@ namespace lf {
 namespace {
 
 constexpr int SMP_THREADS = 1024;
+constexpr int SMP_REG = 32;  // probabilities per thread held in registers (vocabulary <= SMP_REG * SMP_THREADS)
 
 __device__ __forceinline__ void philox4x32_10(uint32_t c[4], uint32_t k0, uint32_t k1) {
 #pragma unroll
@@ -76,6 +82,66 @@ __device__ float bsum(float v, float *red, float *bcast) {
     return *bcast;
 }
 
+// Three block sums at once, each by the same tree as bsum.
+__device__ float3 bsum3(float a, float b, float c, float3 *red, float3 *bcast) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, o);
+        b += __shfl_xor_sync(0xffffffffu, b, o);
+        c += __shfl_xor_sync(0xffffffffu, c, o);
+    }
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = make_float3(a, b, c);
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float3 t = red[threadIdx.x];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            t.x += __shfl_xor_sync(0xffffffffu, t.x, o);
+            t.y += __shfl_xor_sync(0xffffffffu, t.y, o);
+            t.z += __shfl_xor_sync(0xffffffffu, t.z, o);
+        }
+        if (threadIdx.x == 0) *bcast = t;
+    }
+    __syncthreads();
+    return *bcast;
+}
+
+// Bisection for the largest bit pattern lo with mass(lo) >= target, two
+// steps per pass: the midpoint m1 of [lo, hi] and the midpoints of [lo,
+// m1 - 1] and [m1, hi], whichever the first step leaves.  sums(m1, ma, mb,
+// &s1, &sa, &sb) gives this thread's partial masses in index order.
+template <class Sums>
+__device__ void bisect(uint32_t &lo, uint32_t &hi, float target, float &kept, bool &have, Sums sums, float3 *red3,
+                       float3 *bc3) {
+    int round = 0;
+    while (lo < hi) {
+        const uint32_t m1 = lo + (hi - lo + 1) / 2;
+        const uint32_t ma = lo + (m1 - lo) / 2;      // the next midpoint if mass(m1) < target
+        const uint32_t mb = m1 + (hi - m1 + 1) / 2;  // the next midpoint if mass(m1) >= target
+        float s1 = 0.f, sa = 0.f, sb = 0.f;
+        sums(m1, ma, mb, s1, sa, sb);
+        const float3 M = bsum3(s1, sa, sb, red3, &bc3[round++ & 1]);
+        const bool up = M.x >= target;
+        if (up) {
+            lo = m1;
+            kept = M.x;
+            have = true;
+        } else {
+            hi = m1 - 1;
+        }
+        if (lo < hi) {  // the second step's midpoint is mb (up) or ma
+            const float mass = up ? M.z : M.y;
+            if (mass >= target) {
+                lo = up ? mb : ma;
+                kept = mass;
+                have = true;
+            } else {
+                hi = (up ? mb : ma) - 1;
+            }
+        }
+    }
+}
+
 __global__ void __launch_bounds__(SMP_THREADS, 1)
     sample_kernel(const float *__restrict__ logits_all, int V, float temperature, float top_p, uint32_t key0,
                   uint32_t key1, uint32_t position, uint32_t sample0, int *__restrict__ out_all,
@@ -89,6 +155,8 @@ __global__ void __launch_bounds__(SMP_THREADS, 1)
     };
     extern __shared__ float pv[];  // [V] unnormalised probabilities
     __shared__ float red[SMP_THREADS / 32];
+    __shared__ float3 red3[SMP_THREADS / 32];
+    __shared__ float3 bc3[2];
     __shared__ float wtot[SMP_THREADS / 32];
     __shared__ float bc[2];
     __shared__ int tok;
@@ -123,21 +191,35 @@ __global__ void __launch_bounds__(SMP_THREADS, 1)
     uint32_t lo = 0, hi = __float_as_uint(1.0f);
     float kept = 0.f;
     bool have = false;
-    while (lo < hi) {
-        const uint32_t mid = lo + (hi - lo + 1) / 2;
-        float s = 0.f;
-        for (int i = tid; i < V; i += SMP_THREADS) {
-            const float p = pv[i];
-            s += __float_as_uint(p) >= mid ? p : 0.f;
-        }
-        const float mass = bsum(s, red, &bc[(lo ^ hi) & 1]);
-        if (mass >= target) {
-            lo = mid;
-            kept = mass;
-            have = true;
-        } else {
-            hi = mid - 1;
-        }
+    if (V <= SMP_REG * SMP_THREADS) {
+        float pr[SMP_REG];  // this thread's values in index order (zeros past the vocabulary add nothing)
+#pragma unroll
+        for (int k = 0; k < SMP_REG; ++k) pr[k] = tid + k * SMP_THREADS < V ? pv[tid + k * SMP_THREADS] : 0.f;
+        bisect(
+            lo, hi, target, kept, have,
+            [&](uint32_t m1, uint32_t ma, uint32_t mb, float &s1, float &sa, float &sb) {
+#pragma unroll
+                for (int k = 0; k < SMP_REG; ++k) {
+                    const uint32_t u = __float_as_uint(pr[k]);
+                    if (u >= m1) s1 += pr[k];
+                    if (u >= ma) sa += pr[k];
+                    if (u >= mb) sb += pr[k];
+                }
+            },
+            red3, bc3);
+    } else {
+        bisect(
+            lo, hi, target, kept, have,
+            [&](uint32_t m1, uint32_t ma, uint32_t mb, float &s1, float &sa, float &sb) {
+                for (int i = tid; i < V; i += SMP_THREADS) {
+                    const float p = pv[i];
+                    const uint32_t u = __float_as_uint(p);
+                    if (u >= m1) s1 += p;
+                    if (u >= ma) sa += p;
+                    if (u >= mb) sb += p;
+                }
+            },
+            red3, bc3);
     }
     if (!have) {  // lo never moved: every token is kept
         float s = 0.f;

@@ -245,6 +245,8 @@ lf_status lf_debug_skip_arrival(lf_engine *e, int cta);
  * The slot of a lane-sum op (REDUCE) holds, on the CTAs that sum a chunk
  * (cta < d_model / 32), [wait start, publish time, ns waiting for the
  * partials, ns copying them, 0, 0]; it stays zero on the other CTAs.
+ * A launch of several steps (lf_generate) leaves its
+ * last step's record: every step rewrites the same slots as its ops end.
  * lf_debug_read_trace copies the last step's record: n_words must equal
  * n_sm * n_ops * LF_TRACE_WORDS (lf_engine_info [0] and [6]); `ops`
  * (nullable, n_ops entries) receives the op list, each entry
