@@ -555,10 +555,9 @@ lf_status enqueue_batch_step(lf_engine *e, BatchState &b, cudaStream_t main) {
         a.ldy = s.V;
         gs = lf::gemv_tc(wt(4 * L), h, a, main);
     }
-    if (gs == LF_OK) {
-        ba_argmax<<<B, 1024, 0, main>>>(b.logits, s.V, b.am);
-        ba_bump<<<1, 1, 0, main>>>(b.d_pos);
-    }
+    // (the argmax runs outside the graph, for lf_batch_step: the generation
+    // loop draws its tokens from the logits with the sampler)
+    if (gs == LF_OK) ba_bump<<<1, 1, 0, main>>>(b.d_pos);
     destroy();
     if (gs != LF_OK) return gs;
     return cudaGetLastError() == cudaSuccess ? LF_OK : LF_ERR_CUDA;
@@ -703,6 +702,10 @@ extern "C" lf_status lf_batch_step(lf_engine *e, const int32_t *tokens, float *l
     cudaStream_t st = e->stream;
     cudaError_t err = cudaMemcpyAsync(b.tok, tokens, (size_t)b.B * sizeof(int32_t), cudaMemcpyHostToDevice, st);
     if (err == cudaSuccess) err = cudaGraphLaunch(b.graph, st);
+    if (err == cudaSuccess && argmax) {
+        ba_argmax<<<b.B, 1024, 0, st>>>(b.logits, s.V, b.am);
+        err = cudaGetLastError();
+    }
     if (err == cudaSuccess && logits)
         err = cudaMemcpyAsync(logits, b.logits, (size_t)b.B * s.V * sizeof(float), cudaMemcpyDeviceToHost, st);
     if (err == cudaSuccess && argmax)
