@@ -881,15 +881,16 @@ struct Attention {
     // (plus, when cur, this step's own key and value), for its GL q heads:
     // the warp's (acc, m, l) partial per q head goes to p.apart.
     //
-    // Scores: S^T = K_tile q^T on the MMA, keys as M (two 16-row blocks: row
-    // r of block b is key 4 (r % 8) + 2 b + r / 8 of the tile, so that the 8
-    // rows of a matrix load come from the 8 key groups),
-    // the q heads as N (zero columns past GL), head_dim as K; q enters as
-    // FP16 hi + lo so that the products keep about fp32 precision (the keys
-    // are FP16 in the cache).  P.V: O^T += V^T P^T, head_dim as M (MD blocks
-    // of 16), the q heads as N, keys as K, P again as hi + lo.  Online softmax
-    // over the tiles in registers: lane 4g + t holds q heads 2t and 2t + 1
-    // of every score and accumulator fragment.
+    // Scores: S^T = K_tile q^T on the MMA with keys as M, the q heads as N
+    // (zero columns past GL) and head_dim as K.  The keys form two 16-row
+    // blocks: row r of block b is key 4 (r % 8) + 2 b + r / 8 of the tile,
+    // so that the 8 rows of a matrix load come from the 8 key groups.  q
+    // enters as FP16 hi + lo so that the products keep about fp32 precision
+    // (the keys are FP16 in the cache).  P.V: O^T += V^T P^T with head_dim as
+    // M (MD blocks of 16), the q heads as N and the keys as K (the same two
+    // blocks), P again as hi + lo.  Online softmax over the tiles in
+    // registers: lane 4g + t holds q heads 2t and 2t + 1 of every score and
+    // accumulator fragment.
     __device__ void head(int l, int lane_id, int g, int a, int n_prev, int T, int T_eff, bool cur) {
         const int GL = p.GL, gq = lane >> 2, t4 = lane & 3;
         const bool hv0 = 2 * t4 < GL, hv1 = 2 * t4 + 1 < GL;
