@@ -37,7 +37,7 @@ def test_step_bytes(name):
 
 
 def test_full_shape_headline_figures():
-    # the survey's figures: 4.4148 GB of streamed weights, 4.478 GB per step at position 512
+    # 2,207,379,456 streamed FP16 parameters (4.4148 GB) and 4.478 GB per step at position 512
     assert weight_bytes(synth.FULL) == 4_414_758_912
     assert bench.algorithmic_bytes(synth.FULL, 512) == 4_477_796_352
 
