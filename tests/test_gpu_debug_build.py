@@ -71,18 +71,21 @@ def test_release_library_refuses_the_debug_calls():
 
 
 @pytest.mark.slow
-def test_full_shape_step_with_every_check_on():
+@pytest.mark.parametrize("fill", [1030, 4000])
+def test_full_shape_step_with_every_check_on(fill):
+    # past the 1024-key window, every lane and op of the real plan; at 4000
+    # a CTA's share of a full-attention layer spans seven 32-key tiles
     from decode_persistent_sm_gb300 import Engine
     shape = synth.FULL
     blob = synth.make_weights(shape, 1)
-    kv = synth.make_kv(shape, 1, 1030)
+    kv = synth.make_kv(shape, 1, fill)
     toks = synth.make_tokens(53, 2, shape.vocab)
     orc = oracle.Oracle(shape, blob)
-    orc.load_kv(kv, 1030)
+    orc.load_kv(kv, fill)
     with Engine.from_shape(shape, debug=True) as eng:
         eng.load_weights(blob)
-        eng.load_kv(kv, 1030)
-        for t in toks:  # past the 1024-key window, every lane and op of the real plan
+        eng.load_kv(kv, fill)
+        for t in toks:
             got, am = eng.decode_step(int(t))
             ref = orc.step(int(t))
             assert note(got, ref, am) <= 1e-2 and am == oracle.argmax(ref)
