@@ -29,6 +29,7 @@ _SIGS = {
     "lf_decode_step": (_ci, [_vp, _i32, _vp, _vp]),
     "lf_matmul_f16": (_ci, [_vp, _vp, _vp, _ci, _ci, _ci, _vp]),
     "lf_matmul_f16_async": (_ci, [_vp, _vp, _vp, _ci, _ci, _ci, _vp, _vp]),
+    "lf_matmul_add_f16": (_ci, [_vp, _vp, _vp, _vp, _ci, _ci, _ci, _vp]),
     "lf_prefill_batched": (_ci, [_vp, _vp, _ci, _vp, _vp]),
     "lf_set_prefill_attention": (_ci, [_vp, _ci]),
     "lf_generate": (_ci, [_vp, _i32, _ci, _vp, _vp]),
@@ -136,6 +137,13 @@ def matmul_f16(a_ptr: int, b_ptr: int, c_ptr: int, m: int, n: int, k: int, strea
     FP16 a, b row-major, fp32 c); waits for the stream."""
     lib = load_library()
     _check("lf_matmul_f16", lib.lf_matmul_f16(a_ptr, b_ptr, c_ptr, int(m), int(n), int(k), stream))
+
+
+def matmul_add_f16(a_ptr: int, b_ptr: int, c_in_ptr: int, c_ptr: int, m: int, n: int, k: int,
+                   stream: Optional[int] = None):
+    """c = c_in + a . b^T (lf_matmul_add_f16; c_in may equal c); waits for the stream."""
+    lib = load_library()
+    _check("lf_matmul_add_f16", lib.lf_matmul_add_f16(a_ptr, b_ptr, c_in_ptr, c_ptr, int(m), int(n), int(k), stream))
 
 
 def matmul_f16_async(a_ptr: int, b_ptr: int, c_ptr: int, m: int, n: int, k: int, err_ptr: int,

@@ -37,6 +37,8 @@ struct lf_engine {
     uint32_t *pf_err = nullptr;  // device word: GEMM wait timeouts during a batched prefill
     __half *pf_vt = nullptr;     // batched prefill: V caches transposed for the tensor-core attention (owned separately)
     int pf_tc_attention = 1;     // batched prefill attention on the tensor cores (head_dim 128)
+    cudaStream_t pf_side = nullptr;     // batched prefill: second stream (odd sub-blocks), created on first use
+    std::vector<cudaEvent_t> pf_ev;     // batched prefill: fork, join, one per sub-block (its residual written)
     lf::BatchState *batch = nullptr;  // lf_batch_begin .. lf_batch_end (owned separately)
     void *wtile = nullptr;            // batched decode: the GEMVs' weights in their streaming layout
     bool wtile_ok = false;            // wtile matches the loaded weights

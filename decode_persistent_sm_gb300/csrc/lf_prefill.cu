@@ -5,11 +5,25 @@
 // vector, so the prompt's forward needs no lanes: sub-block s reads
 // x(s) = e + sum_{u <= s-1-2d} P[u], where P[u] is the full projection output
 // of sub-block u (the lanes' partials summed).  Each sub-block runs over all
-// n positions at once: the arriving partial added and the RMSNorm to FP16 in
-// one kernel, one tensor-core GEMM against the weight matrix in its file
-// layout with RoPE + the KV-cache append (attention) or SwiGLU (FFN) in its
-// epilogue, causal windowed attention over the cache, and a second GEMM whose
-// output is P[s]; P[s] joins the residual 2d + 1 sub-blocks later.
+// n positions at once: the RMSNorm of x(s) to FP16, one tensor-core GEMM
+// against the weight matrix in its file layout with RoPE + the KV-cache
+// append (attention) or SwiGLU (FFN) in its epilogue, causal windowed
+// attention over the cache, and a second GEMM whose product P[s] joins the
+// residual 2d + 1 sub-blocks later.  That GEMM adds P[s] in its epilogue:
+// it reads x(s + 2d) and writes x(s + 2d + 1) = x(s + 2d) + P[s], so P never
+// reaches memory.  x(s) lives in slot max(0, s - 2d) mod (2d + 2): x(0) ..
+// x(2d) are all the embedding (slot 0), and the 2d + 2 residuals live at
+// once (x(s) .. x(s + 2d + 1) while sub-block s runs) take distinct slots.
+//
+// Sub-block s + 1 reads x(s + 1), which does not contain P[s] (d >= 1), so
+// consecutive sub-blocks overlap: even sub-blocks run on the caller's stream,
+// odd ones on a second stream, each with its own scratch.  Sub-block s waits
+// for the GEMM that wrote x(s) (sub-block s - 1 - 2d) before its norm, and
+// for sub-block s - 1's projection GEMM before its own, which reads the
+// residual that one wrote; a slot is overwritten only after both readers of
+// its previous residual (a norm and a projection GEMM) have run.  The norm
+// (memory-bound) then runs beside a GEMM (tensor-bound), and a kernel's
+// last, partial wave of CTAs beside the next sub-block's kernels.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -33,12 +47,6 @@ __global__ void pf_embed(const __half *__restrict__ emb, const int *__restrict__
     const size_t row = blockIdx.x;
     const __half *e = emb + (size_t)tok[row] * D;
     for (int c = threadIdx.x; c < D; c += blockDim.x) x[row * D + c] = __half2float(e[c]);
-}
-
-// x[i] += p[i] over n floats
-__global__ void pf_add(float *__restrict__ x, const float *__restrict__ p, size_t n) {
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
-        x[i] += p[i];
 }
 
 // vt[z][d][p] = vc[z][p][d] for positions p < P (32 x 32 tiles through shared memory).
@@ -137,21 +145,38 @@ extern "C" lf_status lf_set_prefill_attention(lf_engine *e, int tensor_cores) {
     return LF_OK;
 }
 
-extern "C" lf_status lf_matmul_f16(const void *a_device, const void *b_device, float *c_device, int m, int n, int k,
-                                   void *cuda_stream) {
+namespace {
+
+// lf_matmul_f16 and lf_matmul_add_f16: c (= c_in when not null) + a b^T, waited for.
+lf_status matmul_sync(const void *a_device, const void *b_device, const float *c_in, float *c_device, int m, int n,
+                      int k, void *cuda_stream) {
     if (!a_device || !b_device || !c_device || m < 1 || n < 1 || k < 64 || k % 64) return LF_ERR_INVALID_ARG;
     uint32_t *err = matmul_err_word();
     if (!err) return LF_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     if (cudaMemsetAsync(err, 0, sizeof(uint32_t), s) != cudaSuccess) return LF_ERR_CUDA;
-    lf_status st = lf::tc_gemm_f16(static_cast<const __half *>(a_device), static_cast<const __half *>(b_device),
-                                   c_device, m, n, k, n, err, kGemmTimeoutNs, s);
+    const __half *a = static_cast<const __half *>(a_device), *b = static_cast<const __half *>(b_device);
+    lf_status st = c_in ? lf::tc_gemm_add_f16(a, b, c_in, c_device, m, n, k, n, err, kGemmTimeoutNs, s)
+                        : lf::tc_gemm_f16(a, b, c_device, m, n, k, n, err, kGemmTimeoutNs, s);
     if (st != LF_OK) return st;
     uint32_t h = 0;
     if (cudaMemcpyAsync(&h, err, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess)
         return LF_ERR_CUDA;
     return h ? LF_ERR_TIMEOUT : LF_OK;
+}
+
+}  // namespace
+
+extern "C" lf_status lf_matmul_f16(const void *a_device, const void *b_device, float *c_device, int m, int n, int k,
+                                   void *cuda_stream) {
+    return matmul_sync(a_device, b_device, nullptr, c_device, m, n, k, cuda_stream);
+}
+
+extern "C" lf_status lf_matmul_add_f16(const void *a_device, const void *b_device, const float *c_in_device,
+                                       float *c_device, int m, int n, int k, void *cuda_stream) {
+    if (!c_in_device) return LF_ERR_INVALID_ARG;
+    return matmul_sync(a_device, b_device, c_in_device, c_device, m, n, k, cuda_stream);
 }
 
 extern "C" lf_status lf_matmul_f16_async(const void *a_device, const void *b_device, float *c_device, int m, int n,
@@ -316,8 +341,9 @@ size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 // Scratch of one batched prefill of M positions, carved from one allocation.
 struct PfBufs {
     int *tok;
-    float *x, *ring, *qf, *gu;
-    __half *h, *o, *u, *q16;
+    float *xs;  // 2d + 2 residual slots of M x D
+    float *qf[2], *gu[2];  // per stream (sub-block parity), like the rest
+    __half *h[2], *o[2], *u[2], *q16[2];
     size_t bytes;
 };
 
@@ -325,7 +351,7 @@ struct PfBufs {
 // when SwiGLU is not fused into the gate/up GEMM.
 PfBufs carve(uint8_t *base, const lf::Shape &s, int M, bool need_qf, bool need_gu) {
     const size_t D = s.D, QD = (size_t)s.NQ * s.DH, F = s.F;
-    const size_t R = 2 * (size_t)s.delay + 1;
+    const size_t R = 2 * (size_t)s.delay + 2;
     PfBufs b{};
     size_t at = 0;
     auto take = [&](size_t bytes) {
@@ -334,14 +360,15 @@ PfBufs carve(uint8_t *base, const lf::Shape &s, int M, bool need_qf, bool need_g
         return p;
     };
     b.tok = reinterpret_cast<int *>(take(M * sizeof(int)));
-    b.x = reinterpret_cast<float *>(take(M * D * 4));
-    b.ring = reinterpret_cast<float *>(take(R * M * D * 4));
-    b.qf = need_qf ? reinterpret_cast<float *>(take(M * QD * 4)) : nullptr;
-    b.gu = need_gu ? reinterpret_cast<float *>(take(M * 2 * F * 4)) : nullptr;
-    b.h = reinterpret_cast<__half *>(take(M * std::max(D, F) * 2));
-    b.o = reinterpret_cast<__half *>(take(M * QD * 2));
-    b.u = reinterpret_cast<__half *>(take(M * F * 2));
-    b.q16 = reinterpret_cast<__half *>(take(M * QD * 2));
+    b.xs = reinterpret_cast<float *>(take(R * M * D * 4));
+    for (int p = 0; p < 2; ++p) {
+        b.qf[p] = need_qf ? reinterpret_cast<float *>(take(M * QD * 4)) : nullptr;
+        b.gu[p] = need_gu ? reinterpret_cast<float *>(take(M * 2 * F * 4)) : nullptr;
+        b.h[p] = reinterpret_cast<__half *>(take(M * std::max(D, F) * 2));
+        b.o[p] = reinterpret_cast<__half *>(take(M * QD * 2));
+        b.u[p] = reinterpret_cast<__half *>(take(M * F * 2));
+        b.q16[p] = reinterpret_cast<__half *>(take(M * QD * 2));
+    }
     b.bytes = at;
     return b;
 }
@@ -349,6 +376,20 @@ PfBufs carve(uint8_t *base, const lf::Shape &s, int M, bool need_qf, bool need_g
 lf_status pf_fail(lf_engine *e) {
     e->poisoned = LF_ERR_CUDA;
     return LF_ERR_CUDA;
+}
+
+// The side stream and the events of the two-stream schedule (created once per engine).
+bool pf_streams(lf_engine *e, int n_sub) {
+    if (!e->pf_side && cudaStreamCreateWithFlags(&e->pf_side, cudaStreamNonBlocking) != cudaSuccess) {
+        e->pf_side = nullptr;
+        return false;
+    }
+    while ((int)e->pf_ev.size() < n_sub + 2) {
+        cudaEvent_t v;
+        if (cudaEventCreateWithFlags(&v, cudaEventDisableTiming) != cudaSuccess) return false;
+        e->pf_ev.push_back(v);
+    }
+    return true;
 }
 
 }  // namespace
@@ -363,7 +404,7 @@ extern "C" lf_status lf_prefill_batched(lf_engine *e, const int32_t *tokens, int
         if (tokens[i] < 0 || tokens[i] >= s.V) return LF_ERR_INVALID_ARG;
     if (!e->blob) return LF_ERR_OOM;
     const int D = s.D, DH = s.DH, NQ = s.NQ, NKV = s.NKV, F = s.F, L = s.L, QD = NQ * DH;
-    const int R = 2 * s.delay + 1, M = n, p0 = e->pos;
+    const int M = n, p0 = e->pos;
     if (D % 64 || QD % 64 || F % 64 || (DH != 128 && DH != 32) || D > 4 * kNormV * kNormThreads)
         return LF_ERR_UNSUPPORTED;
     cudaStream_t st = e->stream;
@@ -411,24 +452,40 @@ extern "C" lf_status lf_prefill_batched(lf_engine *e, const int32_t *tokens, int
     if (cudaMemcpyAsync(b.tok, tokens, (size_t)M * sizeof(int), cudaMemcpyHostToDevice, st) != cudaSuccess ||
         cudaMemsetAsync(e->pf_err, 0, sizeof(uint32_t), st) != cudaSuccess)
         return pf_fail(e);
-    pf_embed<<<M, 256, 0, st>>>(e->emb, b.tok, b.x, D);
-
     const float scale = (float)(1.0 / std::sqrt((double)DH)), eps = e->cfg.rms_eps;
     const size_t MD = (size_t)M * D;
+    const int d2 = 2 * s.delay;
+    auto X = [&](int sb) { return b.xs + (size_t)(std::max(0, sb - d2) % (d2 + 2)) * MD; };  // x(sb)
+    pf_embed<<<M, 256, 0, st>>>(e->emb, b.tok, X(0), D);
+    if (!pf_streams(e, 2 * L)) return pf_fail(e);
+    cudaStream_t side = e->pf_side;
+    cudaEvent_t *ev = e->pf_ev.data();  // [0] fork, [1] join, [2 + sb] sub-block sb's residual written
+    if (cudaEventRecord(ev[0], st) != cudaSuccess || cudaStreamWaitEvent(side, ev[0], 0) != cudaSuccess)
+        return pf_fail(e);
+    // every exit from here on first makes the caller's stream wait for the side stream's work
+    auto stop = [&](lf_status gs) {
+        if (cudaEventRecord(ev[1], side) != cudaSuccess || cudaStreamWaitEvent(st, ev[1], 0) != cudaSuccess)
+            gs = LF_ERR_CUDA;
+        return gs == LF_ERR_CUDA ? pf_fail(e) : gs;
+    };
+
     for (int sb = 0; sb < 2 * L; ++sb) {
-        const int l = sb / 2, ua = sb - 1 - 2 * s.delay;
-        // the partial of sub-block ua arrives in the residual now, just before the norm that reads it
-        const int n_arrive = ua >= 0 ? 1 : 0;
+        const int l = sb / 2, p = sb % 2, u = sb - 1 - d2;
+        cudaStream_t ss = p == 0 ? st : side;
         const __half *lw = e->blob + s.off_layer0 + (long long)l * s.per_layer;
-        float *P = b.ring + (size_t)(sb % R) * MD;
+        float *xin = X(sb + d2), *xout = X(sb + d2 + 1);  // the projection GEMM: xout = xin + P[sb]
+        __half *h = b.h[p];
+        // x(sb) is complete once sub-block u's projection GEMM is (x(0) .. x(2d) are the embedding)
+        if (u >= 0 && cudaStreamWaitEvent(ss, ev[2 + u], 0) != cudaSuccess) return stop(LF_ERR_CUDA);
+        pf_addnorm<<<M, kNormThreads, 0, ss>>>(X(sb), nullptr, MD, 0, 0, 1,
+                                               e->gains + (size_t)(p == 0 ? l : L + l) * D, h, D, eps);
         lf_status gs;
-        if (sb % 2 == 0) {
-            pf_addnorm<<<M, kNormThreads, 0, st>>>(b.x, b.ring, MD, ua, n_arrive, R, e->gains + (size_t)l * D, b.h,
-                                                   D, eps);
+        const __half *a2;  // the operand of the projection GEMM
+        if (p == 0) {
             // QKV projection with RoPE and the KV-cache append in the GEMM epilogue
             lf::QkvEpi qe;
-            qe.q16 = b.q16;
-            qe.qf = tc_attn ? nullptr : b.qf;
+            qe.q16 = b.q16[p];
+            qe.qf = tc_attn ? nullptr : b.qf[p];
             qe.kc = e->kc;
             qe.vc = e->vc;
             qe.vt = tc_attn ? e->pf_vt : nullptr;
@@ -443,42 +500,49 @@ extern "C" lf_status lf_prefill_batched(lf_engine *e, const int32_t *tokens, int
             qe.l = l;
             qe.HKV_L = s.HKV_L;
             qe.ctx = s.ctx;
-            gs = lf::tc_gemm_qkv_rope_f16(b.h, lw + s.o_wq, M, D, qe, e->pf_err, kGemmTimeoutNs, st);
-            if (gs != LF_OK) return gs == LF_ERR_CUDA ? pf_fail(e) : gs;
+            gs = lf::tc_gemm_qkv_rope_f16(h, lw + s.o_wq, M, D, qe, e->pf_err, kGemmTimeoutNs, ss);
+            if (gs != LF_OK) return stop(gs);
             const dim3 ag((M + PF_QB - 1) / PF_QB, NQ);
             if (tc_attn) {
-                lf::TcAttnArgs ta{M, p0, NQ, s.HQ_L, s.GL, s.HKV_L, L, l, s.ctx, e->cfg.swa_window[l], scale, b.o, QD};
-                gs = lf::pf_attention_tc(b.q16, e->kc, e->pf_vt, ta, s.NL, e->pf_err, kGemmTimeoutNs, st);
-                if (gs != LF_OK) return gs == LF_ERR_CUDA ? pf_fail(e) : gs;
+                lf::TcAttnArgs ta{M, p0, NQ, s.HQ_L, s.GL, s.HKV_L, L, l, s.ctx, e->cfg.swa_window[l], scale, b.o[p],
+                                  QD};
+                gs = lf::pf_attention_tc(b.q16[p], e->kc, e->pf_vt, ta, s.NL, e->pf_err, kGemmTimeoutNs, ss);
+                if (gs != LF_OK) return stop(gs);
             } else if (DH == 128)
-                pf_attention<128><<<ag, 128, pf_attn_smem<128>(), st>>>(b.qf, e->kc, e->vc, b.o, M, p0, NQ, s.HQ_L,
-                                                                         s.GL, s.HKV_L, L, l, s.ctx,
+                pf_attention<128><<<ag, 128, pf_attn_smem<128>(), ss>>>(b.qf[p], e->kc, e->vc, b.o[p], M, p0, NQ,
+                                                                         s.HQ_L, s.GL, s.HKV_L, L, l, s.ctx,
                                                                          e->cfg.swa_window[l], scale);
             else
-                pf_attention<32><<<ag, 128, pf_attn_smem<32>(), st>>>(b.qf, e->kc, e->vc, b.o, M, p0, NQ, s.HQ_L,
-                                                                       s.GL, s.HKV_L, L, l, s.ctx,
+                pf_attention<32><<<ag, 128, pf_attn_smem<32>(), ss>>>(b.qf[p], e->kc, e->vc, b.o[p], M, p0, NQ,
+                                                                       s.HQ_L, s.GL, s.HKV_L, L, l, s.ctx,
                                                                        e->cfg.swa_window[l], scale);
-            gs = lf::tc_gemm_f16(b.o, lw + s.o_wo, P, M, D, QD, D, e->pf_err, kGemmTimeoutNs, st);
+            a2 = b.o[p];
         } else {
-            pf_addnorm<<<M, kNormThreads, 0, st>>>(b.x, b.ring, MD, ua, n_arrive, R, e->gains + (size_t)(L + l) * D,
-                                                   b.h, D, eps);
             if (fused_swiglu) {
-                gs = lf::tc_gemm_swiglu_f16(b.h, lw + s.o_wg, b.u, M, F, D, F, e->pf_err, kGemmTimeoutNs, st);
+                gs = lf::tc_gemm_swiglu_f16(h, lw + s.o_wg, b.u[p], M, F, D, F, e->pf_err, kGemmTimeoutNs, ss);
             } else {
-                gs = lf::tc_gemm_f16(b.h, lw + s.o_wg, b.gu, M, 2 * F, D, 2 * F, e->pf_err, kGemmTimeoutNs, st);
-                if (gs != LF_OK) return gs == LF_ERR_CUDA ? pf_fail(e) : gs;
+                gs = lf::tc_gemm_f16(h, lw + s.o_wg, b.gu[p], M, 2 * F, D, 2 * F, e->pf_err, kGemmTimeoutNs, ss);
+                if (gs != LF_OK) return stop(gs);
                 const size_t nf = (size_t)M * F;
-                pf_swiglu<<<(int)std::min<size_t>((nf + 255) / 256, 4096), 256, 0, st>>>(b.gu, b.u, F, nf);
+                pf_swiglu<<<(int)std::min<size_t>((nf + 255) / 256, 4096), 256, 0, ss>>>(b.gu[p], b.u[p], F, nf);
             }
-            if (gs != LF_OK) return gs == LF_ERR_CUDA ? pf_fail(e) : gs;
-            gs = lf::tc_gemm_f16(b.u, lw + s.o_wd, P, M, D, F, D, e->pf_err, kGemmTimeoutNs, st);
+            if (gs != LF_OK) return stop(gs);
+            a2 = b.u[p];
         }
-        if (gs != LF_OK) return gs == LF_ERR_CUDA ? pf_fail(e) : gs;
+        // xin is sub-block sb - 1's output, and xout's slot held x(sb - 1), which that sub-block's norm
+        // read before its GEMM
+        if (sb > 0 && cudaStreamWaitEvent(ss, ev[2 + sb - 1], 0) != cudaSuccess) return stop(LF_ERR_CUDA);
+        gs = lf::tc_gemm_add_f16(a2, lw + (p == 0 ? s.o_wo : s.o_wd), xin, xout, M, D, p == 0 ? QD : F, D, e->pf_err,
+                                 kGemmTimeoutNs, ss);
+        if (gs != LF_OK) return stop(gs);
+        if (cudaEventRecord(ev[2 + sb], ss) != cudaSuccess) return stop(LF_ERR_CUDA);
     }
-    // drain for the last position: the partials not yet in its residual
-    float *xl = b.x + (size_t)(M - 1) * D;
-    for (int u = std::max(0, 2 * L - 1 - 2 * s.delay); u < 2 * L; ++u)
-        pf_add<<<(D + 255) / 256, 256, 0, st>>>(xl, b.ring + (size_t)(u % R) * MD + (size_t)(M - 1) * D, D);
+    {
+        const lf_status js = stop(LF_OK);  // the caller's stream waits for the side stream (the last sub-block)
+        if (js != LF_OK) return js;
+    }
+    // the last sub-block's GEMM wrote x(2L + 2d) = e + every P: the last position's row feeds the LM head
+    const float *xl = X(2 * L + d2) + (size_t)(M - 1) * D;
     pf_lmhead<<<608, 256, D * sizeof(float), st>>>(xl, e->gains + (size_t)2 * L * D, e->blob + s.off_lm, e->logits,
                                                    D, s.V, eps);
     pf_argmax<<<1, 1024, 0, st>>>(e->logits, s.V, reinterpret_cast<int *>(e->status));

@@ -240,6 +240,8 @@ void lf_destroy(lf_engine *e) {
     if (e->trace) cudaFree(e->trace);
     if (e->pf_mem) cudaFree(e->pf_mem);
     if (e->pf_vt) cudaFree(e->pf_vt);
+    for (cudaEvent_t v : e->pf_ev) cudaEventDestroy(v);
+    if (e->pf_side) cudaStreamDestroy(e->pf_side);
     if (e->h_status) cudaFreeHost(e->h_status);
     delete e;
 }

@@ -9,6 +9,9 @@
 // epilogue writes U[M][F] = FP16(silu(gate) * up) and the fp32 gate/up
 // product never reaches memory.
 //
+// Residual variant: C = Cin + A * B^T, the fp32 product added to another fp32
+// matrix of the same layout in the epilogue (Cin may be C itself).
+//
 // QKV variant: the epilogue applies RoPE to the q and k columns (a 256-column
 // tile holds whole heads, so both columns of each pair are in the thread's
 // row) and writes q in FP16 (and fp32 on request), k and v into the FP16
@@ -85,11 +88,12 @@ enum GemmMode : int { GEMM_F32 = 0, GEMM_SWIGLU = 1, GEMM_QKV = 2 };
 // GEMM_SWIGLU: N = 2F is the row count of B, the grid of tiles is M x F/128
 // and C is the FP16 U[M][F] (row stride ldc halves); GEMM_QKV: the epilogue
 // rotates q and k (RoPE at position p0 + row) and writes q and the K/V cache
-// rows (qe); otherwise C is fp32.
+// rows (qe); otherwise C is fp32, and with Cin (fp32, row stride ldc) not
+// null each element is stored as Cin + the product.
 template <int kMode>
 __global__ void __launch_bounds__(TG_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, void *C,
-                   int M, int N, int K, int ldc, uint32_t *err, unsigned long long timeout_ns,
+                   const float *Cin, int M, int N, int K, int ldc, uint32_t *err, unsigned long long timeout_ns,
                    const __grid_constant__ QkvEpi qe) {
     constexpr bool kSwiGLU = kMode == GEMM_SWIGLU;
     extern __shared__ __align__(1024) uint8_t tg_raw[];
@@ -97,7 +101,6 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
     TgShared &S = *reinterpret_cast<TgShared *>(tiles + (size_t)TG_STAGES * STAGE_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int mt = (M + BM - 1) / BM, nt = kSwiGLU ? N / BN : (N + BN - 1) / BN, ntiles = mt * nt, nk = K / BK;
-    const uint64_t deadline = global_timer_ns() + timeout_ns;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < TG_STAGES; ++s) {
@@ -114,6 +117,7 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
     }
+    const uint64_t deadline = global_timer_ns() + timeout_ns;
     if (warp == 1) tc_alloc(&S.tmem_base, TMEM_COLS);
     tc_fence_before();
     __syncthreads();
@@ -288,14 +292,25 @@ __global__ void __launch_bounds__(TG_THREADS, 1)
                 const int col = n * BN + c0;
                 if (row < M && col < N) {
                     float *dst = static_cast<float *>(C) + (size_t)row * ldc + col;
+                    const float *src = Cin ? Cin + (size_t)row * ldc + col : nullptr;
                     if (col + 32 <= N && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
+                        if (src) {  // dst and src share the row stride, so src is 16-byte aligned too
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4) {
+                                const float4 c = *reinterpret_cast<const float4 *>(src + i);
+                                v[i] = c.x + v[i];
+                                v[i + 1] = c.y + v[i + 1];
+                                v[i + 2] = c.z + v[i + 2];
+                                v[i + 3] = c.w + v[i + 3];
+                            }
+                        }
 #pragma unroll
                         for (int i = 0; i < 32; i += 4)
                             *reinterpret_cast<float4 *>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
                     } else {
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            if (col + i < N) dst[i] = v[i];
+                            if (col + i < N) dst[i] = src ? src[i] + v[i] : v[i];
                     }
                 }
             }
@@ -358,8 +373,8 @@ size_t tc_gemm_smem_bytes() { return TG_SMEM; }
 namespace {
 
 template <int kMode>
-lf_status launch(const __half *A, const __half *B, void *C, int M, int N, int K, int ldc, uint32_t *err,
-                 unsigned long long timeout_ns, cudaStream_t stream, const QkvEpi &qe = QkvEpi()) {
+lf_status launch(const __half *A, const __half *B, void *C, const float *Cin, int M, int N, int K, int ldc,
+                 uint32_t *err, unsigned long long timeout_ns, cudaStream_t stream, const QkvEpi &qe = QkvEpi()) {
     constexpr bool kSwiGLU = kMode == GEMM_SWIGLU;
     CUtensorMap ma, mb;
     if (!make_map(&ma, A, M, K, BM) || !make_map(&mb, B, N, K, BH)) return LF_ERR_CUDA;
@@ -378,8 +393,8 @@ lf_status launch(const __half *A, const __half *B, void *C, int M, int N, int K,
             return LF_ERR_CUDA;
     }
     const int nt = kSwiGLU ? N / BN : (N + BN - 1) / BN, ntiles = ((M + BM - 1) / BM) * nt;
-    tc_gemm_kernel<kMode><<<ntiles < n_sm ? ntiles : n_sm, TG_THREADS, TG_SMEM, stream>>>(ma, mb, C, M, N, K, ldc,
-                                                                                        err, timeout_ns, qe);
+    tc_gemm_kernel<kMode><<<ntiles < n_sm ? ntiles : n_sm, TG_THREADS, TG_SMEM, stream>>>(ma, mb, C, Cin, M, N, K,
+                                                                                        ldc, err, timeout_ns, qe);
     return cudaGetLastError() == cudaSuccess ? LF_OK : LF_ERR_CUDA;
 }
 
@@ -391,7 +406,16 @@ lf_status tc_gemm_f16(const __half *A, const __half *B, float *C, int M, int N, 
                       unsigned long long timeout_ns, cudaStream_t stream) {
     if (!A || !B || !C || !err || M < 1 || N < 1 || K < BK || K % BK || ldc < N) return LF_ERR_INVALID_ARG;
     if (!aligned16(A) || !aligned16(B)) return LF_ERR_INVALID_ARG;
-    return launch<GEMM_F32>(A, B, C, M, N, K, ldc, err, timeout_ns, stream);
+    return launch<GEMM_F32>(A, B, C, nullptr, M, N, K, ldc, err, timeout_ns, stream);
+}
+
+lf_status tc_gemm_add_f16(const __half *A, const __half *B, const float *Cin, float *C, int M, int N, int K, int ldc,
+                          uint32_t *err, unsigned long long timeout_ns, cudaStream_t stream) {
+    if (!A || !B || !Cin || !C || !err || M < 1 || N < 1 || K < BK || K % BK || ldc < N) return LF_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B) || (reinterpret_cast<uintptr_t>(Cin) & 15) !=
+                                              (reinterpret_cast<uintptr_t>(C) & 15))
+        return LF_ERR_INVALID_ARG;
+    return launch<GEMM_F32>(A, B, C, Cin, M, N, K, ldc, err, timeout_ns, stream);
 }
 
 lf_status tc_gemm_swiglu_f16(const __half *A, const __half *Bgu, __half *U, int M, int F, int K, int ldu,
@@ -399,7 +423,7 @@ lf_status tc_gemm_swiglu_f16(const __half *A, const __half *Bgu, __half *U, int 
     if (!A || !Bgu || !U || !err || M < 1 || F < BH || F % BH || K < BK || K % BK || ldu < F || ldu % 8)
         return LF_ERR_INVALID_ARG;
     if (!aligned16(A) || !aligned16(Bgu) || !aligned16(U)) return LF_ERR_INVALID_ARG;
-    return launch<GEMM_SWIGLU>(A, Bgu, U, M, 2 * F, K, ldu, err, timeout_ns, stream);
+    return launch<GEMM_SWIGLU>(A, Bgu, U, nullptr, M, 2 * F, K, ldu, err, timeout_ns, stream);
 }
 
 lf_status tc_gemm_qkv_rope_f16(const __half *A, const __half *Wqkv, int M, int K, const QkvEpi &e, uint32_t *err,
@@ -411,7 +435,7 @@ lf_status tc_gemm_qkv_rope_f16(const __half *A, const __half *Wqkv, int M, int K
     if (!aligned16(A) || !aligned16(Wqkv) || !aligned16(e.q16) || !aligned16(e.kc) || !aligned16(e.vc))
         return LF_ERR_INVALID_ARG;
     __half *none = e.q16;  // C is not written in this mode
-    return launch<GEMM_QKV>(A, Wqkv, none, M, N, K, N, err, timeout_ns, stream, e);
+    return launch<GEMM_QKV>(A, Wqkv, none, nullptr, M, N, K, N, err, timeout_ns, stream, e);
 }
 
 }  // namespace lf

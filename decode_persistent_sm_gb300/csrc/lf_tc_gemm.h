@@ -15,6 +15,11 @@ namespace lf {
 lf_status tc_gemm_f16(const __half *A, const __half *B, float *C, int M, int N, int K, int ldc, uint32_t *err,
                       unsigned long long timeout_ns, cudaStream_t stream);
 
+// C = Cin + A * B^T: the same product added in the epilogue to Cin (fp32, the
+// layout of C and the same alignment modulo 16 bytes; Cin == C adds in place).
+lf_status tc_gemm_add_f16(const __half *A, const __half *B, const float *Cin, float *C, int M, int N, int K, int ldc,
+                          uint32_t *err, unsigned long long timeout_ns, cudaStream_t stream);
+
 // U[M][F] (FP16, row stride ldu halves, a multiple of 8) = silu(A Wg^T) * (A Wu^T)
 // elementwise, where Bgu = [Wg; Wu] holds the F gate rows then the F up rows
 // (each K long).  F a multiple of 128; the fp32 products stay in TMEM.

@@ -310,9 +310,12 @@ lf_status lf_decode_step_static_scratch(lf_engine *e, int32_t token, float *logi
  * advances the position by n; logits (host, vocab floats, nullable) and
  * argmax (host, nullable) receive the last position's result, which also
  * stays on the device (lf_get_logits_device / lf_get_argmax_device).
- * Scratch is allocated on first use and kept (about 0.14 MB per position
+ * Scratch is allocated on first use and kept (about 0.18 MB per position
  * at full shape, delay 2, plus a transposed copy of the V caches, the size
- * of the V cache, for the tensor-core attention).  Synchronous.  LF_ERR_INVALID_ARG for n < 1, a
+ * of the V cache, for the tensor-core attention), and so are a second
+ * stream and events: consecutive sub-blocks, which the delayed sum leaves
+ * independent, run on the engine's stream and that one, which the engine's
+ * stream waits for before the call returns.  Synchronous.  LF_ERR_INVALID_ARG for n < 1, a
  * NULL tokens array or a token outside [0, vocab); LF_ERR_CTX_OVERFLOW if
  * position + n > ctx_cap; LF_ERR_OOM when the resident weights or the
  * scratch could not be allocated; LF_ERR_TIMEOUT if a GEMM's device-side
@@ -338,6 +341,19 @@ lf_status lf_set_prefill_attention(lf_engine *e, int tensor_cores);
  * device-side wait ran out; LF_ERR_CUDA on a CUDA error. */
 lf_status lf_matmul_f16(const void *a_device, const void *b_device, float *c_device, int m, int n, int k,
                         void *cuda_stream);
+
+/* c[m][n] = c_in[m][n] + sum_k a[m][k] * b[n][k]: the product of
+ * lf_matmul_f16 added to c_in (fp32 DEVICE array of c's shape, row-major)
+ * as it leaves the accumulator, the residual update that follows every
+ * attention and FFN block (Blog, "Designing the architecture": a standard
+ * decoder; the batched prefill adds each block's output to the residual that
+ * way).  Each element is c_in + the fp32 product in one rounding; c_in may
+ * be c itself (added in place); c_in and c otherwise must not overlap.
+ * Sizes and alignment as lf_matmul_f16, and c_in and c have the same
+ * address modulo 16 bytes.  Synchronous on `cuda_stream`; errors as
+ * lf_matmul_f16. */
+lf_status lf_matmul_add_f16(const void *a_device, const void *b_device, const float *c_in_device, float *c_device,
+                            int m, int n, int k, void *cuda_stream);
 
 /* The same product, only enqueued on `cuda_stream` (no wait, no status read
  * back): for callers that chain several products, and for timing the kernel

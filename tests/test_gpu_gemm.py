@@ -1,5 +1,7 @@
-"""The tensor-core GEMM of the batched prefill (lf_matmul_f16), through the
-C ABI, against the exact product of the same FP16 inputs in fp64 on the CPU.
+"""The tensor-core GEMM of the batched prefill (lf_matmul_f16, and
+lf_matmul_add_f16, which adds the product to an fp32 matrix in its epilogue),
+through the C ABI, against the exact product of the same FP16 inputs in fp64
+on the CPU.
 
 fp32 accumulation of K FP16 products: the error bound used is
 K * 2^-23 * sum_k |a_mk b_nk| (a loose form of the standard accumulation
@@ -69,3 +71,47 @@ def test_async_matmul_equals_the_synchronous_call():
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert np.array_equal(tc.cpu().numpy(), c)  # same kernel, same summation order
+
+
+def run_add(m, n, k, seed, in_place=False):
+    import torch
+    from decode_persistent_sm_gb300 import matmul_add_f16
+    g = np.random.default_rng(seed)
+    a = g.standard_normal((m, k)).astype(np.float16)
+    b = (0.05 * g.standard_normal((n, k))).astype(np.float16)
+    r = (4.0 * g.standard_normal((m, n))).astype(np.float32)
+    ta = torch.from_numpy(a).cuda()
+    tb = torch.from_numpy(b).cuda()
+    tr = torch.from_numpy(r).cuda()
+    tc = tr if in_place else torch.full((m, n), float("nan"), dtype=torch.float32, device="cuda")
+    matmul_add_f16(ta.data_ptr(), tb.data_ptr(), tr.data_ptr(), tc.data_ptr(), m, n, k)
+    return a, b, r, tc.cpu().numpy()
+
+
+@pytest.mark.parametrize("m,n,k,in_place", [(128, 256, 64, False), (200, 300, 128, False), (257, 513, 192, True),
+                                            (130, 4096, 4096, False), (3, 37, 64, True)])
+def test_matmul_add_is_the_input_plus_the_exact_product(m, n, k, in_place):
+    # n = 37, 300, 513: the last column tile is partial (scalar epilogue path)
+    a, b, r, c = run_add(m, n, k, m + 3 * n + k, in_place)
+    a64, b64 = a.astype(np.float64), b.astype(np.float64)
+    ref = r.astype(np.float64) + a64 @ b64.T
+    # the product's accumulation bound plus one rounding of the sum
+    bound = k * 2.0 ** -23 * (np.abs(a64) @ np.abs(b64).T) + 2.0 ** -23 * np.abs(ref) + 1e-30
+    assert np.all(np.isfinite(c))
+    assert np.all(np.abs(c - ref) <= bound), f"max err/bound {np.max(np.abs(c - ref) / bound):.3f}"
+
+
+def test_matmul_add_equals_matmul_then_add():
+    # the epilogue adds the same fp32 product lf_matmul_f16 stores: one fp32 sum, bit for bit
+    a, b, c = run(200, 300, 256, 9)
+    a2, b2, r, c2 = run_add(200, 300, 256, 9)
+    assert np.array_equal(a, a2) and np.array_equal(b, b2)
+    assert np.array_equal(c2, (r + c).astype(np.float32))
+
+
+def test_matmul_add_rejects_a_null_input():
+    import ctypes
+    from decode_persistent_sm_gb300 import load_library
+    lib = load_library()
+    p = ctypes.c_void_p(256)
+    assert lib.lf_matmul_add_f16(p, p, None, p, 1, 1, 64, None) == 1
