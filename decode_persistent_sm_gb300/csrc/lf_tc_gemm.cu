@@ -45,7 +45,9 @@ constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTE
 constexpr int BH = BN / 2, BH_BYTES = BH * BK * 2;  // B is copied as two 128-row halves
 constexpr int TG_THREADS = 192;  // warp 0 copies, warp 1 MMA + TMEM owner, warps 2-5 epilogue
 constexpr uint32_t TMEM_COLS = 512;  // two 256-column accumulators
-constexpr int GROUP_M = 8;  // tile order: 8 M-tiles share each B tile while it is in L2
+// tile order: up to 32 M-tiles (every M-tile of a prompt of up to 4096 positions) take each B tile in
+// turn, so B is read from DRAM once while A (at most 4096 x 7168 FP16, 58 MB) stays in L2
+constexpr int GROUP_M = 32;
 constexpr size_t TG_SMEM = (size_t)TG_STAGES * STAGE_BYTES + 1024 + 256;
 
 struct TgShared {
