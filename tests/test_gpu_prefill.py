@@ -180,3 +180,45 @@ def test_tensor_core_attention_after_decode_steps():
     assert rel_l2(g1, g0) <= REL_L2 and a1 == a0
     for (l1, m1), (l0, m0) in zip(s1, s0):
         assert rel_l2(l1, l0) <= REL_L2 and m1 == m0
+
+
+def _small_hd128(delay):
+    # full width and head size (the tensor-core attention), 3 layers, small FFN and vocabulary
+    return synth.FULL.replace(n_layers=3, ffn_dim=1024, vocab=2048, dtp_delay=delay, swa_window=(0, 100, 40),
+                              ctx_cap=512)
+
+
+@pytest.mark.parametrize("shape_name,delay", [("tiny", 0), ("tiny", 2), ("hd128", 2)])
+def test_prefill_on_a_callers_stream_is_bitwise_the_default_streams(shape_name, delay):
+    # the pass runs its odd sub-blocks on a second stream that the engine's
+    # stream waits for: on a caller's stream it must give bit for bit what it
+    # gives on the default stream (same kernels, same fp32 summation order),
+    # the KV cache it leaves and the steps after it included
+    import torch
+    from decode_persistent_sm_gb300 import Engine
+    if shape_name == "tiny":
+        shape = synth.TINY.replace(dtp_delay=delay, n_layers=4, swa_window=(64, 0, 16, 0), ctx_cap=256)
+    else:
+        shape = _small_hd128(delay)
+    seed = 71 + delay
+    blob = synth.make_weights(shape, seed, gain_std=0.1)
+    tokens = synth.make_tokens(seed, 203, shape.vocab)
+    side = torch.cuda.Stream()
+    out = []
+    with Engine.from_shape(shape) as eng:
+        eng.load_weights(blob)
+        for stream in (None, side.cuda_stream):
+            eng.reset()
+            eng.set_stream(stream)
+            got, am = eng.prefill_batched(tokens[:200])
+            kv = [eng.read_kv(l, h, p) for l in range(shape.n_layers) for h in range(shape.n_kv_heads)
+                  for p in (0, 99, 199)]
+            steps = [eng.decode_step(int(t)) for t in tokens[200:]]
+            out.append((got, am, kv, steps))
+        eng.set_stream(None)
+    (g0, a0, kv0, s0), (g1, a1, kv1, s1) = out
+    assert np.array_equal(g0, g1) and a0 == a1
+    for (k0, v0), (k1, v1) in zip(kv0, kv1):
+        assert np.array_equal(k0, k1) and np.array_equal(v0, v1)
+    for (l0, m0), (l1, m1) in zip(s0, s1):
+        assert np.array_equal(l0, l1) and m0 == m1
