@@ -1,8 +1,10 @@
 // Batched prefill: the whole prompt in one pass per sub-block, GEMMs on the
 // tensor cores (lf_tc_gemm.cu), and the C-ABI entry points that expose it.
 //
-// With the delayed lane sum every lane's copy of the residual is the same
-// vector, so the prompt's forward needs no lanes: sub-block s reads
+// With the delayed lane sum (Blog, "Hiding overhead": each lane's partial joins
+// every lane's residual 2d + 1 sub-blocks after it was computed) every lane's
+// copy of the residual is the same vector, so the prompt's forward needs no
+// lanes: sub-block s reads
 // x(s) = e + sum_{u <= s-1-2d} P[u], where P[u] is the full projection output
 // of sub-block u (the lanes' partials summed).  Each sub-block runs over all
 // n positions at once: the RMSNorm of x(s) to FP16, one tensor-core GEMM
